@@ -1,0 +1,259 @@
+"""Seeded synthetic inputs for the DSA decode hot path.
+
+This module only draws random numbers and lays them out; it holds none of the
+method's arithmetic.  Number-format conversions of the drawn values (FP32 to
+bfloat16, FP32 to FP8 E4M3 for the pre-filled latent cache) are done by
+PyTorch's dtype casts.  Both the CUDA path and the CPU oracle consume exactly
+the byte arrays produced here.
+
+Shapes follow the pages' geometry ("glm5next_dsa/layer.rs": 512-wide latent
+in an FP8 paged cache shared by K and V, block tables per row, index heads x
+index head dim keys with a per-token gate, K-token verify rows with their own
+position / slot / seq_len / table row) and the five named workloads:
+
+=========  =====================================================================
+tiny       1 row, len 4096, 16 heads, index 8x64, topk 256, shuffled 64-block table
+single     1 row, len 32768, 64 heads, index 32x128, topk 2048, 512 of 1024 blocks
+batched    32 seqs x 1 row, len ~ U[8192, 65536], blocks of all seqs interleaved
+verify     8 seqs x 4 rows (lens base..base+3), base ~ U[65536, 131072]
+long       64 seqs x 1 row, len log-uniform [4096, 131072], 128 heads, index
+           64x128, pool twice the size needed with free blocks interleaved, and
+           the new row's latent written by the latent-write step first
+=========  =====================================================================
+
+Value distributions: latent ~ N(0,1) stored as fp8(x / kv_scale) with
+kv_scale 0.02; keys ~ N(0,1) bf16; q_idx ~ N(0,1) fp32; w ~ N(0,1) * Hi^-0.5;
+gate = sigmoid(N(0,1)) bf16; Q ~ 0.05 * N(0,1) bf16; kv_a ~ N(0,1) bf16;
+norm weight ~ N(1, 0.1^2) bf16; eps 1e-6; sm_scale = 256^-0.5.
+
+Draw order (one ``numpy.random.default_rng(seed)``): lens -> tables -> latent
+-> k -> gate -> q_idx -> w -> Q -> kv_a -> norm_w.  Unused pool blocks are
+filled with the FP8 NaN code 0x7F and a guard band after the key arena with
+the bf16 NaN 0x7FC0, so a stray read shows up as NaN in a parity check.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+LATENT_DIM = 512
+FP8_NAN = 0x7F
+BF16_NAN = 0x7FC0
+ARENA_GUARD_TOKENS = 256
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    seed: int
+    rows: int
+    group_rows: int            # consecutive rows that share one sequence (key arena base)
+    heads: int
+    index_heads: int
+    index_dim: int
+    topk: int
+    block_size: int
+    max_blocks: int            # entries per block-table row
+    bt_stride: int             # elements between block-table rows (0 = one shared row)
+    kv_scale: float
+    sm_scale: float
+    eps: float
+    seq_lens: np.ndarray       # [R] int32
+    positions: np.ndarray      # [R] uint32 (= seq_len - 1)
+    slots: np.ndarray          # [R] int64
+    block_table: np.ndarray    # [R or 1, max_blocks] int32 (-1 = no block)
+    pool: np.ndarray           # [nslots, 512] uint8 FP8 codes
+    idx_k: np.ndarray          # [T, D] uint16 bf16 bits (arena, all sequences)
+    idx_gate: np.ndarray       # [T] uint16 bf16 bits
+    idx_base: np.ndarray       # [R] int64 (row's sequence start in the arena)
+    q_idx: np.ndarray          # [R, Hi, D] float32
+    head_w: np.ndarray         # [R, Hi] float32
+    Q: np.ndarray              # [R, H, 512] uint16 bf16 bits
+    kv_a: np.ndarray | None    # [R, 512] uint16 bf16 bits (rows written by the latent write)
+    norm_w: np.ndarray | None  # [512] uint16 bf16 bits
+
+    @property
+    def max_len(self) -> int:
+        return int(self.seq_lens.max()) if self.rows else 0
+
+    @property
+    def latent_dim(self) -> int:
+        return LATENT_DIM
+
+    @property
+    def nslots(self) -> int:
+        return int(self.pool.shape[0])
+
+    @property
+    def has_write(self) -> bool:
+        return self.kv_a is not None
+
+    def algorithmic_bytes(self) -> int:
+        """Roofline bytes of one pass: keys + gate once per sequence over its
+        longest row, plus per row min(topk, len) latent rows and Q + out."""
+        total = 0
+        for g in range(0, self.rows, self.group_rows):
+            lmax = int(self.seq_lens[g:g + self.group_rows].max())
+            total += lmax * (2 * self.index_dim + 2)
+        for r in range(self.rows):
+            L = int(self.seq_lens[r])
+            total += min(self.topk, L) * LATENT_DIM + 2 * self.heads * LATENT_DIM * 2
+        return total
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _fp8_codes(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
+def make_workload(name: str, seed: int, *, seqs: int, rows_per_seq: int, len_kind: str,
+                  len_lo: int, len_hi: int, heads: int, index_heads: int, index_dim: int,
+                  topk: int, block_size: int = 64, pool_blocks: int | None = None,
+                  free_fraction: float = 0.0, shuffle_blocks: bool = True,
+                  with_write: bool = False, kv_scale: float = 0.02,
+                  sm_scale: float = 256 ** -0.5, eps: float = 1e-6,
+                  shared_table: bool = False) -> Workload:
+    """Draw one workload.  ``len_kind``: 'fixed' (len_lo), 'uniform' (integers
+    in [len_lo, len_hi]) or 'loguniform' (exp of uniform in [ln lo, ln hi],
+    floored).  A sequence's rows have lens base, base+1, ... (K-token verify).
+    ``pool_blocks`` defaults to the blocks needed / (1 - free_fraction)."""
+    rng = np.random.default_rng(seed)
+    rows = seqs * rows_per_seq
+
+    # ---- lens
+    if len_kind == "fixed":
+        base = np.full(seqs, len_lo, np.int64)
+    elif len_kind == "uniform":
+        base = rng.integers(len_lo, len_hi, size=seqs, endpoint=True).astype(np.int64)
+    elif len_kind == "loguniform":
+        u = rng.uniform(math.log(len_lo), math.log(len_hi), size=seqs)
+        base = np.floor(np.exp(u)).astype(np.int64)
+    else:
+        raise ValueError(len_kind)
+    seq_lens = np.zeros(rows, np.int32)
+    for s in range(seqs):
+        for j in range(rows_per_seq):
+            seq_lens[s * rows_per_seq + j] = base[s] + j
+    seq_tokens = base + (rows_per_seq - 1)          # tokens each sequence holds
+
+    # ---- tables
+    blocks_per_seq = [int(-(-int(t) // block_size)) for t in seq_tokens]
+    needed = sum(blocks_per_seq)
+    if pool_blocks is None:
+        pool_blocks = int(math.ceil(needed / (1.0 - free_fraction)))
+    assert pool_blocks >= needed
+    if shuffle_blocks:
+        phys = rng.permutation(pool_blocks)[:needed].astype(np.int64)
+    else:
+        phys = np.arange(needed, dtype=np.int64)
+    max_blocks = max(blocks_per_seq)
+    seq_tables = np.full((seqs, max_blocks), -1, np.int32)
+    off = 0
+    for s in range(seqs):
+        nb = blocks_per_seq[s]
+        seq_tables[s, :nb] = phys[off:off + nb]
+        off += nb
+    if shared_table:
+        assert seqs == 1
+        block_table = seq_tables[:1].copy()
+        bt_stride = 0
+    else:
+        block_table = np.repeat(seq_tables, rows_per_seq, axis=0)
+        bt_stride = max_blocks
+
+    # ---- latent (only blocks in use get values; the rest is NaN)
+    pool = np.full((pool_blocks * block_size, LATENT_DIM), FP8_NAN, np.uint8)
+    for p in phys:                                   # in allocation order
+        x = rng.standard_normal((block_size, LATENT_DIM), dtype=np.float32)
+        pool[p * block_size:(p + 1) * block_size] = _fp8_codes(x / np.float32(kv_scale))
+
+    # ---- indexer key arena: sequences back to back, then a NaN guard band
+    seq_base = np.zeros(seqs, np.int64)
+    np.cumsum(seq_tokens[:-1], out=seq_base[1:])
+    T = int(seq_tokens.sum())
+    idx_k = np.full((T + ARENA_GUARD_TOKENS, index_dim), BF16_NAN, np.uint16)
+    chunk = 1 << 16
+    for t0 in range(0, T, chunk):
+        t1 = min(T, t0 + chunk)
+        idx_k[t0:t1] = _bf16_bits(rng.standard_normal((t1 - t0, index_dim), dtype=np.float32))
+    idx_gate = np.full(T + ARENA_GUARD_TOKENS, BF16_NAN, np.uint16)
+    g = rng.standard_normal(T, dtype=np.float32)
+    idx_gate[:T] = _bf16_bits(1.0 / (1.0 + np.exp(-g.astype(np.float64))))
+    idx_base = np.repeat(seq_base, rows_per_seq).astype(np.int64)
+
+    # ---- queries
+    q_idx = rng.standard_normal((rows, index_heads, index_dim), dtype=np.float32)
+    head_w = (rng.standard_normal((rows, index_heads), dtype=np.float32)
+              * np.float32(index_heads ** -0.5)).astype(np.float32)
+    Q = _bf16_bits(np.float32(0.05) * rng.standard_normal((rows, heads, LATENT_DIM),
+                                                          dtype=np.float32))
+
+    # ---- the new row's latent (written by the latent-write step)
+    kv_a = norm_w = None
+    if with_write:
+        kv_a = _bf16_bits(rng.standard_normal((rows, LATENT_DIM), dtype=np.float32))
+        norm_w = _bf16_bits(1.0 + 0.1 * rng.standard_normal(LATENT_DIM, dtype=np.float32))
+
+    positions = (seq_lens.astype(np.int64) - 1).clip(min=0).astype(np.uint32)
+    slots = np.zeros(rows, np.int64)
+    for r in range(rows):
+        pos = int(positions[r])
+        bt_row = block_table[r if bt_stride else 0]
+        slots[r] = int(bt_row[pos // block_size]) * block_size + pos % block_size
+
+    return Workload(name=name, seed=seed, rows=rows, group_rows=rows_per_seq, heads=heads,
+                    index_heads=index_heads, index_dim=index_dim, topk=topk,
+                    block_size=block_size, max_blocks=max_blocks, bt_stride=bt_stride,
+                    kv_scale=kv_scale, sm_scale=sm_scale, eps=eps, seq_lens=seq_lens,
+                    positions=positions, slots=slots, block_table=block_table, pool=pool,
+                    idx_k=idx_k, idx_gate=idx_gate, idx_base=idx_base, q_idx=q_idx,
+                    head_w=head_w, Q=Q, kv_a=kv_a, norm_w=norm_w)
+
+
+# The five named workloads, each with a scale-down factor for parity cases the
+# oracle finishes in seconds (shorter contexts, fewer sequences, same shapes).
+NAMED = {
+    "tiny": dict(seed=0, seqs=1, rows_per_seq=1, len_kind="fixed", len_lo=4096, len_hi=4096,
+                 heads=16, index_heads=8, index_dim=64, topk=256, pool_blocks=64),
+    "single": dict(seed=1, seqs=1, rows_per_seq=1, len_kind="fixed", len_lo=32768,
+                   len_hi=32768, heads=64, index_heads=32, index_dim=128, topk=2048,
+                   pool_blocks=1024),
+    "batched": dict(seed=2, seqs=32, rows_per_seq=1, len_kind="uniform", len_lo=8192,
+                    len_hi=65536, heads=64, index_heads=32, index_dim=128, topk=2048),
+    "verify": dict(seed=3, seqs=8, rows_per_seq=4, len_kind="uniform", len_lo=65536,
+                   len_hi=131072, heads=64, index_heads=32, index_dim=128, topk=2048),
+    "long": dict(seed=4, seqs=64, rows_per_seq=1, len_kind="loguniform", len_lo=4096,
+                 len_hi=131072, heads=128, index_heads=64, index_dim=128, topk=2048,
+                 free_fraction=0.5, with_write=True),
+}
+
+
+def named(name: str, **overrides) -> Workload:
+    """One of the five named workloads at full size (``overrides`` replace fields)."""
+    spec = dict(NAMED[name])
+    spec.update(overrides)
+    seed = spec.pop("seed")
+    return make_workload(name, seed, **spec)
+
+
+def scaled(name: str, seqs: int | None = None, len_div: int = 8, **overrides) -> Workload:
+    """A reduced copy of a named workload: same heads, index geometry, topk and
+    structure, contexts divided by ``len_div`` and optionally fewer sequences."""
+    spec = dict(NAMED[name])
+    spec["len_lo"] = max(1, spec["len_lo"] // len_div)
+    spec["len_hi"] = max(spec["len_lo"], spec["len_hi"] // len_div)
+    if "pool_blocks" in spec:
+        spec["pool_blocks"] = max(1, spec["pool_blocks"] // len_div)
+    if seqs is not None:
+        spec["seqs"] = seqs
+    spec.update(overrides)
+    seed = spec.pop("seed")
+    return make_workload(f"{name}/len{len_div}", seed, **spec)

@@ -1,0 +1,357 @@
+"""Pins of the FP64 CPU oracle against things other than itself.
+
+Each test ties one oracle function to a fact the pages or the mathematics fix:
+published number-format definitions checked exhaustively against a library
+routine, closed forms, hand-derived small cases, brute force on tiny inputs,
+invariants (permuted block table, softmax normalisation, dense reduction) and
+the block-table values printed on the "glm5next_dsa/layer.rs" page.  A
+plausible mistake in the oracle (dropped term, wrong sign or index, swapped
+operand, the (1+w) RMSNorm) fails at least one of them; ``test_planted_*``
+checks that for a few such mistakes planted in a copy of the oracle's inputs
+or formula.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16(x):
+    t = torch.tensor(np.asarray(x, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+# ----------------------------------------------------------------------------- formats
+def test_bf16_value_all_patterns_match_torch(oracle):
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    got = np.array([oracle.bf16_value(int(b)) for b in bits])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+    assert oracle.bf16_value(0x3F80) == 1.0 and oracle.bf16_value(0xC000) == -2.0
+
+
+def test_e4m3_value_closed_forms_and_torch_table(oracle):
+    # OCP E4M3: bias 7, max 448, min subnormal 2^-9, min normal 2^-6, 0x7F NaN.
+    assert oracle.e4m3_value(0x7E) == 448.0
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9
+    assert oracle.e4m3_value(0x08) == 2.0 ** -6
+    assert oracle.e4m3_value(0x38) == 1.0
+    assert oracle.e4m3_value(0xB8) == -1.0
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    got = np.array([oracle.e4m3_value(int(c)) for c in codes])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def test_e4m3_encode_roundtrip_every_code(oracle):
+    for c in range(256):
+        v = oracle.e4m3_value(c)
+        if math.isnan(v):
+            continue
+        code, _ = oracle.e4m3_encode(v)
+        assert code == c, (hex(c), v, hex(code))
+
+
+def test_e4m3_encode_matches_torch_rne(oracle):
+    rng = np.random.default_rng(123)
+    vals = np.concatenate([
+        rng.standard_normal(4000) * 50.0,
+        rng.uniform(-448, 448, 2000),
+        rng.standard_normal(2000) * 2.0 ** -8,          # subnormal range
+    ]).astype(np.float32)
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v))[0] for v in vals], np.uint8)
+    assert (got == ref).all()
+
+
+def test_e4m3_encode_ties_saturation_and_halfulp(oracle):
+    assert oracle.e4m3_encode(1.0625) == (0x38, True)     # tie 1.0 / 1.125 -> even
+    assert oracle.e4m3_encode(1.1875) == (0x3A, True)     # tie 1.125 / 1.25 -> even
+    assert oracle.e4m3_encode(1.07)[0] == 0x39
+    assert oracle.e4m3_encode(1000.0)[0] == 0x7E          # satfinite
+    assert oracle.e4m3_encode(-1e9)[0] == 0xFE
+    assert oracle.e4m3_encode(float("nan"))[0] == 0x7F
+    assert oracle.e4m3_encode(-0.0)[0] == 0x80
+    rng = np.random.default_rng(7)
+    for v in rng.uniform(-440, 440, 500):
+        c, _ = oracle.e4m3_encode(v)
+        q = oracle.e4m3_value(c)
+        # half an ulp of the binade of q (subnormal spacing 2^-9)
+        e = max(math.floor(math.log2(max(abs(q), 2.0 ** -6))), -6)
+        assert abs(q - v) <= 0.5 * 2.0 ** (e - 3) + 1e-12
+
+
+# ----------------------------------------------------------------------------- S0
+def test_latent_write_hand_example(oracle):
+    # dim 2, x = (3, 4), w = (1, 1), eps 0, scale 1: rms = 1/sqrt(12.5)
+    # y = (0.8485.., 1.1313..) -> E4M3: 0.875 (0x36) and 1.125 (0x39)
+    codes, pre, _ = oracle.latent_write_row(_bf16([3.0, 4.0]), _bf16([1.0, 1.0]), 0.0, 1.0)
+    assert list(codes) == [0x36, 0x39]
+    assert pre[0] == pytest.approx(3 / math.sqrt(12.5), rel=1e-15)
+    assert pre[1] == pytest.approx(4 / math.sqrt(12.5), rel=1e-15)
+
+
+def test_latent_write_unit_weight_gives_unit_rms(oracle):
+    rng = np.random.default_rng(1)
+    x = _bf16(rng.standard_normal(512))
+    codes, pre, _ = oracle.latent_write_row(x, _bf16(np.ones(512)), 1e-6, 0.5)
+    inv = float(np.float32(1.0) / np.float32(0.5))
+    y = pre / inv
+    assert math.sqrt(np.mean(y ** 2)) == pytest.approx(1.0, abs=1e-6)
+
+
+def test_latent_write_is_vanilla_not_one_plus_w(oracle):
+    """The trap on the layer.rs page: x*rms*w vs x*rms*(1+w) must differ."""
+    rng = np.random.default_rng(2)
+    xf = rng.standard_normal(512)
+    wf = 1.0 + 0.1 * rng.standard_normal(512)
+    x, w = _bf16(xf), _bf16(wf)
+    xd = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy()
+    wd = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).double().numpy()
+    rms = 1.0 / math.sqrt(np.mean(xd ** 2) + float(np.float32(1e-6)))
+    inv = float(np.float32(1.0) / np.float32(0.02))
+    _, pre, _ = oracle.latent_write_row(x, w, 1e-6, 0.02)
+    assert np.allclose(pre, xd * rms * wd * inv, rtol=1e-13, atol=0)
+    assert not np.allclose(pre, xd * rms * (1.0 + wd) * inv, rtol=1e-2)
+
+
+def test_latent_write_scale_inverse_is_fp32(oracle):
+    """1/kv_scale is taken in FP32 (the write kernel receives an f32)."""
+    x = _bf16([1.0] * 4)
+    _, pre, _ = oracle.latent_write_row(x, _bf16([1.0] * 4), 0.0, 0.3)
+    inv32 = float(np.float32(1.0) / np.float32(0.3))
+    assert pre[0] == inv32 and pre[0] != 1.0 / 0.3
+
+
+# ----------------------------------------------------------------------------- S1
+def _rand_index_case(rng, heads, dim, n):
+    q = rng.standard_normal((heads, dim)).astype(np.float32)
+    w = (rng.standard_normal(heads) * heads ** -0.5).astype(np.float32)
+    k = _bf16(rng.standard_normal((n, dim)))
+    gate = _bf16(1.0 / (1.0 + np.exp(-rng.standard_normal(n))))
+    return q, w, k, gate
+
+
+def _to_f64(bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def test_index_scores_brute_force(oracle):
+    rng = np.random.default_rng(3)
+    q, w, k, gate = _rand_index_case(rng, 4, 16, 37)
+    s, A = oracle.index_scores_row(q, w, k, gate, 37)
+    kd, gd = _to_f64(k), _to_f64(gate)
+    dots = kd @ q.astype(np.float64).T                       # [n, heads]
+    ref = gd * (np.maximum(dots, 0) @ w.astype(np.float64))
+    ref_a = gd * (np.maximum(dots, 0) @ np.abs(w.astype(np.float64)))
+    assert np.allclose(s, ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(A, ref_a, rtol=1e-12, atol=1e-12)
+    assert (A >= np.abs(s) - 1e-12).all()
+    # token-list form gives the same numbers
+    toks = np.array([36, 0, 5], np.int64)
+    s2, _ = oracle.index_scores_row(q, w, k, gate, 0, tokens=toks)
+    assert np.array_equal(s2, s[toks])
+
+
+def test_index_scores_special_cases(oracle):
+    rng = np.random.default_rng(4)
+    q, _, k, _ = _rand_index_case(rng, 1, 32, 50)
+    one = np.ones(1, np.float32)
+    g1 = _bf16(np.ones(50))
+    s, _ = oracle.index_scores_row(q, one, k, g1, 50)
+    dots = _to_f64(k) @ q[0].astype(np.float64)
+    assert np.allclose(s, np.maximum(dots, 0.0), rtol=1e-13, atol=1e-13)
+    # linear in w
+    q4, w4, k4, gate4 = _rand_index_case(rng, 4, 32, 20)
+    s_a, _ = oracle.index_scores_row(q4, w4, k4, gate4, 20)
+    s_b, _ = oracle.index_scores_row(q4, (w4 * np.float32(4.0)).astype(np.float32), k4, gate4, 20)
+    assert np.allclose(s_b, 4.0 * s_a, rtol=1e-13, atol=1e-13)
+    # every dot negative -> score exactly 0
+    kneg = _bf16(-np.abs(rng.standard_normal((8, 32))))
+    qpos = np.abs(rng.standard_normal((4, 32))).astype(np.float32)
+    s0, _ = oracle.index_scores_row(qpos, w4, kneg, gate4, 8)
+    assert (s0 == 0.0).all()
+
+
+# ----------------------------------------------------------------------------- S2
+def _brute_topk(scores, L, K):
+    order = sorted(range(L), key=lambda t: (-scores[t], t))[:min(K, L)]
+    return sorted(order) + [-1] * (K - min(K, L))
+
+
+def test_topk_brute_force_with_ties(oracle):
+    s = np.array([1.0, 3.0, 3.0, 2.0, 3.0])
+    assert list(oracle.select_topk_row(s, 5, 2)) == [1, 2]
+    assert list(oracle.select_topk_row(s, 5, 4)) == [1, 2, 3, 4]
+    assert list(oracle.select_topk_row(s, 5, 8)) == [0, 1, 2, 3, 4, -1, -1, -1]
+    assert list(oracle.select_topk_row(s, 0, 3)) == [-1, -1, -1]
+    rng = np.random.default_rng(5)
+    for trial in range(50):
+        L = int(rng.integers(1, 200))
+        K = int(rng.integers(1, 64))
+        sc = rng.integers(-5, 5, L).astype(np.float64)      # many exact ties
+        if trial % 2:
+            sc = rng.standard_normal(L)
+        assert list(oracle.select_topk_row(sc, L, K)) == _brute_topk(sc, L, K)
+
+
+def test_topk_zero_signs_tie(oracle):
+    s = np.array([-0.0, 0.0, -0.0, -1.0])
+    assert list(oracle.select_topk_row(s, 4, 2)) == [0, 1]
+
+
+# ----------------------------------------------------------------------------- S3
+def _decode_case(rng, H=4, L=40, bs=8, nblocks=8, dim=512):
+    pool = torch.from_numpy((rng.standard_normal((nblocks * bs, dim)) / 0.02).astype(np.float32))
+    pool = pool.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    bt = rng.permutation(nblocks)[: -(-L // bs)].astype(np.int32)
+    Q = _bf16(0.05 * rng.standard_normal((H, dim)))
+    return pool, bt, Q
+
+
+def test_decode_topk_ge_len_is_dense_attention(oracle):
+    rng = np.random.default_rng(6)
+    pool, bt, Q = _decode_case(rng)
+    sel = np.concatenate([np.arange(40), -np.ones(8)]).astype(np.int32)
+    out, lse = oracle.mla_decode_row(Q, pool, bt, 8, 40, sel, 0.02, 0.0625)
+    dout, dlse = oracle.dense_mla_row(Q, pool, bt, 8, 40, 0.02, 0.0625)
+    assert np.allclose(out, dout, rtol=1e-12, atol=1e-14)
+    assert np.allclose(lse, dlse, rtol=1e-13, atol=1e-13)
+
+
+def test_decode_against_library_softmax(oracle):
+    rng = np.random.default_rng(8)
+    pool, bt, Q = _decode_case(rng, H=3, L=33)
+    sel = np.array([0, 4, 7, 20, 32, -1], np.int32)
+    out, lse = oracle.mla_decode_row(Q, pool, bt, 8, 33, sel, 0.02, 0.0625)
+    slots = [int(bt[j // 8]) * 8 + j % 8 for j in sel if j >= 0]
+    kv = torch.from_numpy(pool[slots]).view(torch.float8_e4m3fn).double() * float(np.float32(0.02))
+    q = torch.from_numpy(Q.view(np.int16)).view(torch.bfloat16).double()
+    z = (q @ kv.T) * 0.0625
+    ref = torch.softmax(z, dim=-1) @ kv
+    assert np.allclose(out, ref.numpy(), rtol=1e-12, atol=1e-14)
+    assert np.allclose(lse, torch.logsumexp(z, -1).numpy(), rtol=1e-13)
+
+
+def test_decode_softmax_weights_sum_to_one(oracle):
+    rng = np.random.default_rng(9)
+    pool, bt, Q = _decode_case(rng)
+    pool[:] = 0x3C                       # every latent element 1.5
+    sel = np.arange(40, dtype=np.int32)
+    out, _ = oracle.mla_decode_row(Q, pool, bt, 8, 40, sel, 0.02, 0.0625)
+    assert np.abs(out - 1.5 * float(np.float32(0.02))).max() < 1e-12 * 0.03
+
+
+def test_decode_single_token_and_uniform_logits(oracle):
+    rng = np.random.default_rng(10)
+    pool, bt, Q = _decode_case(rng)
+    sel = np.array([-1, 17, -1], np.int32)
+    out, lse = oracle.mla_decode_row(Q, pool, bt, 8, 40, sel, 0.02, 0.0625)
+    slot = int(bt[17 // 8]) * 8 + 17 % 8
+    khat = torch.from_numpy(pool[slot]).view(torch.float8_e4m3fn).double().numpy() * float(np.float32(0.02))
+    assert np.array_equal(out, np.broadcast_to(khat, out.shape))
+    zeros = np.zeros_like(Q)
+    sel5 = np.array([1, 2, 3, 10, 39], np.int32)
+    out, lse = oracle.mla_decode_row(zeros, pool, bt, 8, 40, sel5, 0.02, 0.0625)
+    slots = [int(bt[j // 8]) * 8 + j % 8 for j in sel5]
+    mean = (torch.from_numpy(pool[slots]).view(torch.float8_e4m3fn).double().numpy().mean(0)
+            * float(np.float32(0.02)))
+    assert np.allclose(out, mean, rtol=1e-13, atol=1e-16)
+    assert np.allclose(lse, math.log(5.0), rtol=1e-15)
+
+
+def test_decode_invariant_under_permuted_block_table(oracle):
+    rng = np.random.default_rng(11)
+    pool, bt, Q = _decode_case(rng, L=40, nblocks=8)
+    perm = rng.permutation(8)
+    pool2 = np.empty_like(pool)
+    for b in range(8):                   # move physical block b to perm[b]
+        pool2[perm[b] * 8:(perm[b] + 1) * 8] = pool[b * 8:(b + 1) * 8]
+    bt2 = perm[bt].astype(np.int32)
+    sel = np.array([0, 3, 9, 15, 22, 31, 39], np.int32)
+    a, la = oracle.mla_decode_row(Q, pool, bt, 8, 40, sel, 0.02, 0.0625)
+    b_, lb = oracle.mla_decode_row(Q, pool2, bt2, 8, 40, sel, 0.02, 0.0625)
+    assert np.array_equal(a, b_) and np.array_equal(la, lb)
+
+
+def test_decode_rejects_out_of_range(oracle):
+    rng = np.random.default_rng(12)
+    pool, bt, Q = _decode_case(rng)
+    with pytest.raises(ValueError):
+        oracle.mla_decode_row(Q, pool, bt, 8, 40, np.array([40], np.int32), 0.02, 0.0625)
+    with pytest.raises(ValueError):
+        oracle.mla_decode_row(Q, pool, bt, 8, 40, np.array([-2], np.int32), 0.02, 0.0625)
+
+
+def test_decode_empty_selection(oracle):
+    rng = np.random.default_rng(13)
+    pool, bt, Q = _decode_case(rng)
+    out, lse = oracle.mla_decode_row(Q, pool, bt, 8, 0, np.full(4, -1, np.int32), 0.02, 0.0625)
+    assert (out == 0).all() and np.isneginf(lse).all()
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+def test_planted_wrong_operand_fails_decode_pin(oracle):
+    """Transposed / wrong-slot reads: a decode that reads slot j instead of
+    bt[j/bs]*bs + j%bs breaks the permuted-table invariance."""
+    rng = np.random.default_rng(14)
+    pool, bt, Q = _decode_case(rng, L=40, nblocks=8)
+    sel = np.array([0, 3, 9, 15, 22, 31, 39], np.int32)
+    good, _ = oracle.mla_decode_row(Q, pool, bt, 8, 40, sel, 0.02, 0.0625)
+    identity = np.arange(8, dtype=np.int32)       # the mistake: ignore the table
+    bad, _ = oracle.mla_decode_row(Q, pool, identity, 8, 40, sel, 0.02, 0.0625)
+    assert not np.allclose(good, bad)
+
+
+def test_planted_missing_gate_fails_index_pin(oracle):
+    rng = np.random.default_rng(15)
+    q, w, k, gate = _rand_index_case(rng, 4, 16, 30)
+    s, _ = oracle.index_scores_row(q, w, k, gate, 30)
+    s_nogate, _ = oracle.index_scores_row(q, w, k, _bf16(np.ones(30)), 30)
+    assert not np.allclose(s, s_nogate)
+
+
+# ----------------------------------------------------------------------------- whole path
+def test_k_rows_equal_serial_rows_in_oracle(oracle):
+    from sparse_attention_mla_dsa_gb300 import workloads
+    wl = workloads.make_workload("krow", 21, seqs=2, rows_per_seq=3, len_kind="uniform",
+                                 len_lo=300, len_hi=500, heads=2, index_heads=4,
+                                 index_dim=64, topk=32)
+    together = oracle.run_path_rows(wl, threads=3)
+    for r in range(wl.rows):
+        alone = oracle.run_path_rows(wl, rows=[r])[r]
+        for key in ("s", "sel", "out", "lse"):
+            assert np.array_equal(together[r][key], alone[key])
+
+
+# ----------------------------------------------------------------------------- block table
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(x) for x in line.split()])
+    return rows
+
+
+def test_bt_entries_needed_golden(oracle):
+    for seq_len, k, bs, expected in _read_golden("bt_entries_needed.txt"):
+        assert oracle.bt_entries_needed(seq_len, k, bs) == expected
+    pool = 262_144 // 16 + 2
+    assert pool == 16_386 and pool > 16_384
+    assert oracle.bt_entries_needed(16_384, 4, 16) <= 16_384
+
+
+def test_bt_entries_cover_every_indexable_position(oracle):
+    for seq_len, k, bs in _read_golden("bt_cover_grid.txt"):
+        n = oracle.bt_entries_needed(seq_len, k, bs)
+        highest = max(seq_len + k - 1, 0) // bs
+        assert highest < n
