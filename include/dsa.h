@@ -1,0 +1,204 @@
+/*
+ * dsa.h -- C ABI of libdsa_gb300: the DSA decode hot path of the GLM-5.3
+ * sparse layers on one GB300 (sm_103a).
+ *
+ * Per decode row the path is
+ *   S0 dsa_latent_write    RMSNorm + FP8 quantisation + paged slot write of the
+ *                          row's new latent
+ *   S1 dsa_index_scores    lightning-indexer score of every visible token
+ *   S2 dsa_select_topk     per-row top-k of those scores
+ *   S3 dsa_mla_decode_fp8  absorbed NoPE MLA gather-attend over the selection
+ * issued in that order on one stream.  Sources (spark_model documentation):
+ * the "glm5next_dsa/layer.rs" source page (module header: decode data flow
+ * and its traps; decode_k: latent write, per-row metadata, one attend for all
+ * rows; attend_rows; the selection notes on a total order) and the "Struct
+ * Glm5NextDsaLayer" rustdoc page (kv_scale, decode_k).
+ *
+ * Conventions for every entry point
+ *   - Every pointer argument is a DEVICE pointer on the current CUDA device,
+ *     owned by the caller and unchanged until the work on `stream` completes.
+ *     The library never allocates, frees, copies host<->device or
+ *     synchronises inside these calls (so the calls can be recorded into a
+ *     CUDA graph by the caller).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous: a DSA_OK return means the work was enqueued.
+ *   - bf16 tensors are passed as uint16_t bit patterns; FP8 as uint8_t E4M3
+ *     codes (OCP: bias 7, max 448, no infinities).
+ *   - Argument errors detectable on the host return DSA_ERR_INVALID_ARG or
+ *     DSA_ERR_UNSUPPORTED before anything is launched.  Launch failures return
+ *     DSA_ERR_CUDA.  Values only visible on the device (a seq_len above
+ *     max_len, a selected index outside [0, seq_len), a negative block id, a
+ *     slot outside the pool, mismatched arena bases) make the kernel skip the
+ *     offending access and record the first such error in a sticky device
+ *     error word that dsa_get_error() reads; kernels never trap.  Every wait
+ *     inside a kernel is bounded and records DSA_DEVERR_TIMEOUT when it gives
+ *     up.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+#define DSA_LATENT_DIM 512
+
+typedef enum dsa_status {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,
+    DSA_ERR_UNSUPPORTED = 2,
+    DSA_ERR_CUDA = 3,
+    DSA_ERR_DEVICE = 4,      /* dsa_get_error found a recorded device-side error */
+    DSA_ERR_WORKSPACE = 5    /* workspace missing or smaller than dsa_workspace_bytes() */
+} dsa_status;
+
+/* Codes recorded in the device error word. */
+enum {
+    DSA_DEVERR_NONE = 0,
+    DSA_DEVERR_SEQ_LEN = 1,   /* seq_len < 0 or > max_len                               */
+    DSA_DEVERR_SLOT = 2,      /* latent-write slot outside [0, nslots)                  */
+    DSA_DEVERR_SELECT = 3,    /* selected index outside [0, seq_len) and not -1         */
+    DSA_DEVERR_BLOCK = 4,     /* block-table entry missing, negative or past the pool   */
+    DSA_DEVERR_ARENA = 5,     /* idx_base invalid, or rows of one group differ in base  */
+    DSA_DEVERR_POSITION = 6,  /* positions[r] != seq_lens[r]-1, or slot != table slot   */
+    DSA_DEVERR_TIMEOUT = 7    /* a bounded wait inside a kernel gave up                 */
+};
+
+/*
+ * Per-row metadata of one call ("glm5next_dsa/layer.rs", decode_k: the K-row
+ * attn_metadata -- positions [k] u32, slot [k] i64, seq_len [k] i32,
+ * block_table [k][max_blocks_per_seq] i32 -- at stable device addresses; row r
+ * reads element r of each).  All pointers are device pointers.
+ */
+typedef struct dsa_rows {
+    const uint32_t *positions;  /* [rows] token position of the row (= seq_len-1); may be
+                                   NULL.  When given, dsa_latent_write checks it against
+                                   seq_lens and the table and refuses inconsistent rows. */
+    const int64_t *slots;       /* [rows] paged slot of the row's new latent:
+                                   block_table[pos/block_size]*block_size + pos%block_size.
+                                   Read only by dsa_latent_write; may be NULL otherwise.  */
+    const int32_t *seq_lens;    /* [rows] the row sees tokens [0, seq_len)               */
+    const int32_t *block_table; /* row r at block_table + r*bt_stride, max_blocks_per_seq
+                                   entries of physical block ids; -1 = none.             */
+    int32_t max_blocks_per_seq; /* entries per table row (bounds every lookup)           */
+    int32_t bt_stride;          /* elements between table rows; 0 = every row uses row 0
+                                   (rows of one sequence sharing one table)              */
+    int32_t block_size;         /* tokens per paged block, > 0                           */
+    int32_t rows;               /* R >= 1                                                */
+} dsa_rows;
+
+/*
+ * S0 -- latent write ("glm5next_dsa/layer.rs", module header trap 1 and
+ * decode_k "kv path: latent -> FP8 -> paged slot"; "Struct Glm5NextDsaLayer",
+ * kv_scale: the write takes 1/scale).  For each row r:
+ *   y = kv_a[r] * rsqrt(mean(kv_a[r]^2) + eps) * norm_w      (vanilla: w, not 1+w)
+ *   pool[slots[r]][i] = E4M3_RNE_satfinite(y[i] * fl32(1/kv_scale))
+ * The norm and scaling are computed in double, with one rounding to FP8.
+ *   kv_a    [rows][latent_dim] bf16      norm_w [latent_dim] bf16
+ *   pool    [nslots][latent_dim] FP8, written in place at the rows' slots
+ * latent_dim must be 512.  A slot outside [0, nslots) (or a row inconsistent
+ * with `positions`, when given) is skipped and recorded on the device.
+ */
+dsa_status dsa_latent_write(const dsa_rows *rows, const uint16_t *kv_a, const uint16_t *norm_w,
+                            uint8_t *pool, int64_t nslots, int32_t latent_dim, float eps,
+                            float kv_scale, void *stream);
+
+/*
+ * S1 -- lightning-indexer scores ("glm5next_dsa/layer.rs", module header:
+ * q_idx, k_normed, gate and the head weights feed select_tokens; trap 3:
+ * weights_proj already carries index_heads^-0.5 and the score does not scale).
+ * For each row r and token t in [0, seq_lens[r]):
+ *   scores[r*max_len + t] = gate[b+t] * sum_h head_w[r][h] * max(0, sum_d q_idx[r][h][d]*idx_k[b+t][d])
+ * with b = idx_base[r].  Entries t >= seq_lens[r] of a scores row are not written.
+ *   q_idx  [rows][index_heads][index_dim] fp32   head_w [rows][index_heads] fp32
+ *   idx_k  [idx_tokens][index_dim] bf16 (key arena, all sequences)
+ *   idx_gate [idx_tokens] bf16 (per-token scalar gate)
+ *   idx_base [rows] int64: the row's sequence start in the arena
+ *   scores [rows][max_len] fp32 (output)
+ * rows_per_seq: consecutive rows that share one sequence (a K-token verify);
+ * they must have equal idx_base (checked on the device) and their keys are
+ * read once for all of them.  rows must be a multiple of rows_per_seq.
+ * Supported: index_dim in {64, 128}; index_heads in [1, 256]; idx_k 16-byte
+ * aligned; idx_tokens < 2^31.  Each row's result does not depend on
+ * rows_per_seq or on the other rows (bit for bit).
+ */
+dsa_status dsa_index_scores(const dsa_rows *rows, const float *q_idx, const float *head_w,
+                            const uint16_t *idx_k, const uint16_t *idx_gate, int64_t idx_tokens,
+                            const int64_t *idx_base, int32_t index_heads, int32_t index_dim,
+                            int32_t rows_per_seq, int32_t max_len, float *scores, void *stream);
+
+/*
+ * S2 -- per-row top-k ("glm5next_dsa/layer.rs", notes on batch_select_enabled
+ * and select_rows_batched: the selection is taken under the total order score
+ * DESC, then index ASC, so it is unique).  For each row r, the n = min(topk,
+ * seq_lens[r]) tokens of [0, seq_lens[r]) that come first under that order are
+ * written to sel[r*topk + 0 .. n) in ASCENDING token order; sel[r*topk + n ..
+ * topk) = -1.  -0.0 and +0.0 compare equal.  Scores must not be NaN.
+ *   scores [rows][max_len] fp32 (as written by dsa_index_scores)
+ *   sel    [rows][topk] int32 (output)
+ * topk in [1, 65536].  No workspace is used at present; pass the same
+ * workspace as to dsa_mla_decode_fp8 (or NULL / 0).
+ */
+dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t max_len,
+                           int32_t topk, int32_t *sel, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/*
+ * S3 -- absorbed NoPE MLA gather-attend over the selection
+ * ("glm5next_dsa/layer.rs", module header trap 4: Q arrives absorbed into the
+ * 512-d latent space; attend_rows: one launch for all rows, each with its own
+ * selection row, seq_len and table row, K and V the same latent pool; decode_k:
+ * slot = block*block_size + pos%block_size).  For each row r and head h, over
+ * the entries j of sel[r] that are not -1:
+ *   Khat_j = e4m3(pool[slot(j)]) * kv_scale
+ *   z_j    = sm_scale * (q[r][h] . Khat_j)
+ *   out[r][h] = sum_j softmax(z)_j * Khat_j           (bf16, latent space)
+ *   lse[r][h] = log sum_j exp(z_j)                     (fp32, optional)
+ * A row with nothing selected gets out = 0 and lse = -inf.
+ *   q   [rows][heads][latent_dim] bf16       pool [nslots][latent_dim] FP8
+ *   sel [rows][topk] int32                   out  [rows][heads][latent_dim] bf16
+ * latent_dim must be 512; heads a multiple of 16.  The work of a row is split
+ * over its selection in a way that depends only on topk, so each row's result
+ * is bit-identical whatever the other rows of the call are.  The workspace
+ * holds the split partials: at least dsa_workspace_bytes(rows, heads, topk).
+ */
+dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,
+                              int64_t nslots, const int32_t *sel, int32_t topk, int32_t heads,
+                              int32_t latent_dim, float kv_scale, float sm_scale, uint16_t *out,
+                              float *lse_or_null, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/* Device bytes of the caller-owned workspace that dsa_select_topk and
+ * dsa_mla_decode_fp8 need for a call of this shape (0 on bad arguments). */
+size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
+
+/*
+ * Read the sticky device error word of the current device: *code_out is the
+ * first DSA_DEVERR_* recorded since the last reset (0 if none), *row_out the
+ * row it concerned and *count_out how many errors were recorded.  Any out
+ * pointer may be NULL.  This call synchronises the device.  reset != 0 clears
+ * the word.  Returns DSA_ERR_DEVICE when an error was recorded, else DSA_OK
+ * (or DSA_ERR_CUDA).
+ */
+dsa_status dsa_get_error(int32_t *code_out, int32_t *row_out, int32_t *count_out, int32_t reset);
+
+/* Block-table entries the paged gather can index for k rows starting at
+ * seq_len, plus one of slack: (seq_len + k) / block_size + 2, a block size of
+ * 0 counted as 1 ("glm5next_dsa/layer.rs", bt_entries_needed). */
+int64_t dsa_bt_entries_needed(int64_t seq_len, int64_t k, int64_t block_size);
+
+/* Static text for a status code. */
+const char *dsa_status_string(dsa_status status);
+
+/* DSA_ABI_VERSION of the loaded library. */
+int32_t dsa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H */

@@ -1,0 +1,196 @@
+"""ctypes binding of libdsa_gb300 (include/dsa.h), same entry-point names.
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity and passed as raw device pointers together with the current torch
+CUDA stream.  Every step of the path runs in the library's CUDA kernels; if the
+library is missing this module raises instead of computing anything itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+LATENT_DIM = 512
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
+           4: "device-side error recorded", 5: "workspace missing or too small"}
+DEVERR = {0: "none", 1: "seq_len", 2: "slot", 3: "select", 4: "block", 5: "arena",
+          6: "position", 7: "timeout"}
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {_STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+class Rows(ctypes.Structure):
+    """dsa_rows: per-row metadata, all device pointers."""
+    _fields_ = [("positions", ctypes.c_void_p), ("slots", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("max_blocks_per_seq", ctypes.c_int32), ("bt_stride", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("rows", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libdsa_gb300.so is not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    RP = ctypes.POINTER(Rows)
+    sig = {
+        "dsa_latent_write": [RP, P, P, P, i64, i32, f32, f32, P],
+        "dsa_index_scores": [RP, P, P, P, P, i64, P, i32, i32, i32, i32, P, P],
+        "dsa_select_topk": [RP, P, i32, i32, P, P, sz, P],
+        "dsa_mla_decode_fp8": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, sz, P],
+        "dsa_get_error": [P, P, P, i32],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.dsa_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.dsa_workspace_bytes.restype = sz
+    lib.dsa_bt_entries_needed.argtypes = [i64, i64, i64]
+    lib.dsa_bt_entries_needed.restype = i64
+    lib.dsa_status_string.argtypes = [ctypes.c_int]
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_abi_version.argtypes = []
+    lib.dsa_abi_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise DsaError(fn, status)
+
+
+_BITS16 = (torch.uint16, torch.int16, torch.bfloat16)
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name: str = "") -> int | None:
+    """Device pointer of a contiguous CUDA tensor.  bf16 arguments (bit
+    patterns) may be passed as uint16, int16 or bfloat16 tensors."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    allowed = _BITS16 if dtype is torch.uint16 else (dtype,)
+    if dtype is not None and t.dtype not in allowed:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_rows(seq_lens: torch.Tensor, block_table: torch.Tensor | None = None,
+              block_size: int = 64, slots: torch.Tensor | None = None,
+              positions: torch.Tensor | None = None, shared_table: bool = False) -> Rows:
+    """Build dsa_rows from device tensors: seq_lens int32 [R], block_table int32
+    [R, max_blocks] (or [1, max_blocks] with shared_table), slots int64 [R],
+    positions int32/uint32 [R].  The tensors must outlive the calls."""
+    R = seq_lens.shape[0]
+    rows = Rows()
+    rows.seq_lens = _ptr(seq_lens, torch.int32, "seq_lens")
+    rows.slots = _ptr(slots, torch.int64, "slots")
+    rows.positions = _ptr(positions, None, "positions")
+    if block_table is not None:
+        rows.block_table = _ptr(block_table, torch.int32, "block_table")
+        rows.max_blocks_per_seq = block_table.shape[-1]
+        rows.bt_stride = 0 if shared_table else block_table.shape[-1]
+    rows.block_size = block_size
+    rows.rows = R
+    return rows
+
+
+def dsa_latent_write(rows: Rows, kv_a: torch.Tensor, norm_w: torch.Tensor, pool: torch.Tensor,
+                     eps: float, kv_scale: float, stream=None) -> None:
+    lib = load()
+    st = lib.dsa_latent_write(ctypes.byref(rows), _ptr(kv_a, torch.uint16, "kv_a"),
+                              _ptr(norm_w, torch.uint16, "norm_w"), _ptr(pool, torch.uint8, "pool"),
+                              pool.shape[0], pool.shape[-1], float(eps), float(kv_scale),
+                              _stream(stream))
+    _check("dsa_latent_write", st)
+
+
+def dsa_index_scores(rows: Rows, q_idx: torch.Tensor, head_w: torch.Tensor, idx_k: torch.Tensor,
+                     idx_gate: torch.Tensor, idx_base: torch.Tensor, rows_per_seq: int,
+                     max_len: int, scores: torch.Tensor, stream=None) -> None:
+    lib = load()
+    heads, dim = q_idx.shape[-2], q_idx.shape[-1]
+    st = lib.dsa_index_scores(ctypes.byref(rows), _ptr(q_idx, torch.float32, "q_idx"),
+                              _ptr(head_w, torch.float32, "head_w"), _ptr(idx_k, torch.uint16, "idx_k"),
+                              _ptr(idx_gate, torch.uint16, "idx_gate"), idx_k.shape[0],
+                              _ptr(idx_base, torch.int64, "idx_base"), heads, dim, int(rows_per_seq),
+                              int(max_len), _ptr(scores, torch.float32, "scores"), _stream(stream))
+    _check("dsa_index_scores", st)
+
+
+def dsa_select_topk(rows: Rows, scores: torch.Tensor, max_len: int, topk: int, sel: torch.Tensor,
+                    workspace: torch.Tensor | None = None, stream=None) -> None:
+    lib = load()
+    ws = _ptr(workspace, None, "workspace")
+    st = lib.dsa_select_topk(ctypes.byref(rows), _ptr(scores, torch.float32, "scores"), int(max_len),
+                             int(topk), _ptr(sel, torch.int32, "sel"), ws,
+                             0 if workspace is None else workspace.numel() * workspace.element_size(),
+                             _stream(stream))
+    _check("dsa_select_topk", st)
+
+
+def dsa_mla_decode_fp8(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: torch.Tensor, topk: int,
+                       kv_scale: float, sm_scale: float, out: torch.Tensor,
+                       lse: torch.Tensor | None, workspace: torch.Tensor, stream=None) -> None:
+    lib = load()
+    heads = q.shape[-2]
+    st = lib.dsa_mla_decode_fp8(ctypes.byref(rows), _ptr(q, torch.uint16, "q"),
+                                _ptr(pool, torch.uint8, "pool"), pool.shape[0],
+                                _ptr(sel, torch.int32, "sel"), int(topk), heads, q.shape[-1],
+                                float(kv_scale), float(sm_scale), _ptr(out, torch.uint16, "out"),
+                                _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("dsa_mla_decode_fp8", st)
+
+
+def dsa_workspace_bytes(rows: int, heads: int, topk: int) -> int:
+    return int(load().dsa_workspace_bytes(int(rows), int(heads), int(topk)))
+
+
+def dsa_get_error(reset: bool = True) -> tuple[int, int, int]:
+    """(code, row, count) of the sticky device error word; synchronises."""
+    code, row, count = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    st = load().dsa_get_error(ctypes.byref(code), ctypes.byref(row), ctypes.byref(count),
+                              1 if reset else 0)
+    if st not in (0, 4):
+        raise DsaError("dsa_get_error", st)
+    return code.value, row.value, count.value
+
+
+def dsa_bt_entries_needed(seq_len: int, k: int, block_size: int) -> int:
+    return int(load().dsa_bt_entries_needed(int(seq_len), int(k), int(block_size)))
+
+
+def dsa_abi_version() -> int:
+    return int(load().dsa_abi_version())

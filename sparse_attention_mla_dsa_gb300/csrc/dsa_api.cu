@@ -1,0 +1,272 @@
+// dsa_api.cu -- the C ABI declared in include/dsa.h: argument validation,
+// launch planning, the device error word and the TMA descriptor of the key
+// arena.  No call here allocates, frees, copies host<->device or synchronises
+// (except dsa_get_error, which says so).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "dsa_device.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+// The sticky device error word (one per device that loads the library).
+__device__ int g_error_word[4];
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int* err = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return nullptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    d.err = static_cast<int*>(p);
+    d.ready = true;
+  }
+  return &d;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode_tiled == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode_tiled;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+dsa_status check_rows(const dsa_rows* rows, bool need_table) {
+  if (rows == nullptr || rows->rows < 1 || rows->seq_lens == nullptr) return DSA_ERR_INVALID_ARG;
+  if (rows->rows > 65535) return DSA_ERR_UNSUPPORTED;
+  if (need_table) {
+    if (rows->block_table == nullptr || rows->block_size < 1 || rows->max_blocks_per_seq < 1 ||
+        rows->bt_stride < 0)
+      return DSA_ERR_INVALID_ARG;
+    if (rows->bt_stride != 0 && rows->bt_stride < rows->max_blocks_per_seq)
+      return DSA_ERR_INVALID_ARG;
+  }
+  return DSA_OK;
+}
+
+dsa_status launched(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+dsa_status dsa_latent_write(const dsa_rows* rows, const uint16_t* kv_a, const uint16_t* norm_w,
+                            uint8_t* pool, int64_t nslots, int32_t latent_dim, float eps,
+                            float kv_scale, void* stream) {
+  dsa_status st = check_rows(rows, rows != nullptr && rows->positions != nullptr);
+  if (st != DSA_OK) return st;
+  if (rows->slots == nullptr || kv_a == nullptr || norm_w == nullptr || pool == nullptr ||
+      nslots < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (latent_dim != DSA_LATENT_DIM) return DSA_ERR_UNSUPPORTED;
+  if (!(kv_scale > 0.0f) || !(eps >= 0.0f)) return DSA_ERR_INVALID_ARG;
+  if (!aligned(kv_a, 8) || !aligned(norm_w, 8) || !aligned(pool, 4)) return DSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = device_info();
+  if (dev == nullptr) return DSA_ERR_CUDA;
+  LatentWriteParams p{};
+  p.rows = *rows;
+  p.kv_a = kv_a;
+  p.norm_w = norm_w;
+  p.pool = pool;
+  p.nslots = nslots;
+  p.eps = eps;
+  p.inv_scale = 1.0f / kv_scale;
+  p.err = dev->err;
+  return launched(launch_latent_write(p, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_index_scores(const dsa_rows* rows, const float* q_idx, const float* head_w,
+                            const uint16_t* idx_k, const uint16_t* idx_gate, int64_t idx_tokens,
+                            const int64_t* idx_base, int32_t index_heads, int32_t index_dim,
+                            int32_t rows_per_seq, int32_t max_len, float* scores, void* stream) {
+  dsa_status st = check_rows(rows, false);
+  if (st != DSA_OK) return st;
+  if (q_idx == nullptr || head_w == nullptr || idx_k == nullptr || idx_gate == nullptr ||
+      idx_base == nullptr || scores == nullptr || idx_tokens < 1 || max_len < 0)
+    return DSA_ERR_INVALID_ARG;
+  if (rows_per_seq < 1 || rows->rows % rows_per_seq != 0) return DSA_ERR_INVALID_ARG;
+  if (index_dim != 64 && index_dim != 128) return DSA_ERR_UNSUPPORTED;
+  if (index_heads < 1 || index_heads > 256) return DSA_ERR_UNSUPPORTED;
+  if (idx_tokens > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
+  if (!aligned(idx_k, 16) || !aligned(q_idx, 16)) return DSA_ERR_INVALID_ARG;
+  if (max_len == 0) return DSA_OK;
+  const DeviceInfo* dev = device_info();
+  if (dev == nullptr) return DSA_ERR_CUDA;
+  auto encode = encode_tiled();
+  if (encode == nullptr) return DSA_ERR_CUDA;
+
+  IndexParams p{};
+  p.seq_lens = rows->seq_lens;
+  p.q_idx = q_idx;
+  p.head_w = head_w;
+  p.gate = idx_gate;
+  p.idx_base = idx_base;
+  p.scores = scores;
+  p.err = dev->err;
+  p.idx_tokens = idx_tokens;
+  p.rows = rows->rows;
+  p.rows_per_seq = rows_per_seq;
+  // Rows of one sequence share each key tile as long as their heads fit one
+  // MMA N (<= 256); a head count that is not a multiple of 16 runs one row
+  // per launch group so that no 16-column TMEM load straddles two rows.
+  int sub = 256 / index_heads;
+  if (index_heads % 16 != 0) sub = 1;
+  sub = sub < 1 ? 1 : (sub > 32 ? 32 : sub);
+  if (sub > rows_per_seq) sub = rows_per_seq;
+  p.sub_rows = sub;
+  p.subs_per_seq = (rows_per_seq + sub - 1) / sub;
+  p.heads = index_heads;
+  p.dim = index_dim;
+  p.npad = ((sub * index_heads + 15) / 16) * 16;
+  p.max_len = max_len;
+  p.wait_ns = kDefaultWaitNs;
+  plan_index_scores(p, dev->num_sms);
+
+  // Key arena [idx_tokens, index_dim] bf16, boxes of 128 tokens x 64 dims
+  // (128 bytes, the swizzle span); rows past the arena read as zero.
+  CUtensorMap kmap;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(index_dim), static_cast<cuuint64_t>(idx_tokens)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(index_dim) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult cr = encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(idx_k),
+                       gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return DSA_ERR_INVALID_ARG;
+  return launched(launch_index_scores(p, kmap, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_select_topk(const dsa_rows* rows, const float* scores, int32_t max_len,
+                           int32_t topk, int32_t* sel, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  dsa_status st = check_rows(rows, false);
+  if (st != DSA_OK) return st;
+  if (scores == nullptr || sel == nullptr || max_len < 0) return DSA_ERR_INVALID_ARG;
+  if (topk < 1 || topk > 65536) return DSA_ERR_UNSUPPORTED;
+  const DeviceInfo* dev = device_info();
+  if (dev == nullptr) return DSA_ERR_CUDA;
+  TopkParams p{};
+  p.seq_lens = rows->seq_lens;
+  p.scores = scores;
+  p.sel = sel;
+  p.err = dev->err;
+  p.rows = rows->rows;
+  p.max_len = max_len;
+  p.topk = topk;
+  return launched(launch_select_topk(p, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uint8_t* pool,
+                              int64_t nslots, const int32_t* sel, int32_t topk, int32_t heads,
+                              int32_t latent_dim, float kv_scale, float sm_scale, uint16_t* out,
+                              float* lse_or_null, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  dsa_status st = check_rows(rows, true);
+  if (st != DSA_OK) return st;
+  if (q == nullptr || pool == nullptr || sel == nullptr || out == nullptr || nslots < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (latent_dim != DSA_LATENT_DIM) return DSA_ERR_UNSUPPORTED;
+  if (heads < 16 || heads % 16 != 0 || heads > 4096) return DSA_ERR_UNSUPPORTED;
+  if (topk < 1 || topk > 65536) return DSA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(out, 8)) return DSA_ERR_INVALID_ARG;
+  const size_t need = decode_workspace_bytes(rows->rows, heads, topk);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return DSA_ERR_WORKSPACE;
+  const DeviceInfo* dev = device_info();
+  if (dev == nullptr) return DSA_ERR_CUDA;
+  DecodeParams p{};
+  p.rows = *rows;
+  p.q = q;
+  p.pool = pool;
+  p.nslots = nslots;
+  p.sel = sel;
+  p.out = out;
+  p.lse = lse_or_null;
+  p.topk = topk;
+  p.heads = heads;
+  p.splits = decode_splits(topk);
+  const size_t n = static_cast<size_t>(rows->rows) * p.splits * heads;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                       ((n * 512 * sizeof(float) + 255) & ~static_cast<size_t>(255)));
+  p.err = dev->err;
+  p.kv_scale = kv_scale;
+  p.sm_scale = sm_scale;
+  return launched(launch_mla_decode(p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
+  if (rows < 1 || heads < 1 || topk < 1) return 0;
+  return decode_workspace_bytes(rows, heads, topk);
+}
+
+dsa_status dsa_get_error(int32_t* code_out, int32_t* row_out, int32_t* count_out, int32_t reset) {
+  const DeviceInfo* dev = device_info();
+  if (dev == nullptr) return DSA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DSA_ERR_CUDA;
+  int word[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(word, dev->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (reset) {
+    if (cudaMemset(dev->err, 0, sizeof word) != cudaSuccess) return DSA_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  if (code_out) *code_out = word[0];
+  if (row_out) *row_out = word[1];
+  if (count_out) *count_out = word[2];
+  return word[0] != 0 ? DSA_ERR_DEVICE : DSA_OK;
+}
+
+int64_t dsa_bt_entries_needed(int64_t seq_len, int64_t k, int64_t block_size) {
+  const int64_t bs = block_size > 0 ? block_size : 1;
+  return (seq_len + k) / bs + 2;
+}
+
+const char* dsa_status_string(dsa_status status) {
+  switch (status) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported shape or size";
+    case DSA_ERR_CUDA: return "CUDA error";
+    case DSA_ERR_DEVICE: return "device-side error recorded";
+    case DSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// dsa_internal.h -- host-side launch interfaces between the C ABI layer
+// (dsa_api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+// Bound on every mbarrier wait in the kernels (wall time).
+constexpr uint64_t kDefaultWaitNs = 500ull * 1000ull * 1000ull;
+
+struct LatentWriteParams {
+  dsa_rows rows;
+  const uint16_t* kv_a;
+  const uint16_t* norm_w;
+  uint8_t* pool;
+  int64_t nslots;
+  float eps;
+  float inv_scale;  // fl32(1 / kv_scale)
+  int* err;
+};
+cudaError_t launch_latent_write(const LatentWriteParams& p, cudaStream_t stream);
+
+struct IndexParams {
+  const int32_t* seq_lens;
+  const float* q_idx;
+  const float* head_w;
+  const uint16_t* gate;
+  const int64_t* idx_base;
+  float* scores;
+  int* err;
+  int64_t idx_tokens;
+  int32_t rows;
+  int32_t rows_per_seq;   // caller's sequence group size G
+  int32_t sub_rows;       // rows per launch group (<= G, npad <= 256)
+  int32_t subs_per_seq;   // ceil(G / sub_rows)
+  int32_t heads;
+  int32_t dim;            // 64 or 128
+  int32_t npad;           // sub_rows*heads rounded up to a multiple of 16
+  int32_t max_len;
+  int32_t chunk_tiles;    // 128-token tiles per CTA
+  int32_t stages;         // smem pipeline depth
+  uint32_t tmem_cols;
+  uint32_t smem_bytes;
+  uint64_t wait_ns;
+};
+// Fills in chunk_tiles / stages / tmem_cols / smem_bytes from the shape.
+void plan_index_scores(IndexParams& p, int num_sms);
+cudaError_t launch_index_scores(const IndexParams& p, const CUtensorMap& kmap,
+                                cudaStream_t stream);
+
+struct TopkParams {
+  const int32_t* seq_lens;
+  const float* scores;
+  int32_t* sel;
+  int* err;
+  int32_t rows;
+  int32_t max_len;
+  int32_t topk;
+};
+cudaError_t launch_select_topk(const TopkParams& p, cudaStream_t stream);
+
+struct DecodeParams {
+  dsa_rows rows;
+  const uint16_t* q;
+  const uint8_t* pool;
+  int64_t nslots;
+  const int32_t* sel;
+  uint16_t* out;
+  float* lse;
+  float* part_o;    // [rows][splits][heads][512]
+  float* part_ml;   // [rows][splits][heads][2]
+  int* err;
+  int32_t topk;
+  int32_t heads;
+  int32_t splits;
+  float kv_scale;
+  float sm_scale;
+};
+int32_t decode_splits(int32_t topk);
+size_t decode_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
+cudaError_t launch_mla_decode(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace dsa

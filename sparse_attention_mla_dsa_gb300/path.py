@@ -1,0 +1,136 @@
+"""Device-resident state and one decode step of the DSA hot path.
+
+``DeviceWorkload`` uploads a synthetic workload (key arena, gate, paged FP8
+latent pool, per-row metadata and queries) once and runs the four C-ABI calls
+in stream order -- S0 latent write (when the workload writes new rows), S1
+index scores, S2 top-k, S3 gather-attend -- without any host synchronisation.
+
+``DsaDecoder`` is the host-facing form: per step it copies that step's inputs
+(queries, head weights, the new latent rows, row metadata) from pinned host
+memory to the device, runs the same four calls and reads the attention output
+back into pinned host memory.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import api
+
+
+def _dev(a: np.ndarray, device) -> torch.Tensor:
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    elif a.dtype == np.uint32:
+        a = a.view(np.int32)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class DeviceWorkload:
+    """All inputs of a workload resident on one CUDA device, plus outputs."""
+
+    def __init__(self, wl, device: str | torch.device = "cuda", pool: torch.Tensor | None = None):
+        self.wl = wl
+        self.device = torch.device(device)
+        d = self.device
+        self.seq_lens = _dev(wl.seq_lens.astype(np.int32), d)
+        self.positions = _dev(wl.positions.astype(np.int32), d)
+        self.slots = _dev(wl.slots.astype(np.int64), d)
+        self.block_table = _dev(wl.block_table.astype(np.int32), d)
+        self.pool = pool if pool is not None else _dev(wl.pool, d)
+        self.idx_k = _dev(wl.idx_k, d)
+        self.idx_gate = _dev(wl.idx_gate, d)
+        self.idx_base = _dev(wl.idx_base.astype(np.int64), d)
+        self.q_idx = _dev(wl.q_idx, d)
+        self.head_w = _dev(wl.head_w, d)
+        self.Q = _dev(wl.Q, d)
+        self.kv_a = _dev(wl.kv_a, d) if wl.kv_a is not None else None
+        self.norm_w = _dev(wl.norm_w, d) if wl.norm_w is not None else None
+        R, H = wl.rows, wl.heads
+        self.max_len = max(1, wl.max_len)
+        self.scores = torch.empty((R, self.max_len), dtype=torch.float32, device=d)
+        self.sel = torch.empty((R, wl.topk), dtype=torch.int32, device=d)
+        self.out = torch.empty((R, H, 512), dtype=torch.int16, device=d)
+        self.lse = torch.empty((R, H), dtype=torch.float32, device=d)
+        nbytes = api.dsa_workspace_bytes(R, H, wl.topk)
+        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=d)
+        self.rows = api.make_rows(self.seq_lens, self.block_table, wl.block_size, self.slots,
+                                  self.positions, shared_table=(wl.bt_stride == 0))
+
+    # ---- the four steps
+    def latent_write(self, stream=None):
+        wl = self.wl
+        api.dsa_latent_write(self.rows, self.kv_a, self.norm_w, self.pool, wl.eps, wl.kv_scale,
+                             stream)
+
+    def index_scores(self, stream=None):
+        api.dsa_index_scores(self.rows, self.q_idx, self.head_w, self.idx_k, self.idx_gate,
+                             self.idx_base, self.wl.group_rows, self.max_len, self.scores, stream)
+
+    def select_topk(self, stream=None):
+        api.dsa_select_topk(self.rows, self.scores, self.max_len, self.wl.topk, self.sel,
+                            self.workspace, stream)
+
+    def mla_decode(self, stream=None):
+        wl = self.wl
+        api.dsa_mla_decode_fp8(self.rows, self.Q, self.pool, self.sel, wl.topk, wl.kv_scale,
+                               wl.sm_scale, self.out, self.lse, self.workspace, stream)
+
+    def step(self, stream=None):
+        """One pass of the whole hot path (S0 when the workload writes, S1-S3)."""
+        if self.kv_a is not None:
+            self.latent_write(stream)
+        self.index_scores(stream)
+        self.select_topk(stream)
+        self.mla_decode(stream)
+
+    # ---- host views of the results
+    def out_f32(self) -> np.ndarray:
+        return self.out.view(torch.bfloat16).float().cpu().numpy()
+
+
+class DsaDecoder:
+    """Host-facing decode: resident caches, per-step host inputs and outputs.
+
+    The caches (key arena, gate, FP8 latent pool) live on the device; each
+    ``decode`` call stages the step's inputs in pinned host buffers, copies
+    them to the device, runs S0-S3 and copies the attention output back."""
+
+    def __init__(self, wl, device: str | torch.device = "cuda"):
+        self.dw = DeviceWorkload(wl, device)
+        dw = self.dw
+        self._host_in = {}
+        for name in ("q_idx", "head_w", "Q", "seq_lens", "positions", "slots", "block_table",
+                     "idx_base") + (("kv_a",) if dw.kv_a is not None else ()):
+            t = getattr(dw, name)
+            self._host_in[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        self.host_out = torch.empty(dw.out.shape, dtype=dw.out.dtype, pin_memory=True)
+
+    @property
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self._host_in.values())
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.host_out.numel() * self.host_out.element_size()
+
+    def stage(self, wl) -> None:
+        """Fill the pinned input buffers from a workload's per-step arrays."""
+        src = {"q_idx": wl.q_idx, "head_w": wl.head_w, "Q": wl.Q.view(np.int16),
+               "seq_lens": wl.seq_lens.astype(np.int32), "positions": wl.positions.astype(np.int32),
+               "slots": wl.slots.astype(np.int64), "block_table": wl.block_table.astype(np.int32),
+               "idx_base": wl.idx_base.astype(np.int64)}
+        if "kv_a" in self._host_in:
+            src["kv_a"] = wl.kv_a.view(np.int16)
+        for k, t in self._host_in.items():
+            t.copy_(torch.from_numpy(np.ascontiguousarray(src[k])))
+
+    def decode(self, stream=None) -> torch.Tensor:
+        """Copy staged inputs in, run the path, copy the output out (async on
+        the stream; synchronise before reading ``host_out``)."""
+        dw = self.dw
+        for k, t in self._host_in.items():
+            getattr(dw, k).copy_(t, non_blocking=True)
+        dw.step(stream)
+        self.host_out.copy_(dw.out, non_blocking=True)
+        return self.host_out

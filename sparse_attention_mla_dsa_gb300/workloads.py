@@ -120,10 +120,11 @@ def make_workload(name: str, seed: int, *, seqs: int, rows_per_seq: int, len_kin
                   free_fraction: float = 0.0, shuffle_blocks: bool = True,
                   with_write: bool = False, kv_scale: float = 0.02,
                   sm_scale: float = 256 ** -0.5, eps: float = 1e-6,
-                  shared_table: bool = False) -> Workload:
+                  shared_table: bool = False, lens=None) -> Workload:
     """Draw one workload.  ``len_kind``: 'fixed' (len_lo), 'uniform' (integers
     in [len_lo, len_hi]) or 'loguniform' (exp of uniform in [ln lo, ln hi],
     floored).  A sequence's rows have lens base, base+1, ... (K-token verify).
+    'list' takes the per-sequence lens from ``lens``.
     ``pool_blocks`` defaults to the blocks needed / (1 - free_fraction)."""
     rng = np.random.default_rng(seed)
     rows = seqs * rows_per_seq
@@ -133,6 +134,9 @@ def make_workload(name: str, seed: int, *, seqs: int, rows_per_seq: int, len_kin
         base = np.full(seqs, len_lo, np.int64)
     elif len_kind == "uniform":
         base = rng.integers(len_lo, len_hi, size=seqs, endpoint=True).astype(np.int64)
+    elif len_kind == "list":
+        base = np.asarray(lens, np.int64)
+        assert base.shape == (seqs,)
     elif len_kind == "loguniform":
         u = rng.uniform(math.log(len_lo), math.log(len_hi), size=seqs)
         base = np.floor(np.exp(u)).astype(np.int64)
@@ -257,3 +261,16 @@ def scaled(name: str, seqs: int | None = None, len_div: int = 8, **overrides) ->
     spec.update(overrides)
     seed = spec.pop("seed")
     return make_workload(f"{name}/len{len_div}", seed, **spec)
+
+
+def select_rows(wl: Workload, rows) -> Workload:
+    """A workload holding only the given rows of ``wl`` (same arena, pool and
+    tables): used to run rows one at a time against a batched call."""
+    rows = np.asarray(rows, dtype=np.int64)
+    bt = wl.block_table if wl.bt_stride == 0 else wl.block_table[rows]
+    return dataclasses.replace(
+        wl, name=f"{wl.name}/rows{list(rows)}", rows=len(rows), group_rows=1,
+        seq_lens=wl.seq_lens[rows], positions=wl.positions[rows], slots=wl.slots[rows],
+        block_table=bt, idx_base=wl.idx_base[rows], q_idx=wl.q_idx[rows],
+        head_w=wl.head_w[rows], Q=wl.Q[rows],
+        kv_a=None if wl.kv_a is None else wl.kv_a[rows])

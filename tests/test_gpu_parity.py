@@ -1,0 +1,172 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Element-by-element on reduced copies of the five named workloads (same head
+counts, index geometry, topk and structure; shorter contexts so the oracle
+finishes in seconds, still several 128-token tiles with ragged tails), plus
+the K-row bit-identity of a verify batch against the same rows run one at a
+time, the shared-table form, and device-side error reporting.
+"""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_mla_dsa_gb300 import workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_attention_mla_dsa_gb300 import api, path
+    api.load()
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    api.dsa_get_error(reset=True)
+    return api, path
+
+
+SMALL = {
+    "tiny": lambda: workloads.named("tiny"),
+    "single": lambda: workloads.scaled("single", len_div=8),
+    "batched": lambda: workloads.scaled("batched", seqs=4, len_div=16),
+    "verify": lambda: workloads.scaled("verify", seqs=2, len_div=32),
+    "long": lambda: workloads.scaled("long", seqs=6, len_div=16),
+}
+
+
+def _oracle_pool_after_write(oracle, wl):
+    pool = wl.pool.copy()
+    near = None
+    if wl.has_write:
+        _, near = oracle.latent_write(pool, wl.kv_a, wl.norm_w, wl.slots, wl.eps, wl.kv_scale)
+    return pool, near
+
+
+def check_path(oracle, api, path, wl, rows=None):
+    dw = path.DeviceWorkload(wl)
+    dw.step()
+    torch.cuda.synchronize()
+    code, row, count = api.dsa_get_error(reset=True)
+    assert code == 0, f"device error {api.DEVERR.get(code)} row {row} count {count}"
+
+    pool_after, near = _oracle_pool_after_write(oracle, wl)
+    if wl.has_write:
+        gpu_pool = dw.pool.cpu().numpy()
+        for r in range(wl.rows):
+            slot = int(wl.slots[r])
+            diff = gpu_pool[slot] != pool_after[slot]
+            assert not (diff & (near[r] == 0)).any(), f"latent bytes differ in row {r}"
+        assert np.array_equal(np.delete(gpu_pool, wl.slots, axis=0),
+                              np.delete(pool_after, wl.slots, axis=0)), "write touched other slots"
+
+    scores = dw.scores.cpu().numpy()
+    sel = dw.sel.cpu().numpy()
+    out = dw.out_f32()
+    lse = dw.lse.cpu().numpy()
+    rows = range(wl.rows) if rows is None else rows
+    for r in rows:
+        L = int(wl.seq_lens[r])
+        base = int(wl.idx_base[r])
+        s, A = oracle.index_scores_row(wl.q_idx[r], wl.head_w[r], wl.idx_k[base:],
+                                       wl.idx_gate[base:], L)
+        parity.assert_scores(scores[r, :L], s, A, f"{wl.name} row {r} scores")
+        # (b) exact on the GPU's own scores; set-equal to the oracle's own
+        # selection when the boundary gap exceeds the score tolerance.
+        own = oracle.select_topk_row(scores[r, :L].astype(np.float64), L, wl.topk)
+        assert np.array_equal(own, sel[r]), f"{wl.name} row {r}: top-k differs on GPU scores"
+        if parity.topk_gap_ok(s, A, min(wl.topk, L)):
+            ref_sel = oracle.select_topk_row(s, L, wl.topk)
+            assert np.array_equal(ref_sel, sel[r]), f"{wl.name} row {r}: top-k set differs"
+        bt = wl.block_table[r] if wl.bt_stride else wl.block_table[0]
+        o_ref, lse_ref = oracle.mla_decode_row(wl.Q[r], pool_after, bt, wl.block_size, L, sel[r],
+                                               wl.kv_scale, wl.sm_scale)
+        parity.assert_out(out[r], o_ref, f"{wl.name} row {r} out")
+        parity.assert_lse(lse[r], lse_ref, f"{wl.name} row {r} lse")
+    return dw
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_path_parity_small(dsa, oracle, name):
+    api, path = dsa
+    check_path(oracle, api, path, SMALL[name]())
+
+
+def test_shared_table_stride0(dsa, oracle):
+    api, path = dsa
+    wl = workloads.make_workload("shared", 31, seqs=1, rows_per_seq=1, len_kind="fixed",
+                                 len_lo=3000, len_hi=3000, heads=32, index_heads=16,
+                                 index_dim=128, topk=512, shared_table=True, with_write=True)
+    assert wl.bt_stride == 0
+    check_path(oracle, api, path, wl)
+
+
+def test_ragged_and_short_rows(dsa, oracle):
+    """Lens not a multiple of the 128-token tile, below topk, and tiny."""
+    api, path = dsa
+    wl = workloads.make_workload("ragged", 32, seqs=5, rows_per_seq=1, len_kind="list",
+                                 len_lo=0, len_hi=0, lens=[1, 129, 300, 301, 700], heads=16,
+                                 index_heads=32, index_dim=128, topk=300, with_write=True)
+    check_path(oracle, api, path, wl)
+
+
+def test_k_row_verify_bit_identical_to_serial(dsa, oracle):
+    """decode_k: a K-row verify launch equals K single-row launches bit for bit."""
+    api, path = dsa
+    wl = workloads.scaled("verify", seqs=2, len_div=32)
+    batch = path.DeviceWorkload(wl)
+    batch.step()
+    torch.cuda.synchronize()
+    for r in range(wl.rows):
+        one = path.DeviceWorkload(workloads.select_rows(wl, [r]))
+        one.step()
+        torch.cuda.synchronize()
+        L = int(wl.seq_lens[r])
+        assert torch.equal(batch.scores[r, :L], one.scores[0, :L]), f"row {r} scores"
+        assert torch.equal(batch.sel[r], one.sel[0]), f"row {r} sel"
+        assert torch.equal(batch.out[r], one.out[0]), f"row {r} out"
+        assert torch.equal(batch.lse[r], one.lse[0]), f"row {r} lse"
+    assert api.dsa_get_error(reset=True)[0] == 0
+
+
+def test_device_errors_are_reported_not_trapped(dsa):
+    api, path = dsa
+    wl = workloads.scaled("tiny", len_div=4)
+    dw = path.DeviceWorkload(wl)
+    dw.step()
+    torch.cuda.synchronize()
+    assert api.dsa_get_error(reset=True)[0] == 0
+    # a selected index past seq_len: recorded as a select error, skipped
+    dw.sel[0, 0] = int(wl.seq_lens[0]) + 5
+    dw.mla_decode()
+    code, row, _ = api.dsa_get_error(reset=True)
+    assert api.DEVERR[code] == "select" and row == 0
+    # a seq_len above max_len: recorded by the indexer, row skipped
+    dw.seq_lens[0] = dw.max_len + 1
+    dw.index_scores()
+    code, _, _ = api.dsa_get_error(reset=True)
+    assert api.DEVERR[code] == "seq_len"
+    dw.seq_lens[0] = int(wl.seq_lens[0])
+    # a slot outside the pool: the write is skipped
+    dw.slots[0] = dw.pool.shape[0] + 3
+    rows = api.make_rows(dw.seq_lens, dw.block_table, wl.block_size, dw.slots, None)
+    kv = torch.zeros((1, 512), dtype=torch.int16, device="cuda")
+    api.dsa_latent_write(rows, kv, kv[0], dw.pool, 1e-6, 0.02)
+    code, _, _ = api.dsa_get_error(reset=True)
+    assert api.DEVERR[code] == "slot"
+
+
+def test_host_argument_errors(dsa):
+    api, path = dsa
+    wl = workloads.scaled("tiny", len_div=4)
+    dw = path.DeviceWorkload(wl)
+    with pytest.raises(api.DsaError) as e:
+        api.dsa_mla_decode_fp8(dw.rows, dw.Q, dw.pool, dw.sel, wl.topk, wl.kv_scale, wl.sm_scale,
+                               dw.out, dw.lse, dw.workspace[:16])
+    assert e.value.status == 5
+    bad = torch.empty((1, 8, 512), dtype=torch.int16, device="cuda")
+    with pytest.raises(api.DsaError) as e:   # 8 heads: not a multiple of 16
+        api.dsa_mla_decode_fp8(dw.rows, bad, dw.pool, dw.sel, wl.topk, wl.kv_scale, wl.sm_scale,
+                               bad, None, dw.workspace)
+    assert e.value.status == 2
