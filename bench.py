@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA decode hot path on GB300.
+
+A step is one pass of the whole path -- latent write (when the workload writes
+new rows), indexer scores, top-k, FP8 gather-attend -- over one batch of the
+named synthetic workload (default "single": 1 decode row at 32k context, 64
+heads, index 32x128, topk 2048).  Inputs are resident in HBM; steps rotate over
+enough copies of the inputs (distinct device addresses) that the working set of
+a rotation exceeds twice the L2, so every step reads its keys and latent from
+HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference     # the FP64 CPU oracle on the host cores
+
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(weak scaling, no data exchange); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DSA decode rows/s (index+top-k+FP8 gather-attend) at 32k ctx; % HBM roofline"
+UNIT = "rows/s"
+DESCRIPTIONS = {
+    "tiny": "tiny: 1 row, len 4096, 16 heads x 512 latent FP8 paged (block 64), index 8x64, topk 256",
+    "single": "single decode: 1 row, len 32768, 64 heads x 512 latent FP8 paged (block 64), "
+              "index 32x128, topk 2048",
+    "batched": "batched decode: 32 seqs x 1 row, len U[8192,65536], 64 heads, index 32x128, topk 2048",
+    "verify": "K-token verify: 8 seqs x 4 rows (len..len+3), base U[65536,131072], 64 heads, "
+              "index 32x128, topk 2048",
+    "long": "long-context batch: 64 seqs x 1 row, len log-U[4096,131072], 128 heads, index 64x128, "
+            "topk 2048, latent write of the new row",
+}
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "index_scores_traffic.txt")
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="single", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        hi = max(sm)
+        loaded = [s for s in sm if s >= 0.5 * hi] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- helpers
+def _peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def _source_hash():
+    p = os.path.join(ROOT, "sparse_attention_mla_dsa_gb300", "csrc", "index_scores.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic_per_unit(workload):
+    """DRAM bytes per key token of the indexer from the committed ncu summary,
+    valid only while index_scores.cu is unchanged since the capture."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for ln in f:
+                if ":" in ln and not ln.lstrip().startswith("#"):
+                    k, v = ln.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256_16") != _source_hash():
+            return None
+        return float(kv["dram_bytes_per_key_token"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def stage_bytes(wl):
+    """Algorithmic bytes per launch of each stage for one step of ``wl``."""
+    D = wl.index_dim
+    keys = 0
+    key_tokens = 0
+    for g in range(0, wl.rows, wl.group_rows):
+        lmax = int(wl.seq_lens[g:g + wl.group_rows].max())
+        keys += lmax * (2 * D + 2)
+        key_tokens += lmax
+    sel = sum(min(wl.topk, int(L)) for L in wl.seq_lens)
+    return {
+        "latent_write": wl.rows * (512 * 2 + 512) if wl.has_write else 0,
+        "index_scores": keys,
+        "select_topk": sum(int(L) * 4 for L in wl.seq_lens) + wl.rows * wl.topk * 4,
+        "mla_decode": sel * 512 + wl.rows * 2 * wl.heads * 512 * 2,
+    }, key_tokens
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__
+    from sparse_attention_mla_dsa_gb300 import build as _b
+    if rank == 0 and _b.is_stale():
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from sparse_attention_mla_dsa_gb300 import api, path, workloads
+
+    wl = workloads.named(args.workload)
+    sb, key_tokens = stage_bytes(wl)
+    alg_bytes = wl.algorithmic_bytes()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    first = path.DeviceWorkload(wl, dev)
+    # Enough replicas that one rotation moves more than 2x L2 of inputs.
+    touched = max(alg_bytes, 1)
+    n_rep = max(2, min(64, math.ceil(2.0 * l2 / touched) + 1))
+    reps = [first] + [first.clone() for _ in range(n_rep - 1)]
+    stream = torch.cuda.current_stream()
+    stages = (["latent_write"] if wl.has_write else []) + ["index_scores", "select_topk", "mla_decode"]
+
+    def one_step(dw, evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        k = 1
+        if wl.has_write:
+            dw.latent_write()
+            if evs is not None:
+                evs[k].record(stream)
+                k += 1
+        dw.index_scores()
+        if evs is not None:
+            evs[k].record(stream)
+            k += 1
+        dw.select_topk()
+        if evs is not None:
+            evs[k].record(stream)
+            k += 1
+        dw.mla_decode()
+        if evs is not None:
+            evs[k].record(stream)
+
+    for i in range(max(3, args.warmup)):
+        one_step(reps[i % n_rep])
+    torch.cuda.synchronize()
+    code, row, _ = api.dsa_get_error(reset=True)
+    if code != 0:
+        raise RuntimeError(f"device error during warm-up: {api.DEVERR.get(code)} row {row}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(K):
+            one_step(reps[i % n_rep], evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    stage_ms = {s: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                for j, s in enumerate(stages)}
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    code, row, _ = api.dsa_get_error(reset=True)
+    if code != 0:
+        raise RuntimeError(f"device error during the timed steps: {api.DEVERR.get(code)} row {row}")
+
+    value = K * wl.rows * world / (elapsed_ms / 1e3)
+    peak, peak_kind = _peaks()
+    dominant = max(stages, key=lambda s: stage_ms[s])
+    ach = sb[dominant] / (stage_ms[dominant] / 1e3) / 1e9
+    traffic = None
+    if dominant == "index_scores":
+        per_tok = _traffic_per_unit(args.workload)
+        if per_tok is not None:
+            traffic = per_tok * key_tokens
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
+                "traffic": traffic, "algorithmic_bytes": sb[dominant],
+                "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+                "path_frac": round(alg_bytes / (elapsed_ms / K / 1e3) / 1e9 / peak, 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        del reps
+        torch.cuda.empty_cache()
+        dec = path.DsaDecoder(wl, dev, replicas=n_rep)
+        dec.stage(wl)
+        for i in range(max(3, args.warmup)):
+            dec.decode()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(K):
+            dec.decode()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": round(K * wl.rows * world / (ems / 1e3), 2), "unit": UNIT,
+               "h2d_bytes_per_step": dec.h2d_bytes, "d2h_bytes_per_step": dec.d2h_bytes}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, rows_target=None)
+
+    launches_per_step = len(stages) + 1   # the gather-attend is a split and a combine kernel
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": wl.rows,
+                   "algorithmic_bytes_per_step": alg_bytes,
+                   "l2": f"rotating {n_rep} input replicas at distinct addresses "
+                         f"({n_rep * alg_bytes / 1e6:.0f} MB of touched inputs per rotation, "
+                         f"L2 {l2 / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": K * launches_per_step, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+def _oracle_rows_per_s(wl, rows, threads):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.run_path_rows(wl, rows=rows, threads=threads)
+    return len(rows) / (time.perf_counter() - t0)
+
+
+def cpu_baseline(wl, rows_target=None):
+    """The oracle as it stands, rows in parallel over the host cores, on a
+    bounded sample of the workload's rows (about 10-30 s of CPU work)."""
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    n = rows_target or max(1, min(2 * cores, 64))
+    rows = [i % wl.rows for i in range(n)]
+    v = _oracle_rows_per_s(wl, rows, cores)
+    return {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} rows of the same workload (index over the full context, full-sort "
+                      f"top-k, gather-attend), rows spread over {cores} threads"}
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from sparse_attention_mla_dsa_gb300 import workloads
+    wl = workloads.named(args.workload)
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    for i in range(args.warmup):
+        _oracle_rows_per_s(wl, [i % wl.rows], 1)
+    # one step = one batch of rows; rows of the timed steps run over all cores
+    K = args.steps
+    rows_per_step = min(wl.rows, 4)
+    rows = [i % wl.rows for i in range(K * rows_per_step)]
+    t0 = time.perf_counter()
+    import oracle as o
+    o.run_path_rows(wl, rows=rows, threads=cores)
+    el = time.perf_counter() - t0
+    value = len(rows) / el
+    sample = (f"{K} steps x {rows_per_step} rows of the workload, rows over {cores} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(el / K * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": rows_per_step},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        if args.steps > 20:
+            args.steps = 20     # the oracle is slow; keep the run within minutes
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -67,7 +67,7 @@ def _load():
             lib.dsa_oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.dsa_oracle_latent_write_row.argtypes = [i32, P, P, f32, f32, P, P, P]
             lib.dsa_oracle_latent_write_row.restype = None
-            lib.dsa_oracle_index_scores_row.argtypes = [i32, i32, P, P, P, P, i64, P, P, P]
+            lib.dsa_oracle_index_scores_row.argtypes = [i32, i32, P, P, P, P, i64, P, P, P, P]
             lib.dsa_oracle_index_scores_row.restype = None
             lib.dsa_oracle_select_topk_row.argtypes = [i64, i32, P, P]
             lib.dsa_oracle_select_topk_row.restype = i32
@@ -145,7 +145,8 @@ def index_scores_row(q: np.ndarray, w: np.ndarray, k_seq: np.ndarray, gate_seq: 
     """Scores of one query row.  q [Hi, D] f32, w [Hi] f32, k_seq [*, D] bf16 bits,
     gate_seq [*] bf16 bits (views starting at the row's sequence base).
     tokens: optional int64 token list; otherwise tokens 0..n-1.
-    Returns (s f64[n], A f64[n])."""
+    Returns (s, A, M), each f64[n]: the score, the head-weighted ReLU magnitude
+    and the magnitude of the terms summed (see dsa_oracle.h)."""
     q = _c(q, np.float32)
     w = _c(w, np.float32)
     k_seq = _c(k_seq, np.uint16)
@@ -156,9 +157,11 @@ def index_scores_row(q: np.ndarray, w: np.ndarray, k_seq: np.ndarray, gate_seq: 
         n = tokens.shape[0]
     s = np.zeros(n, np.float64)
     a = np.zeros(n, np.float64)
+    m = np.zeros(n, np.float64)
     _load().dsa_oracle_index_scores_row(heads, dim, _ptr(q), _ptr(w), _ptr(k_seq),
-                                        _ptr(gate_seq), int(n), _ptr(tokens), _ptr(s), _ptr(a))
-    return s, a
+                                        _ptr(gate_seq), int(n), _ptr(tokens), _ptr(s), _ptr(a),
+                                        _ptr(m))
+    return s, a, m
 
 
 # --------------------------------------------------------------------------- S2
@@ -228,21 +231,21 @@ def run_path_rows(wl, rows=None, threads: int = 1, sel_from=None):
     def one(r):
         L = int(wl.seq_lens[r])
         base = int(wl.idx_base[r])
-        s, a = index_scores_row(wl.q_idx[r], wl.head_w[r], wl.idx_k[base:], wl.idx_gate[base:], L)
+        s, a, m = index_scores_row(wl.q_idx[r], wl.head_w[r], wl.idx_k[base:], wl.idx_gate[base:], L)
         sel = select_topk_row(s, L, wl.topk)
         use = sel if sel_from is None else sel_from[r]
         bt_row = wl.block_table[r] if wl.bt_stride else wl.block_table[0]
         out, lse = mla_decode_row(wl.Q[r], wl.pool, bt_row, wl.block_size, L, use,
                                   wl.kv_scale, wl.sm_scale)
-        return r, s, a, sel, out, lse
+        return r, s, a, m, sel, out, lse
 
     res = {}
     if threads <= 1:
         for r in rows:
-            rr, s, a, sel, out, lse = one(r)
-            res[rr] = dict(s=s, A=a, sel=sel, out=out, lse=lse)
+            rr, s, a, m, sel, out, lse = one(r)
+            res[rr] = dict(s=s, A=a, M=m, sel=sel, out=out, lse=lse)
     else:
         with ThreadPoolExecutor(max_workers=threads) as ex:
-            for rr, s, a, sel, out, lse in ex.map(one, rows):
-                res[rr] = dict(s=s, A=a, sel=sel, out=out, lse=lse)
+            for rr, s, a, m, sel, out, lse in ex.map(one, rows):
+                res[rr] = dict(s=s, A=a, M=m, sel=sel, out=out, lse=lse)
     return res

@@ -122,24 +122,30 @@ void dsa_oracle_latent_write_row(int dim, const uint16_t *kv_a_row,
 void dsa_oracle_index_scores_row(int heads, int dim, const float *q, const float *w,
                                  const uint16_t *k, const uint16_t *gate,
                                  int64_t n, const int64_t *tokens,
-                                 double *s_out, double *a_out)
+                                 double *s_out, double *a_out, double *m_out)
 {
     for (int64_t i = 0; i < n; ++i) {
         int64_t t = tokens ? tokens[i] : i;
         const uint16_t *kt = k + t * (int64_t)dim;
         double g = dsa_oracle_bf16_value(gate[t]);
-        double sum = 0.0, sum_abs = 0.0;
+        double sum = 0.0, sum_abs = 0.0, terms = 0.0;
         for (int h = 0; h < heads; ++h) {
-            double dot = 0.0;
-            for (int d = 0; d < dim; ++d)
-                dot += (double)q[h * dim + d] * dsa_oracle_bf16_value(kt[d]);
+            double dot = 0.0, dot_abs = 0.0;
+            for (int d = 0; d < dim; ++d) {
+                double term = (double)q[h * dim + d] * dsa_oracle_bf16_value(kt[d]);
+                dot += term;
+                dot_abs += fabs(term);
+            }
             double relu = dot > 0.0 ? dot : 0.0;
             sum += (double)w[h] * relu;
             sum_abs += fabs((double)w[h]) * relu;
+            terms += fabs((double)w[h]) * dot_abs;
         }
         s_out[i] = g * sum;
         if (a_out)
             a_out[i] = g * sum_abs;
+        if (m_out)
+            m_out[i] = g * terms;
     }
 }
 

@@ -58,14 +58,16 @@ void dsa_oracle_latent_write_row(int dim, const uint16_t *kv_a_row,
  *   a_h(t) = sum_d q[h][d] * k[t][d]
  *   s(t)   = gate[t] * sum_h w[h] * max(a_h(t), 0)
  *   A(t)   = gate[t] * sum_h |w[h]| * max(a_h(t), 0)   (magnitude scale for tolerances)
+ *   M(t)   = gate[t] * sum_h |w[h]| * sum_d |q[h][d] * k[t][d]|
+ *            (size of the terms summed: the conditioning scale of s(t))
  * q: [heads][dim] float; w: [heads] float (already carrying heads^-0.5);
  * k: [*][dim] bf16 bits for this row's sequence (token t at k + t*dim);
  * gate: [*] bf16 bits.  tokens: the n token indices to score, or NULL for
- * tokens 0..n-1.  s_out, a_out (optional): [n]. */
+ * tokens 0..n-1.  s_out: [n]; a_out, m_out (optional): [n]. */
 void dsa_oracle_index_scores_row(int heads, int dim, const float *q, const float *w,
                                  const uint16_t *k, const uint16_t *gate,
                                  int64_t n, const int64_t *tokens,
-                                 double *s_out, double *a_out);
+                                 double *s_out, double *a_out, double *m_out);
 
 /* S2 -- top-k of one row.  Orders tokens 0..len-1 by (score DESC, index ASC),
  * keeps the first min(topk, len), writes them to sel[0..] in ASCENDING index

@@ -29,8 +29,12 @@ def _dev(a: np.ndarray, device) -> torch.Tensor:
 class DeviceWorkload:
     """All inputs of a workload resident on one CUDA device, plus outputs."""
 
-    def __init__(self, wl, device: str | torch.device = "cuda", pool: torch.Tensor | None = None):
+    def __init__(self, wl, device: str | torch.device = "cuda", pool: torch.Tensor | None = None,
+                 _clone_of: "DeviceWorkload | None" = None):
         self.wl = wl
+        if _clone_of is not None:
+            self._init_clone(_clone_of)
+            return
         self.device = torch.device(device)
         d = self.device
         self.seq_lens = _dev(wl.seq_lens.astype(np.int32), d)
@@ -56,6 +60,26 @@ class DeviceWorkload:
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=d)
         self.rows = api.make_rows(self.seq_lens, self.block_table, wl.block_size, self.slots,
                                   self.positions, shared_table=(wl.bt_stride == 0))
+
+    def _init_clone(self, src: "DeviceWorkload"):
+        self.device = src.device
+        for name in ("seq_lens", "positions", "slots", "block_table", "pool", "idx_k", "idx_gate",
+                     "idx_base", "q_idx", "head_w", "Q", "kv_a", "norm_w", "scores", "sel", "out",
+                     "lse", "workspace"):
+            t = getattr(src, name)
+            setattr(self, name, None if t is None else t.clone())
+        self.max_len = src.max_len
+        wl = self.wl
+        self.rows = api.make_rows(self.seq_lens, self.block_table, wl.block_size, self.slots,
+                                  self.positions, shared_table=(wl.bt_stride == 0))
+
+    def clone(self) -> "DeviceWorkload":
+        """An independent copy at new device addresses (for cold-cache rotation)."""
+        return DeviceWorkload(self.wl, _clone_of=self)
+
+    def input_bytes(self) -> int:
+        return sum(getattr(self, n).numel() * getattr(self, n).element_size()
+                   for n in ("pool", "idx_k", "idx_gate", "Q", "q_idx"))
 
     # ---- the four steps
     def latent_write(self, stream=None):
@@ -96,9 +120,11 @@ class DsaDecoder:
     ``decode`` call stages the step's inputs in pinned host buffers, copies
     them to the device, runs S0-S3 and copies the attention output back."""
 
-    def __init__(self, wl, device: str | torch.device = "cuda"):
-        self.dw = DeviceWorkload(wl, device)
-        dw = self.dw
+    def __init__(self, wl, device: str | torch.device = "cuda", replicas: int = 1):
+        first = DeviceWorkload(wl, device)
+        self.replicas = [first] + [first.clone() for _ in range(replicas - 1)]
+        self._next = 0
+        dw = first
         self._host_in = {}
         for name in ("q_idx", "head_w", "Q", "seq_lens", "positions", "slots", "block_table",
                      "idx_base") + (("kv_a",) if dw.kv_a is not None else ()):
@@ -127,8 +153,10 @@ class DsaDecoder:
 
     def decode(self, stream=None) -> torch.Tensor:
         """Copy staged inputs in, run the path, copy the output out (async on
-        the stream; synchronise before reading ``host_out``)."""
-        dw = self.dw
+        the stream; synchronise before reading ``host_out``).  Successive
+        calls rotate over the resident cache replicas."""
+        dw = self.replicas[self._next]
+        self._next = (self._next + 1) % len(self.replicas)
         for k, t in self._host_in.items():
             getattr(dw, k).copy_(t, non_blocking=True)
         dw.step(stream)

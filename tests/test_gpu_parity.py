@@ -69,14 +69,14 @@ def check_path(oracle, api, path, wl, rows=None):
     for r in rows:
         L = int(wl.seq_lens[r])
         base = int(wl.idx_base[r])
-        s, A = oracle.index_scores_row(wl.q_idx[r], wl.head_w[r], wl.idx_k[base:],
+        s, A, M = oracle.index_scores_row(wl.q_idx[r], wl.head_w[r], wl.idx_k[base:],
                                        wl.idx_gate[base:], L)
-        parity.assert_scores(scores[r, :L], s, A, f"{wl.name} row {r} scores")
+        parity.assert_scores(scores[r, :L], s, A, M, f"{wl.name} row {r} scores")
         # (b) exact on the GPU's own scores; set-equal to the oracle's own
         # selection when the boundary gap exceeds the score tolerance.
         own = oracle.select_topk_row(scores[r, :L].astype(np.float64), L, wl.topk)
         assert np.array_equal(own, sel[r]), f"{wl.name} row {r}: top-k differs on GPU scores"
-        if parity.topk_gap_ok(s, A, min(wl.topk, L)):
+        if parity.topk_gap_ok(s, A, M, min(wl.topk, L)):
             ref_sel = oracle.select_topk_row(s, L, wl.topk)
             assert np.array_equal(ref_sel, sel[r]), f"{wl.name} row {r}: top-k set differs"
         bt = wl.block_table[r] if wl.bt_stride else wl.block_table[0]

@@ -146,17 +146,19 @@ def _to_f64(bits):
 def test_index_scores_brute_force(oracle):
     rng = np.random.default_rng(3)
     q, w, k, gate = _rand_index_case(rng, 4, 16, 37)
-    s, A = oracle.index_scores_row(q, w, k, gate, 37)
+    s, A, M = oracle.index_scores_row(q, w, k, gate, 37)
     kd, gd = _to_f64(k), _to_f64(gate)
     dots = kd @ q.astype(np.float64).T                       # [n, heads]
     ref = gd * (np.maximum(dots, 0) @ w.astype(np.float64))
     ref_a = gd * (np.maximum(dots, 0) @ np.abs(w.astype(np.float64)))
+    ref_m = gd * ((np.abs(kd) @ np.abs(q.astype(np.float64)).T) @ np.abs(w.astype(np.float64)))
     assert np.allclose(s, ref, rtol=1e-12, atol=1e-12)
     assert np.allclose(A, ref_a, rtol=1e-12, atol=1e-12)
-    assert (A >= np.abs(s) - 1e-12).all()
+    assert np.allclose(M, ref_m, rtol=1e-12, atol=1e-12)
+    assert (A >= np.abs(s) - 1e-12).all() and (M >= A - 1e-12).all()
     # token-list form gives the same numbers
     toks = np.array([36, 0, 5], np.int64)
-    s2, _ = oracle.index_scores_row(q, w, k, gate, 0, tokens=toks)
+    s2, _, _ = oracle.index_scores_row(q, w, k, gate, 0, tokens=toks)
     assert np.array_equal(s2, s[toks])
 
 
@@ -165,18 +167,18 @@ def test_index_scores_special_cases(oracle):
     q, _, k, _ = _rand_index_case(rng, 1, 32, 50)
     one = np.ones(1, np.float32)
     g1 = _bf16(np.ones(50))
-    s, _ = oracle.index_scores_row(q, one, k, g1, 50)
+    s, _, _ = oracle.index_scores_row(q, one, k, g1, 50)
     dots = _to_f64(k) @ q[0].astype(np.float64)
     assert np.allclose(s, np.maximum(dots, 0.0), rtol=1e-13, atol=1e-13)
     # linear in w
     q4, w4, k4, gate4 = _rand_index_case(rng, 4, 32, 20)
-    s_a, _ = oracle.index_scores_row(q4, w4, k4, gate4, 20)
-    s_b, _ = oracle.index_scores_row(q4, (w4 * np.float32(4.0)).astype(np.float32), k4, gate4, 20)
+    s_a, _, _ = oracle.index_scores_row(q4, w4, k4, gate4, 20)
+    s_b, _, _ = oracle.index_scores_row(q4, (w4 * np.float32(4.0)).astype(np.float32), k4, gate4, 20)
     assert np.allclose(s_b, 4.0 * s_a, rtol=1e-13, atol=1e-13)
     # every dot negative -> score exactly 0
     kneg = _bf16(-np.abs(rng.standard_normal((8, 32))))
     qpos = np.abs(rng.standard_normal((4, 32))).astype(np.float32)
-    s0, _ = oracle.index_scores_row(qpos, w4, kneg, gate4, 8)
+    s0, _, _ = oracle.index_scores_row(qpos, w4, kneg, gate4, 8)
     assert (s0 == 0.0).all()
 
 
@@ -313,8 +315,8 @@ def test_planted_wrong_operand_fails_decode_pin(oracle):
 def test_planted_missing_gate_fails_index_pin(oracle):
     rng = np.random.default_rng(15)
     q, w, k, gate = _rand_index_case(rng, 4, 16, 30)
-    s, _ = oracle.index_scores_row(q, w, k, gate, 30)
-    s_nogate, _ = oracle.index_scores_row(q, w, k, _bf16(np.ones(30)), 30)
+    s, _, _ = oracle.index_scores_row(q, w, k, gate, 30)
+    s_nogate, _, _ = oracle.index_scores_row(q, w, k, _bf16(np.ones(30)), 30)
     assert not np.allclose(s, s_nogate)
 
 
