@@ -172,6 +172,33 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uin
                               float *lse_or_null, void *workspace, size_t workspace_bytes,
                               void *stream);
 
+/*
+ * S3 without a workspace argument, for callers that cannot allocate device
+ * memory where they run the attend (inside CUDA-graph stream capture, under
+ * another allocator they may not call, or on a serving path that must not
+ * take cudaMalloc's device synchronisation).  No counterpart on the pages:
+ * it is the same computation as dsa_mla_decode_fp8, with the split partials
+ * kept in a device array inside the library instead of a caller workspace.
+ * It allocates nothing and calls no allocating routine.
+ *   - Limit: dsa_workspace_bytes(rows, heads, topk) must not exceed
+ *     DSA_NOALLOC_SCRATCH_BYTES (32 MiB), else DSA_ERR_UNSUPPORTED and
+ *     nothing is launched.  Every GPU that loads the library holds that
+ *     array until the process exits.
+ *   - The first call on a device looks the array's device address up
+ *     (once per device, that device current); make that first call before
+ *     any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls whose work overlaps on
+ *     the GPU (other streams, other threads) race on it: serialise them.
+ * Other arguments, results and errors are those of dsa_mla_decode_fp8.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES (32u << 20)
+dsa_status dsa_mla_decode_fp8_noalloc(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,
+                                      int64_t nslots, const int32_t *sel, int32_t topk,
+                                      int32_t heads, int32_t latent_dim, float kv_scale,
+                                      float sm_scale, uint16_t *out, float *lse_or_null,
+                                      void *stream);
+
 /* Device bytes of the caller-owned workspace that dsa_select_topk and
  * dsa_mla_decode_fp8 need for a call of this shape (0 on bad arguments). */
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);

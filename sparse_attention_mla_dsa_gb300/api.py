@@ -59,6 +59,7 @@ def load() -> ctypes.CDLL:
         "dsa_index_scores": [RP, P, P, P, P, i64, P, i32, i32, i32, i32, P, P],
         "dsa_select_topk": [RP, P, i32, i32, P, P, sz, P],
         "dsa_mla_decode_fp8": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, sz, P],
+        "dsa_mla_decode_fp8_noalloc": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P],
         "dsa_get_error": [P, P, P, i32],
     }
     for name, args in sig.items():
@@ -172,6 +173,23 @@ def dsa_mla_decode_fp8(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: tor
                                 _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
                                 workspace.numel() * workspace.element_size(), _stream(stream))
     _check("dsa_mla_decode_fp8", st)
+
+
+def dsa_mla_decode_fp8_noalloc(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: torch.Tensor,
+                               topk: int, kv_scale: float, sm_scale: float, out: torch.Tensor,
+                               lse: torch.Tensor | None, stream=None) -> None:
+    """dsa_mla_decode_fp8 for callers that cannot allocate a workspace: the
+    split partials live in the library's own device array (see include/dsa.h
+    for its size limit, the first-call set-up and the no-overlap rule)."""
+    lib = load()
+    heads = q.shape[-2]
+    st = lib.dsa_mla_decode_fp8_noalloc(ctypes.byref(rows), _ptr(q, torch.uint16, "q"),
+                                        _ptr(pool, torch.uint8, "pool"), pool.shape[0],
+                                        _ptr(sel, torch.int32, "sel"), int(topk), heads, q.shape[-1],
+                                        float(kv_scale), float(sm_scale),
+                                        _ptr(out, torch.uint16, "out"), _ptr(lse, torch.float32, "lse"),
+                                        _stream(stream))
+    _check("dsa_mla_decode_fp8_noalloc", st)
 
 
 def dsa_workspace_bytes(rows: int, heads: int, topk: int) -> int:

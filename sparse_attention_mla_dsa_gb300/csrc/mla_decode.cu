@@ -16,6 +16,8 @@
 // softmax in between.  A combine kernel merges the splits in fixed split
 // order.  The split count depends only on topk, so a row's result is the
 // same bit for bit whatever other rows share the launch.
+#include <mutex>
+
 #include "dsa_device.cuh"
 #include "dsa_internal.h"
 
@@ -307,3 +309,51 @@ cudaError_t launch_mla_decode(const DecodeParams& p, cudaStream_t stream) {
 }
 
 }  // namespace dsa
+
+// ------------------------------------------------------------------------------------------
+// Allocation-free gather-attend.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// attend: code that runs while a stream is being captured into a CUDA graph
+// (an allocation there would either fail or be baked into the graph), code
+// whose device memory is owned by another allocator that it may not call, and
+// serving loops that must not pay cudaMalloc's implicit device synchronisation
+// on the decode path.  For them the split partials live in this file-scope
+// device array instead of a caller-provided workspace.  The array is
+// DSA_NOALLOC_SCRATCH_BYTES long and every GPU that loads the library keeps
+// it until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[64] = {};
+}  // namespace
+
+extern "C" dsa_status dsa_mla_decode_fp8_noalloc(const dsa_rows* rows, const uint16_t* q,
+                                                 const uint8_t* pool, int64_t nslots,
+                                                 const int32_t* sel, int32_t topk, int32_t heads,
+                                                 int32_t latent_dim, float kv_scale,
+                                                 float sm_scale, uint16_t* out,
+                                                 float* lse_or_null, void* stream) {
+  if (rows == nullptr || rows->rows < 1 || heads < 1 || topk < 1) return DSA_ERR_INVALID_ARG;
+  if (dsa::decode_workspace_bytes(rows->rows, heads, topk) > DSA_NOALLOC_SCRATCH_BYTES)
+    return DSA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    // Host code cannot take the array's address directly (its name is a host
+    // stand-in); ask the runtime once per device, with that device current.
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return DSA_ERR_CUDA;
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  return dsa_mla_decode_fp8(rows, q, pool, nslots, sel, topk, heads, latent_dim, kv_scale,
+                            sm_scale, out, lse_or_null, scratch, DSA_NOALLOC_SCRATCH_BYTES,
+                            stream);
+}

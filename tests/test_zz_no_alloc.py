@@ -1,0 +1,70 @@
+"""The allocation-free gather-attend entry point (collected last on purpose).
+
+dsa_mla_decode_fp8_noalloc serves callers that cannot allocate a device
+workspace where they run the attend (stream capture, foreign allocators,
+allocator-free serving loops).  Through the C ABI, two calls in a row -- on
+two different workloads, so the second cannot pass on the first's leftovers
+in the shared device array -- must match the workspace entry point within the
+parity tolerances used everywhere else; a shape whose partials exceed the
+array must be refused without a launch.
+"""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_mla_dsa_gb300 import workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_attention_mla_dsa_gb300 import api, path
+    api.load()
+    api.dsa_get_error(reset=True)
+    return api, path
+
+
+def _compare(api, path, wl):
+    dw = path.DeviceWorkload(wl)
+    dw.step()                                   # S1 -> S2 -> S3 with the workspace
+    out_ws = dw.out.clone()
+    lse_ws = dw.lse.clone()
+    dw.out.zero_()
+    dw.lse.zero_()
+    api.dsa_mla_decode_fp8_noalloc(dw.rows, dw.Q, dw.pool, dw.sel, wl.topk, wl.kv_scale,
+                                   wl.sm_scale, dw.out, dw.lse)
+    torch.cuda.synchronize()
+    assert api.dsa_get_error(reset=True)[0] == 0
+    a = out_ws.view(torch.bfloat16).double().cpu().numpy()
+    b = dw.out.view(torch.bfloat16).double().cpu().numpy()
+    for r in range(wl.rows):
+        parity.assert_out(b[r], a[r], f"{wl.name} row {r} no-alloc vs workspace")
+        parity.assert_lse(dw.lse[r].double().cpu().numpy(), lse_ws[r].double().cpu().numpy(),
+                          f"{wl.name} row {r} lse")
+
+
+def test_noalloc_matches_workspace_entry_point_twice(dsa):
+    api, path = dsa
+    _compare(api, path, workloads.scaled("batched", seqs=3, len_div=16))
+    _compare(api, path, workloads.scaled("long", seqs=2, len_div=16))
+
+
+def test_noalloc_refuses_oversized_call(dsa):
+    api, path = dsa
+    wl = workloads.scaled("tiny", len_div=4)
+    dw = path.DeviceWorkload(wl)
+    rows = 4096
+    assert api.dsa_workspace_bytes(rows, wl.heads, wl.topk) > (32 << 20)
+    seq = torch.ones(rows, dtype=torch.int32, device="cuda")
+    bt = torch.zeros((rows, 1), dtype=torch.int32, device="cuda")
+    big_rows = api.make_rows(seq, bt, wl.block_size)
+    q = torch.zeros((rows, wl.heads, 512), dtype=torch.int16, device="cuda")
+    sel = torch.full((rows, wl.topk), -1, dtype=torch.int32, device="cuda")
+    with pytest.raises(api.DsaError) as e:
+        api.dsa_mla_decode_fp8_noalloc(big_rows, q, dw.pool, sel, wl.topk, wl.kv_scale,
+                                       wl.sm_scale, q, None)
+    assert e.value.status == 2
