@@ -140,8 +140,9 @@ dsa_status dsa_index_scores(const dsa_rows *rows, const float *q_idx, const floa
  * topk) = -1.  -0.0 and +0.0 compare equal.  Scores must not be NaN.
  *   scores [rows][max_len] fp32 (as written by dsa_index_scores)
  *   sel    [rows][topk] int32 (output)
- * topk in [1, 65536].  No workspace is used at present; pass the same
- * workspace as to dsa_mla_decode_fp8 (or NULL / 0).
+ * topk in [1, 65536]; max_len up to about 390k tokens (a row is held in
+ * shared memory by a cluster of up to 8 CTAs).  No workspace is used at
+ * present; pass the same workspace as to dsa_mla_decode_fp8 (or NULL / 0).
  */
 dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t max_len,
                            int32_t topk, int32_t *sel, void *workspace, size_t workspace_bytes,
@@ -161,10 +162,11 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  * A row with nothing selected gets out = 0 and lse = -inf.
  *   q   [rows][heads][latent_dim] bf16       pool [nslots][latent_dim] FP8
  *   sel [rows][topk] int32                   out  [rows][heads][latent_dim] bf16
- * latent_dim must be 512; heads a multiple of 16.  The work of a row is split
- * over its selection in a way that depends only on topk, so each row's result
- * is bit-identical whatever the other rows of the call are.  The workspace
- * holds the split partials: at least dsa_workspace_bytes(rows, heads, topk).
+ * latent_dim must be 512; heads a multiple of 16.  A row's selection is cut
+ * into at most 8 splits whose count depends only on topk, so each row's result
+ * is bit-identical whatever the other rows of the call are.  The splits of a
+ * (row, 16 heads) run as one thread-block cluster and merge on chip: the
+ * workspace arguments are reserved (may be NULL / 0).
  */
 dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,
                               int64_t nslots, const int32_t *sel, int32_t topk, int32_t heads,
@@ -173,14 +175,15 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uin
                               void *stream);
 
 /*
- * S3 without a workspace argument, for callers that cannot allocate device
- * memory where they run the attend (inside CUDA-graph stream capture, under
- * another allocator they may not call, or on a serving path that must not
- * take cudaMalloc's device synchronisation).  No counterpart on the pages:
- * it is the same computation as dsa_mla_decode_fp8, with the split partials
- * kept in a device array inside the library instead of a caller workspace.
- * It allocates nothing and calls no allocating routine.
- *   - Limit: dsa_workspace_bytes(rows, heads, topk) must not exceed
+ * S3 for callers that cannot allocate device memory where they run the
+ * attend (inside CUDA-graph stream capture, under another allocator they may
+ * not call, or on a serving path that must not take cudaMalloc's device
+ * synchronisation) and that also cannot use thread-block clusters.  No
+ * counterpart on the pages: it is the same computation as dsa_mla_decode_fp8,
+ * run as two kernels (per-split partials, then a combine in fixed split order)
+ * whose partials live in a device array inside the library instead of a
+ * caller workspace.  It allocates nothing and calls no allocating routine.
+ *   - Limit: dsa_noalloc_scratch_bytes(rows, heads, topk) must not exceed
  *     DSA_NOALLOC_SCRATCH_BYTES (32 MiB), else DSA_ERR_UNSUPPORTED and
  *     nothing is launched.  Every GPU that loads the library holds that
  *     array until the process exits.
@@ -199,8 +202,14 @@ dsa_status dsa_mla_decode_fp8_noalloc(const dsa_rows *rows, const uint16_t *q, c
                                       float sm_scale, uint16_t *out, float *lse_or_null,
                                       void *stream);
 
+/* Bytes of the library's array that dsa_mla_decode_fp8_noalloc needs for a
+ * call of this shape (0 on bad arguments). */
+size_t dsa_noalloc_scratch_bytes(int32_t rows, int32_t heads, int32_t topk);
+
 /* Device bytes of the caller-owned workspace that dsa_select_topk and
- * dsa_mla_decode_fp8 need for a call of this shape (0 on bad arguments). */
+ * dsa_mla_decode_fp8 need for a call of this shape.  The current kernels keep
+ * every intermediate on chip, so this is 0; the argument slots stay in the
+ * ABI for kernels that may need one. */
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 
 /*

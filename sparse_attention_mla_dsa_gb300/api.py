@@ -68,6 +68,8 @@ def load() -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     lib.dsa_workspace_bytes.argtypes = [i32, i32, i32]
     lib.dsa_workspace_bytes.restype = sz
+    lib.dsa_noalloc_scratch_bytes.argtypes = [i32, i32, i32]
+    lib.dsa_noalloc_scratch_bytes.restype = sz
     lib.dsa_bt_entries_needed.argtypes = [i64, i64, i64]
     lib.dsa_bt_entries_needed.restype = i64
     lib.dsa_status_string.argtypes = [ctypes.c_int]
@@ -163,7 +165,8 @@ def dsa_select_topk(rows: Rows, scores: torch.Tensor, max_len: int, topk: int, s
 
 def dsa_mla_decode_fp8(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: torch.Tensor, topk: int,
                        kv_scale: float, sm_scale: float, out: torch.Tensor,
-                       lse: torch.Tensor | None, workspace: torch.Tensor, stream=None) -> None:
+                       lse: torch.Tensor | None, workspace: torch.Tensor | None = None,
+                       stream=None) -> None:
     lib = load()
     heads = q.shape[-2]
     st = lib.dsa_mla_decode_fp8(ctypes.byref(rows), _ptr(q, torch.uint16, "q"),
@@ -171,16 +174,18 @@ def dsa_mla_decode_fp8(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: tor
                                 _ptr(sel, torch.int32, "sel"), int(topk), heads, q.shape[-1],
                                 float(kv_scale), float(sm_scale), _ptr(out, torch.uint16, "out"),
                                 _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
-                                workspace.numel() * workspace.element_size(), _stream(stream))
+                                0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                _stream(stream))
     _check("dsa_mla_decode_fp8", st)
 
 
 def dsa_mla_decode_fp8_noalloc(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: torch.Tensor,
                                topk: int, kv_scale: float, sm_scale: float, out: torch.Tensor,
                                lse: torch.Tensor | None, stream=None) -> None:
-    """dsa_mla_decode_fp8 for callers that cannot allocate a workspace: the
-    split partials live in the library's own device array (see include/dsa.h
-    for its size limit, the first-call set-up and the no-overlap rule)."""
+    """dsa_mla_decode_fp8 for callers that can neither allocate device memory
+    nor use thread-block clusters: two kernels whose split partials live in
+    the library's own device array (see include/dsa.h for its size limit, the
+    first-call set-up and the no-overlap rule)."""
     lib = load()
     heads = q.shape[-2]
     st = lib.dsa_mla_decode_fp8_noalloc(ctypes.byref(rows), _ptr(q, torch.uint16, "q"),
@@ -194,6 +199,10 @@ def dsa_mla_decode_fp8_noalloc(rows: Rows, q: torch.Tensor, pool: torch.Tensor, 
 
 def dsa_workspace_bytes(rows: int, heads: int, topk: int) -> int:
     return int(load().dsa_workspace_bytes(int(rows), int(heads), int(topk)))
+
+
+def dsa_noalloc_scratch_bytes(rows: int, heads: int, topk: int) -> int:
+    return int(load().dsa_noalloc_scratch_bytes(int(rows), int(heads), int(topk)))
 
 
 def dsa_get_error(reset: bool = True) -> tuple[int, int, int]:

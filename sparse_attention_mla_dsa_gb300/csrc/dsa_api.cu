@@ -74,6 +74,12 @@ dsa_status check_rows(const dsa_rows* rows, bool need_table) {
 dsa_status launched(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
 }  // namespace
+
+int* device_error_word() {
+  const DeviceInfo* d = device_info();
+  return d ? d->err : nullptr;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -186,6 +192,8 @@ dsa_status dsa_select_topk(const dsa_rows* rows, const float* scores, int32_t ma
   p.rows = rows->rows;
   p.max_len = max_len;
   p.topk = topk;
+  p.cluster = topk_cluster_size(max_len);
+  if (topk_smem_bytes(max_len, p.cluster) > 227u * 1024u) return DSA_ERR_UNSUPPORTED;
   return launched(launch_select_topk(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -194,6 +202,8 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
                               int32_t latent_dim, float kv_scale, float sm_scale, uint16_t* out,
                               float* lse_or_null, void* workspace, size_t workspace_bytes,
                               void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
   dsa_status st = check_rows(rows, true);
   if (st != DSA_OK) return st;
   if (q == nullptr || pool == nullptr || sel == nullptr || out == nullptr || nslots < 1)
@@ -202,9 +212,6 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   if (heads < 16 || heads % 16 != 0 || heads > 4096) return DSA_ERR_UNSUPPORTED;
   if (topk < 1 || topk > 65536) return DSA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(out, 8)) return DSA_ERR_INVALID_ARG;
-  const size_t need = decode_workspace_bytes(rows->rows, heads, topk);
-  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
-    return DSA_ERR_WORKSPACE;
   const DeviceInfo* dev = device_info();
   if (dev == nullptr) return DSA_ERR_CUDA;
   DecodeParams p{};
@@ -217,20 +224,19 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   p.lse = lse_or_null;
   p.topk = topk;
   p.heads = heads;
-  p.splits = decode_splits(topk);
-  const size_t n = static_cast<size_t>(rows->rows) * p.splits * heads;
-  p.part_o = static_cast<float*>(workspace);
-  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                       ((n * 512 * sizeof(float) + 255) & ~static_cast<size_t>(255)));
   p.err = dev->err;
   p.kv_scale = kv_scale;
   p.sm_scale = sm_scale;
-  return launched(launch_mla_decode(p, static_cast<cudaStream_t>(stream)));
+  if (plan_mla_decode_tc(p)) return launched(launch_mla_decode_tc(p, static_cast<cudaStream_t>(stream)));
+  plan_mla_decode_cluster(p);
+  return launched(launch_mla_decode_cluster(p, static_cast<cudaStream_t>(stream)));
 }
 
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
-  if (rows < 1 || heads < 1 || topk < 1) return 0;
-  return decode_workspace_bytes(rows, heads, topk);
+  (void)rows;
+  (void)heads;
+  (void)topk;
+  return 0;  // the current kernels keep all intermediate state on chip
 }
 
 dsa_status dsa_get_error(int32_t* code_out, int32_t* row_out, int32_t* count_out, int32_t reset) {

@@ -11,6 +11,10 @@
 
 namespace dsa {
 
+// Device address of the sticky error word on the current device (nullptr on
+// failure); kernels receive it as an argument.
+int* device_error_word();
+
 // Bound on every mbarrier wait in the kernels (wall time).
 constexpr uint64_t kDefaultWaitNs = 500ull * 1000ull * 1000ull;
 
@@ -62,7 +66,10 @@ struct TopkParams {
   int32_t rows;
   int32_t max_len;
   int32_t topk;
+  int32_t cluster;   // CTAs per row (one thread-block cluster)
 };
+int topk_cluster_size(int32_t max_len);
+size_t topk_smem_bytes(int32_t max_len, int cluster);
 cudaError_t launch_select_topk(const TopkParams& p, cudaStream_t stream);
 
 struct DecodeParams {
@@ -79,11 +86,20 @@ struct DecodeParams {
   int32_t topk;
   int32_t heads;
   int32_t splits;
+  int32_t split_len;   // selection entries per split (cluster form)
   float kv_scale;
   float sm_scale;
 };
+// Two-kernel form (split + combine through a workspace of partials).
 int32_t decode_splits(int32_t topk);
 size_t decode_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 cudaError_t launch_mla_decode(const DecodeParams& p, cudaStream_t stream);
+// Tensor-core form (tcgen05, <= 16 splits of <= 128 entries); returns false
+// when the shape or the device does not allow it.
+bool plan_mla_decode_tc(DecodeParams& p);
+cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream);
+// Cluster form on warp-level MMAs (splits merged through distributed shared memory).
+void plan_mla_decode_cluster(DecodeParams& p);
+cudaError_t launch_mla_decode_cluster(const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace dsa

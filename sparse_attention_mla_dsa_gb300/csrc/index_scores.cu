@@ -88,26 +88,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nrows = min(p.sub_rows, seq_row0 + p.rows_per_seq - r0);
   const int nreal = nrows * p.heads;
 
-  if (threadIdx.x == 0) {
+  // Row lengths and arena bases: one load per row, all rows in parallel.
+  if (threadIdx.x < 32) {
     const bool report = blockIdx.x == 0;
-    const int64_t base = p.idx_base[seq_row0];
-    int maxlen = 0;
-    for (int j = 0; j < nrows; ++j) {
+    const int j = threadIdx.x;
+    const int64_t base = __ldg(p.idx_base + seq_row0);
+    int len = 0;
+    if (j < nrows) {
       const int r = r0 + j;
-      int len = p.seq_lens[r];
+      len = __ldg(p.seq_lens + r);
+      const int64_t rb = __ldg(p.idx_base + r);
       if (len < 0 || len > p.max_len) {
         if (report) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
         len = 0;
-      } else if (p.idx_base[r] != base || base < 0 || base + len > p.idx_tokens) {
+      } else if (rb != base || base < 0 || base + len > p.idx_tokens) {
         if (report) record_error(p.err, DSA_DEVERR_ARENA, r);
         len = 0;
       }
       ctl->row_len[j] = len;
-      maxlen = max(maxlen, len);
     }
-    ctl->max_len_group = maxlen;
-    ctl->base = base;
-    ctl->abort_flag = 0;
+    int maxlen = len;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) maxlen = max(maxlen, __shfl_xor_sync(0xFFFFFFFFu, maxlen, o));
+    if (j == 0) {
+      ctl->max_len_group = maxlen;
+      ctl->base = base;
+      ctl->abort_flag = 0;
+    }
   }
   __syncthreads();
   const int tiles = (ctl->max_len_group + kTileM - 1) / kTileM;

@@ -318,9 +318,10 @@ cudaError_t launch_mla_decode(const DecodeParams& p, cudaStream_t stream) {
 // (an allocation there would either fail or be baked into the graph), code
 // whose device memory is owned by another allocator that it may not call, and
 // serving loops that must not pay cudaMalloc's implicit device synchronisation
-// on the decode path.  For them the split partials live in this file-scope
-// device array instead of a caller-provided workspace.  The array is
-// DSA_NOALLOC_SCRATCH_BYTES long and every GPU that loads the library keeps
+// on the decode path.  This entry point runs the two-kernel split + combine
+// form above (no thread-block clusters) with its split partials in this
+// file-scope device array instead of a caller-provided workspace.  The array
+// is DSA_NOALLOC_SCRATCH_BYTES long and every GPU that loads the library keeps
 // it until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
 
@@ -329,13 +330,29 @@ std::mutex g_noalloc_mutex;
 void* g_noalloc_addr[64] = {};
 }  // namespace
 
+extern "C" size_t dsa_noalloc_scratch_bytes(int32_t rows, int32_t heads, int32_t topk) {
+  if (rows < 1 || heads < 1 || topk < 1) return 0;
+  return dsa::decode_workspace_bytes(rows, heads, topk);
+}
+
 extern "C" dsa_status dsa_mla_decode_fp8_noalloc(const dsa_rows* rows, const uint16_t* q,
                                                  const uint8_t* pool, int64_t nslots,
                                                  const int32_t* sel, int32_t topk, int32_t heads,
                                                  int32_t latent_dim, float kv_scale,
                                                  float sm_scale, uint16_t* out,
                                                  float* lse_or_null, void* stream) {
-  if (rows == nullptr || rows->rows < 1 || heads < 1 || topk < 1) return DSA_ERR_INVALID_ARG;
+  if (rows == nullptr || rows->rows < 1 || rows->rows > 65535 || rows->seq_lens == nullptr ||
+      rows->block_table == nullptr || rows->block_size < 1 || rows->max_blocks_per_seq < 1 ||
+      rows->bt_stride < 0 || (rows->bt_stride != 0 && rows->bt_stride < rows->max_blocks_per_seq))
+    return DSA_ERR_INVALID_ARG;
+  if (q == nullptr || pool == nullptr || sel == nullptr || out == nullptr || nslots < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (latent_dim != DSA_LATENT_DIM) return DSA_ERR_UNSUPPORTED;
+  if (heads < 16 || heads % 16 != 0 || heads > 4096) return DSA_ERR_UNSUPPORTED;
+  if (topk < 1 || topk > 65536) return DSA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(pool) & 15) ||
+      (reinterpret_cast<uintptr_t>(out) & 7))
+    return DSA_ERR_INVALID_ARG;
   if (dsa::decode_workspace_bytes(rows->rows, heads, topk) > DSA_NOALLOC_SCRATCH_BYTES)
     return DSA_ERR_UNSUPPORTED;
   int dev = 0;
@@ -346,14 +363,34 @@ extern "C" dsa_status dsa_mla_decode_fp8_noalloc(const dsa_rows* rows, const uin
     // stand-in); ask the runtime once per device, with that device current.
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     if (g_noalloc_addr[dev] == nullptr) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
         return DSA_ERR_CUDA;
-      g_noalloc_addr[dev] = p;
+      g_noalloc_addr[dev] = addr;
     }
     scratch = g_noalloc_addr[dev];
   }
-  return dsa_mla_decode_fp8(rows, q, pool, nslots, sel, topk, heads, latent_dim, kv_scale,
-                            sm_scale, out, lse_or_null, scratch, DSA_NOALLOC_SCRATCH_BYTES,
-                            stream);
+  int* err = dsa::device_error_word();
+  if (err == nullptr) return DSA_ERR_CUDA;
+  dsa::DecodeParams p{};
+  p.rows = *rows;
+  p.q = q;
+  p.pool = pool;
+  p.nslots = nslots;
+  p.sel = sel;
+  p.out = out;
+  p.lse = lse_or_null;
+  p.topk = topk;
+  p.heads = heads;
+  p.splits = dsa::decode_splits(topk);
+  const size_t n = static_cast<size_t>(rows->rows) * p.splits * heads;
+  p.part_o = static_cast<float*>(scratch);
+  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) +
+                                       ((n * 512 * sizeof(float) + 255) & ~static_cast<size_t>(255)));
+  p.err = err;
+  p.kv_scale = kv_scale;
+  p.sm_scale = sm_scale;
+  return dsa::launch_mla_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DSA_OK
+             : DSA_ERR_CUDA;
 }

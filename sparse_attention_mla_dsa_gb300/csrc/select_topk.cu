@@ -4,11 +4,19 @@
 // the selection is taken under a total order (score DESC, then index ASC), so
 // the top-k set is unique; each row's result is a function of its own scores.
 //
-// One CTA of 1024 threads per row: a three-digit radix select (11 + 11 + 10
-// bits) over an order-preserving 32-bit key finds the k-th largest key T and
-// how many keys equal to T belong to the selection; a final in-order pass then
-// writes every token with key > T plus the lowest-index tokens with key == T,
-// in ascending token order (block-wide prefix sums keep the order).
+// One thread-block cluster of C CTAs per row (1024 threads each, C = 1 up to
+// 4k tokens, at most 8).  CTA c keeps tokens [c*S, (c+1)*S) of the row in
+// shared memory as order-preserving 32-bit keys, read from global once.  A
+// four-digit radix select (8 bits per digit) finds the key T of the k-th
+// largest token.  Scores bunch into few high-order bins, so every histogram
+// keeps one counter per (bin, lane): the 32 lanes of a warp never add to the
+// same address.  With C > 1 the per-CTA bin totals are summed through
+// distributed shared memory and every CTA takes the same decision.  The
+// output pass writes every token with key > T plus the lowest-index tokens
+// with key == T in ascending token order: slices are in index order, so a
+// prefix of the per-CTA counts over the cluster gives each CTA its output
+// offset and its share of the tied tokens, and block-wide prefix sums order
+// the writes inside it.
 #include "dsa_device.cuh"
 #include "dsa_internal.h"
 
@@ -17,12 +25,42 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 8;  // consecutive tokens per thread in the output pass
+constexpr int kBins = 256;             // 8-bit digits
+constexpr int kItems = 8;              // consecutive tokens per thread in the output pass
+constexpr int kKeysPerCta = 4096;      // target keys per CTA when choosing the cluster size
 
 // Larger float -> larger unsigned key; -0.0 is folded onto +0.0 first.
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t remote_addr(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+// Volatile (kept after the cluster barrier) without a memory clobber, so
+// consecutive remote loads are issued back to back.
+__device__ __forceinline__ int ld_remote_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ int2 ld_remote_s32x2(uint32_t addr) {
+  int2 v;
+  asm volatile("ld.shared::cluster.v2.s32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
 }
 
 // Exclusive prefix sum over the CTA; also returns the total.  Contains
@@ -53,82 +91,181 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total)
   return before + x - v;
 }
 
-__global__ void __launch_bounds__(kThreads) select_topk_kernel(TopkParams p) {
-  const int r = blockIdx.x;
-  const int tid = threadIdx.x;
-  __shared__ int hist[2048];
-  __shared__ int warp_tot[kWarps];
-  __shared__ int found_bin, found_above;
+struct TopkShared {
+  int hist[kBins * 32];          // [bin][lane] counters of the current pass
+  int bin_tot[4][kBins];         // per-pass bin totals of this CTA (read remotely)
+  alignas(8) int counts[2];      // this CTA's (key > T, key == T) counts
+  int warp_tot[kWarps];
+  int found_bin, found_above;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) select_topk_kernel(const TopkParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  TopkShared& sh = *reinterpret_cast<TopkShared*>(smem_raw);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkShared));
+  const int r = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t crank = cluster_rank();
+  const int C = p.cluster;
 
   int len = p.seq_lens[r];
   if (len < 0 || len > p.max_len) {
-    if (tid == 0) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
+    if (tid == 0 && crank == 0) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
     len = 0;
   }
-  const float* row = p.scores + static_cast<int64_t>(r) * p.max_len;
   int32_t* out = p.sel + static_cast<int64_t>(r) * p.topk;
   const int want = min(p.topk, len);
-
-  if (len <= p.topk) {  // everything visible is selected
-    for (int i = tid; i < p.topk; i += kThreads) out[i] = i < len ? i : -1;
+  if (len <= p.topk) {  // everything visible is selected (uniform over the cluster)
+    for (int i = crank * kThreads + tid; i < p.topk; i += C * kThreads) out[i] = i < len ? i : -1;
     return;
   }
 
-  // ---- radix select: find the key T of the want-th largest and how many
-  // keys equal to T are taken (`remaining` after the last digit).
+  // This CTA's slice of the row, as keys in shared memory.
+  const int per = (len + C - 1) / C;
+  const int lo = min(len, static_cast<int>(crank) * per);
+  const int n = min(len, lo + per) - lo;
+  const float* row = p.scores + static_cast<int64_t>(r) * p.max_len + lo;
+  for (int base = 0; base < n; base += 8 * kThreads) {  // eight loads in flight per thread
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + j * kThreads + tid;
+      v[j] = i < n ? __ldg(row + i) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + j * kThreads + tid;
+      if (i < n) keys[i] = order_key(v[j]);
+    }
+  }
+
+  // ---- radix select, 8 bits per pass from the top
   uint32_t prefix = 0, prefix_mask = 0;
   int remaining = want;
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int nb = pass == 2 ? 1024 : 2048;
-    for (int b = tid; b < nb; b += kThreads) hist[b] = 0;
-    __syncthreads();
-    for (int t = tid; t < len; t += kThreads) {
-      const uint32_t key = order_key(row[t]);
-      if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1);
-    }
-    __syncthreads();
-    // Thread i owns bins nb-1-2i and nb-2-2i (descending), so an exclusive
-    // scan gives the count of keys in bins above its first bin.
-    const int b0 = nb - 1 - 2 * tid, b1 = nb - 2 - 2 * tid;
-    const int c0 = b0 >= 0 ? hist[b0] : 0;
-    const int c1 = b1 >= 0 ? hist[b1] : 0;
-    int total;
-    const int above = block_excl_scan(c0 + c1, warp_tot, total);
-    if (b0 >= 0 && above < remaining && above + c0 >= remaining) {
-      found_bin = b0;
-      found_above = above;
-    } else if (b1 >= 0 && above + c0 < remaining && above + c0 + c1 >= remaining) {
-      found_bin = b1;
-      found_above = above + c0;
-    }
-    __syncthreads();
-    remaining -= found_above;
-    prefix |= static_cast<uint32_t>(found_bin) << shift;
-    prefix_mask |= static_cast<uint32_t>(nb - 1) << shift;
-    __syncthreads();  // found_* is rewritten by the next pass
-  }
-  const uint32_t thresh = prefix;
-  const int take_equal = remaining;  // >= 1
-
-  // ---- ordered output pass
-  int out_base = 0, eq_base = 0;
-  for (int c0 = 0; c0 < len; c0 += kThreads * kItems) {
-    const int t0 = c0 + tid * kItems;
-    uint32_t gt = 0, eq = 0;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
 #pragma unroll
-    for (int i = 0; i < kItems; ++i) {
-      const int t = t0 + i;
-      if (t < len) {
-        const uint32_t key = order_key(row[t]);
-        gt |= static_cast<uint32_t>(key > thresh) << i;
-        eq |= static_cast<uint32_t>(key == thresh) << i;
+    for (int j = 0; j < kBins * 32 / kThreads; ++j) sh.hist[tid + j * kThreads] = 0;
+    __syncthreads();
+#pragma unroll 8
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t key = keys[i];
+      if ((key & prefix_mask) == prefix) atomicAdd(&sh.hist[((key >> shift) & 255u) * 32 + lane], 1);
+    }
+    __syncthreads();
+    // Bin totals: 4 threads per bin, 8 lane counters each.
+    {
+      const int b = tid >> 2, q = tid & 3;
+      int t = 0;
+#pragma unroll
+      for (int l = 0; l < 8; ++l) t += sh.hist[b * 32 + q * 8 + l];
+      t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
+      t += __shfl_xor_sync(0xFFFFFFFFu, t, 2);
+      if (q == 0) sh.bin_tot[pass][b] = t;
+    }
+    if (C > 1) cluster_sync();  // every CTA's totals of this pass are visible
+    else __syncthreads();
+    // Warp w < 8 scans bins 255-32w .. 224-32w (descending order of bins).
+    if (warp < kBins / 32) {
+      const int b = kBins - 1 - (warp * 32 + lane);
+      int c = 0;
+      if (C > 1) {
+        int v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < C) v[k] = ld_remote_s32(remote_addr(&sh.bin_tot[pass][b], k));
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < C) c += v[k];
+      } else {
+        c = sh.bin_tot[pass][b];
+      }
+      int x = c;  // inclusive scan within the warp
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      sh.warp_tot[warp] = 0;  // placeholder, overwritten below
+      __syncwarp();
+      if (lane == 31) sh.warp_tot[warp] = x;
+      sh.hist[(warp * 32 + lane)] = x - c;   // exclusive within the warp (hist is free now)
+      sh.hist[kBins + warp * 32 + lane] = c;
+    }
+    __syncthreads();
+    if (warp < kBins / 32) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += sh.warp_tot[w];
+      const int above = before + sh.hist[warp * 32 + lane];
+      const int c = sh.hist[kBins + warp * 32 + lane];
+      if (above < remaining && above + c >= remaining) {
+        sh.found_bin = kBins - 1 - (warp * 32 + lane);
+        sh.found_above = above;
       }
     }
-    int eq_total;
-    const int eq_rank = eq_base + block_excl_scan(__popc(eq), warp_tot, eq_total);
+    __syncthreads();
+    remaining -= sh.found_above;
+    prefix |= static_cast<uint32_t>(sh.found_bin) << shift;
+    prefix_mask |= 255u << shift;
+    __syncthreads();  // found_* / hist are rewritten by the next pass
+  }
+  const uint32_t thresh = prefix;
+  const int take_equal = remaining;  // >= 1, counted over the whole row
+
+  // ---- this CTA's counts, then its offsets from the CTAs before it
+  int out_base = 0, eq_base = 0;
+  if (C > 1) {
+    int gt_n = 0, eq_n = 0;
+#pragma unroll 8
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t key = keys[i];
+      gt_n += key > thresh;
+      eq_n += key == thresh;
+    }
+    int gt_total, eq_total;
+    block_excl_scan(gt_n, sh.warp_tot, gt_total);
+    block_excl_scan(eq_n, sh.warp_tot, eq_total);
+    if (tid == 0) {
+      sh.counts[0] = gt_total;
+      sh.counts[1] = eq_total;
+    }
+    cluster_sync();
+    int2 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (c < static_cast<int>(crank)) v[c] = ld_remote_s32x2(remote_addr(&sh.counts[0], c));
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (c < static_cast<int>(crank)) {
+        out_base += v[c].x + min(v[c].y, max(0, take_equal - eq_base));
+        eq_base += v[c].y;
+      }
+  }
+
+  // ---- ordered output of this slice
+  for (int c0 = 0; c0 < n; c0 += kThreads * kItems) {
+    const int t0 = c0 + tid * kItems;
+    uint32_t gt = 0, eq = 0;
+    uint32_t kv[kItems];
+    if (t0 + kItems <= n) {  // two 16-byte loads (t0 is a multiple of 8)
+      const uint4 u0 = *reinterpret_cast<const uint4*>(keys + t0);
+      const uint4 u1 = *reinterpret_cast<const uint4*>(keys + t0 + 4);
+      kv[0] = u0.x; kv[1] = u0.y; kv[2] = u0.z; kv[3] = u0.w;
+      kv[4] = u1.x; kv[5] = u1.y; kv[6] = u1.z; kv[7] = u1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < kItems; ++i) kv[i] = t0 + i < n ? keys[t0 + i] : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+      if (t0 + i < n) {
+        gt |= static_cast<uint32_t>(kv[i] > thresh) << i;
+        eq |= static_cast<uint32_t>(kv[i] == thresh) << i;
+      }
+    }
+    int chunk_eq;
+    int rank = eq_base + block_excl_scan(__popc(eq), sh.warp_tot, chunk_eq);
     uint32_t take = gt;
-    int rank = eq_rank;
 #pragma unroll
     for (int i = 0; i < kItems; ++i) {
       if ((eq >> i) & 1u) {
@@ -136,22 +273,49 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(TopkParams p) {
         ++rank;
       }
     }
-    int take_total;
-    int pos = out_base + block_excl_scan(__popc(take), warp_tot, take_total);
+    int chunk_take;
+    int pos = out_base + block_excl_scan(__popc(take), sh.warp_tot, chunk_take);
 #pragma unroll
     for (int i = 0; i < kItems; ++i)
-      if ((take >> i) & 1u) out[pos++] = t0 + i;
-    eq_base += eq_total;
-    out_base += take_total;
+      if ((take >> i) & 1u) out[pos++] = lo + t0 + i;
+    eq_base += chunk_eq;
+    out_base += chunk_take;
   }
-  for (int i = want + tid; i < p.topk; i += kThreads) out[i] = -1;
+  for (int i = want + crank * kThreads + tid; i < p.topk; i += C * kThreads) out[i] = -1;
+  if (C > 1) cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace
 
+int topk_cluster_size(int32_t max_len) {
+  int c = (max_len + kKeysPerCta - 1) / kKeysPerCta;
+  return c < 1 ? 1 : (c > 8 ? 8 : c);
+}
+
+size_t topk_smem_bytes(int32_t max_len, int cluster) {
+  const size_t per = (static_cast<size_t>(max_len) + cluster - 1) / cluster;
+  return sizeof(TopkShared) + per * sizeof(uint32_t);
+}
+
 cudaError_t launch_select_topk(const TopkParams& p, cudaStream_t stream) {
-  select_topk_kernel<<<p.rows, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const size_t smem = topk_smem_bytes(p.max_len, p.cluster);
+  cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.cluster, p.rows, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, select_topk_kernel, p);
 }
 
 }  // namespace dsa

@@ -161,12 +161,16 @@ def test_host_argument_errors(dsa):
     api, path = dsa
     wl = workloads.scaled("tiny", len_div=4)
     dw = path.DeviceWorkload(wl)
-    with pytest.raises(api.DsaError) as e:
-        api.dsa_mla_decode_fp8(dw.rows, dw.Q, dw.pool, dw.sel, wl.topk, wl.kv_scale, wl.sm_scale,
-                               dw.out, dw.lse, dw.workspace[:16])
-    assert e.value.status == 5
     bad = torch.empty((1, 8, 512), dtype=torch.int16, device="cuda")
     with pytest.raises(api.DsaError) as e:   # 8 heads: not a multiple of 16
         api.dsa_mla_decode_fp8(dw.rows, bad, dw.pool, dw.sel, wl.topk, wl.kv_scale, wl.sm_scale,
-                               bad, None, dw.workspace)
+                               bad, None)
     assert e.value.status == 2
+    with pytest.raises(api.DsaError) as e:   # topk 0
+        api.dsa_select_topk(dw.rows, dw.scores, dw.max_len, 0, dw.sel)
+    assert e.value.status == 2
+    with pytest.raises(api.DsaError) as e:   # rows_per_seq not dividing rows
+        api.dsa_index_scores(dw.rows, dw.q_idx, dw.head_w, dw.idx_k, dw.idx_gate, dw.idx_base, 3,
+                             dw.max_len, dw.scores)
+    assert e.value.status == 1
+    assert api.dsa_get_error(reset=True)[0] == 0   # nothing was launched

@@ -1,8 +1,10 @@
 """The allocation-free gather-attend entry point (collected last on purpose).
 
-dsa_mla_decode_fp8_noalloc serves callers that cannot allocate a device
-workspace where they run the attend (stream capture, foreign allocators,
-allocator-free serving loops).  Through the C ABI, two calls in a row -- on
+dsa_mla_decode_fp8_noalloc serves callers that cannot allocate device memory
+where they run the attend (stream capture, foreign allocators, allocator-free
+serving loops) and cannot use thread-block clusters; its two kernels keep their
+split partials in the library's device array.  Through the C ABI, two calls in
+a row -- on
 two different workloads, so the second cannot pass on the first's leftovers
 in the shared device array -- must match the workspace entry point within the
 parity tolerances used everywhere else; a shape whose partials exceed the
@@ -58,7 +60,7 @@ def test_noalloc_refuses_oversized_call(dsa):
     wl = workloads.scaled("tiny", len_div=4)
     dw = path.DeviceWorkload(wl)
     rows = 4096
-    assert api.dsa_workspace_bytes(rows, wl.heads, wl.topk) > (32 << 20)
+    assert api.dsa_noalloc_scratch_bytes(rows, wl.heads, wl.topk) > (32 << 20)
     seq = torch.ones(rows, dtype=torch.int32, device="cuda")
     bt = torch.zeros((rows, 1), dtype=torch.int32, device="cuda")
     big_rows = api.make_rows(seq, bt, wl.block_size)
