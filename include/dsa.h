@@ -163,10 +163,12 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  *   q   [rows][heads][latent_dim] bf16       pool [nslots][latent_dim] FP8
  *   sel [rows][topk] int32                   out  [rows][heads][latent_dim] bf16
  * latent_dim must be 512; heads a multiple of 16.  A row's selection is cut
- * into at most 8 splits whose count depends only on topk, so each row's result
- * is bit-identical whatever the other rows of the call are.  The splits of a
- * (row, 16 heads) run as one thread-block cluster and merge on chip: the
- * workspace arguments are reserved (may be NULL / 0).
+ * into at most 16 splits whose count depends only on topk, so each row's
+ * result is bit-identical whatever the other rows of the call are.  The
+ * splits of a (row, 64 heads) run as one thread-block cluster; their partial
+ * outputs pass through the workspace (L2-resident, discarded after use), which
+ * must hold dsa_workspace_bytes(rows, heads, topk) bytes, 256-byte aligned
+ * (DSA_ERR_WORKSPACE otherwise).
  */
 dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,
                               int64_t nslots, const int32_t *sel, int32_t topk, int32_t heads,
@@ -178,11 +180,9 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uin
  * S3 for callers that cannot allocate device memory where they run the
  * attend (inside CUDA-graph stream capture, under another allocator they may
  * not call, or on a serving path that must not take cudaMalloc's device
- * synchronisation) and that also cannot use thread-block clusters.  No
- * counterpart on the pages: it is the same computation as dsa_mla_decode_fp8,
- * run as two kernels (per-split partials, then a combine in fixed split order)
- * whose partials live in a device array inside the library instead of a
- * caller workspace.  It allocates nothing and calls no allocating routine.
+ * synchronisation).  No counterpart on the pages: it is dsa_mla_decode_fp8
+ * with the split partials kept in a device array inside the library instead
+ * of a caller workspace.  It allocates nothing and calls no allocating routine.
  *   - Limit: dsa_noalloc_scratch_bytes(rows, heads, topk) must not exceed
  *     DSA_NOALLOC_SCRATCH_BYTES (32 MiB), else DSA_ERR_UNSUPPORTED and
  *     nothing is launched.  Every GPU that loads the library holds that
@@ -207,9 +207,8 @@ dsa_status dsa_mla_decode_fp8_noalloc(const dsa_rows *rows, const uint16_t *q, c
 size_t dsa_noalloc_scratch_bytes(int32_t rows, int32_t heads, int32_t topk);
 
 /* Device bytes of the caller-owned workspace that dsa_select_topk and
- * dsa_mla_decode_fp8 need for a call of this shape.  The current kernels keep
- * every intermediate on chip, so this is 0; the argument slots stay in the
- * ABI for kernels that may need one. */
+ * dsa_mla_decode_fp8 need for a call of this shape (the gather-attend's split
+ * partials; 0 when no workspace is needed or on bad arguments). */
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 
 /*

@@ -182,10 +182,10 @@ def dsa_mla_decode_fp8(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: tor
 def dsa_mla_decode_fp8_noalloc(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: torch.Tensor,
                                topk: int, kv_scale: float, sm_scale: float, out: torch.Tensor,
                                lse: torch.Tensor | None, stream=None) -> None:
-    """dsa_mla_decode_fp8 for callers that can neither allocate device memory
-    nor use thread-block clusters: two kernels whose split partials live in
-    the library's own device array (see include/dsa.h for its size limit, the
-    first-call set-up and the no-overlap rule)."""
+    """dsa_mla_decode_fp8 for callers that cannot allocate device memory where
+    they run the attend: the split partials live in the library's own device
+    array (see include/dsa.h for its size limit, the first-call set-up and the
+    no-overlap rule)."""
     lib = load()
     heads = q.shape[-2]
     st = lib.dsa_mla_decode_fp8_noalloc(ctypes.byref(rows), _ptr(q, torch.uint16, "q"),

@@ -202,8 +202,6 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
                               int32_t latent_dim, float kv_scale, float sm_scale, uint16_t* out,
                               float* lse_or_null, void* workspace, size_t workspace_bytes,
                               void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   dsa_status st = check_rows(rows, true);
   if (st != DSA_OK) return st;
   if (q == nullptr || pool == nullptr || sel == nullptr || out == nullptr || nslots < 1)
@@ -227,16 +225,20 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   p.err = dev->err;
   p.kv_scale = kv_scale;
   p.sm_scale = sm_scale;
-  if (plan_mla_decode_tc(p)) return launched(launch_mla_decode_tc(p, static_cast<cudaStream_t>(stream)));
+  if (plan_mla_decode_tc(p)) {
+    const size_t need = mla_decode_tc_workspace_bytes(rows->rows, heads, topk);
+    if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+      return DSA_ERR_WORKSPACE;
+    p.part_o = static_cast<float*>(workspace);
+    return launched(launch_mla_decode_tc(p, static_cast<cudaStream_t>(stream)));
+  }
   plan_mla_decode_cluster(p);
   return launched(launch_mla_decode_cluster(p, static_cast<cudaStream_t>(stream)));
 }
 
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
-  (void)rows;
-  (void)heads;
-  (void)topk;
-  return 0;  // the current kernels keep all intermediate state on chip
+  if (rows < 1 || heads < 1 || topk < 1) return 0;
+  return mla_decode_tc_workspace_bytes(rows, heads, topk);
 }
 
 dsa_status dsa_get_error(int32_t* code_out, int32_t* row_out, int32_t* count_out, int32_t reset) {

@@ -80,8 +80,7 @@ struct DecodeParams {
   const int32_t* sel;
   uint16_t* out;
   float* lse;
-  float* part_o;    // [rows][splits][heads][512]
-  float* part_ml;   // [rows][splits][heads][2]
+  float* part_o;    // workspace: [rows][head groups][splits][64][512] partial O
   int* err;
   int32_t topk;
   int32_t heads;
@@ -90,13 +89,10 @@ struct DecodeParams {
   float kv_scale;
   float sm_scale;
 };
-// Two-kernel form (split + combine through a workspace of partials).
-int32_t decode_splits(int32_t topk);
-size_t decode_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
-cudaError_t launch_mla_decode(const DecodeParams& p, cudaStream_t stream);
 // Tensor-core form (tcgen05, <= 16 splits of <= 128 entries); returns false
 // when the shape or the device does not allow it.
 bool plan_mla_decode_tc(DecodeParams& p);
+size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream);
 // Cluster form on warp-level MMAs (splits merged through distributed shared memory).
 void plan_mla_decode_cluster(DecodeParams& p);

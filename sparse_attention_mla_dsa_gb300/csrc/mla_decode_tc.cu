@@ -21,10 +21,12 @@
 //      the tile), P^T written as a 64 x 128 K-major f16 operand;
 //   4. O^T = V^T P^T: V^T is the same latent tile read as an MN-major operand
 //      (dims contiguous), 4 x 8 tcgen05.mma (M=128 dims, N=64 heads, K=16);
-//   5. every CTA pushes its unnormalised O rows straight from TMEM into the
-//      shared memory of the CTA that owns each head (distributed shared
-//      memory stores), and each owner merges its heads over the n splits in
-//      fixed split order from local shared memory.
+//   5. every CTA writes its unnormalised O rows from TMEM to the workspace
+//      (coalesced, L2-resident); after one cluster barrier the CTA that owns
+//      a head merges it over the n splits in fixed split order and then
+//      discards the L2 lines it consumed, so the partials never reach HBM.
+#include <mutex>
+
 #include "dsa_device.cuh"
 #include "dsa_internal.h"
 
@@ -105,8 +107,10 @@ __device__ __forceinline__ float ld_remote_f32(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ void st_remote_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+// Drop a 128-byte L2 line without writing it back (its contents become
+// undefined); used on partials that have been consumed.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 // 32 consecutive TMEM columns of this thread's lane (waited in the same asm).
 __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
@@ -135,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
   uint8_t* pop = qop + kQBytes;         // P^T, f16, [64 heads] x [128 tok], 2 sub-tiles
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
   float* sm_s = reinterpret_cast<float*>(qop);     // logits [64 heads][128 tok] after S^T
-  float* part = reinterpret_cast<float*>(tile);    // received partial O rows after O^T
 
   const int hg = blockIdx.y, r = blockIdx.z;
   const uint32_t split = cluster_rank();
@@ -381,89 +384,78 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     }
     tc_fence_after();
     // Warp w reads lane quarter w%4 (dims 32*(w%4) + lane of each block) of
-    // blocks mb = 2*(w/4), 2*(w/4)+1, all 64 heads.
-    float v[2][2][32];
+    // blocks mb = 2*(w/4), 2*(w/4)+1, all 64 heads, and writes them to this
+    // split's partial rows [64 heads][512] (32 lanes = 128 contiguous bytes).
     const int dl = (warp & 3) * 32 + lane;
-#pragma unroll
-    for (int bb = 0; bb < 2; ++bb)
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc)
-        tmem_load32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 64 +
-                        ((warp >> 2) * 2 + bb) * 64 + hc * 32,
-                    v[bb][hc]);
-    tc_fence_before();
-    // Every CTA of the cluster has finished its MMAs (so every tile region,
-    // the receive buffers, is free) before any remote store lands.
-    cluster_sync();
-    // Push: head h is owned by CTA h % n, at local row (h / n); row layout
-    // recv[split][row][512] in the owner's tile region.
-    const int per_cta = (kHeads + nsplit - 1) / nsplit;
+    float* mine = p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) *
+                                 (kHeads * 512);
 #pragma unroll
     for (int bb = 0; bb < 2; ++bb) {
-      const int d = ((warp >> 2) * 2 + bb) * 128 + dl;
+      const int mb = (warp >> 2) * 2 + bb;
 #pragma unroll
-      for (int hc = 0; hc < 2; ++hc)
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[32];
+        tmem_load32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 64 + mb * 64 + hc * 32,
+                    v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int h = hc * 32 + i;
-          if (h < nheads) {
-            const int owner = h % nsplit, row = h / nsplit;
-            st_remote_f32(remote_addr(part + (static_cast<int>(split) * per_cta + row) * 512 + d,
-                                      owner),
-                          v[bb][hc][i]);
-          }
-        }
+        for (int i = 0; i < 32; ++i) mine[(hc * 32 + i) * 512 + mb * 128 + dl] = v[i];
+      }
     }
+    tc_fence_before();
   }
-  cluster_sync();  // every pushed row and every (m, l) is in place
+  cluster_sync();  // every split's partial rows (global) and (m, l) (shared) are visible
 
-  // ---- merge of the owned heads h = split, split + n, ... over the n splits
+  // ---- merge of the owned heads h = split, split + n, ... over the n splits;
+  // 128 threads per head, 4 dims each, all loads in flight before any use.
+  const float* rows0 = p.part_o + (static_cast<int64_t>(r) * gridDim.y + hg) * nsplit * (kHeads * 512);
   const int per_cta = (kHeads + nsplit - 1) / nsplit;
-  for (int item = tid; item < per_cta * 64; item += kThreads) {
-    const int row = item >> 6, d8 = item & 63;
+  for (int item = tid; item < per_cta * 128; item += kThreads) {
+    const int row = item >> 7, d4 = item & 127;
     const int h = static_cast<int>(split) + row * nsplit;
-    if (h >= nheads) continue;
+    if (h >= nheads) continue;  // uniform over each group of 128 threads
     float mc[kMaxSplits], lc[kMaxSplits];
+    float4 vc[kMaxSplits];
 #pragma unroll
     for (int c = 0; c < kMaxSplits; ++c)
       if (c < nsplit) {
         mc[c] = ld_remote_f32(remote_addr(&ctl->m[h], c));
         lc[c] = ld_remote_f32(remote_addr(&ctl->l[h], c));
+        vc[c] = __ldcg(reinterpret_cast<const float4*>(rows0 + (c * kHeads + h) * 512) + d4);
       }
     float mmax = -INFINITY;
 #pragma unroll
     for (int c = 0; c < kMaxSplits; ++c)
       if (c < nsplit) mmax = fmaxf(mmax, mc[c]);
     float lsum = 0.0f;
-    float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (mmax != -INFINITY) {
 #pragma unroll
       for (int c = 0; c < kMaxSplits; ++c)
         if (c < nsplit) {
           const float f = exp2f(mc[c] - mmax);
           lsum += lc[c] * f;
-          const float4* src = reinterpret_cast<const float4*>(part + (c * per_cta + row) * 512 + d8 * 8);
-          const float4 v0 = src[0], v1 = src[1];
-          acc[0] += v0.x * f;
-          acc[1] += v0.y * f;
-          acc[2] += v0.z * f;
-          acc[3] += v0.w * f;
-          acc[4] += v1.x * f;
-          acc[5] += v1.y * f;
-          acc[6] += v1.z * f;
-          acc[7] += v1.w * f;
+          acc.x += vc[c].x * f;
+          acc.y += vc[c].y * f;
+          acc.z += vc[c].z * f;
+          acc.w += vc[c].w * f;
         }
     }
     const float scale = mmax != -INFINITY ? p.kv_scale / lsum : 0.0f;
-    uint4 packed;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.x) : "f"(acc[1] * scale), "f"(acc[0] * scale));
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.y) : "f"(acc[3] * scale), "f"(acc[2] * scale));
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.z) : "f"(acc[5] * scale), "f"(acc[4] * scale));
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.w) : "f"(acc[7] * scale), "f"(acc[6] * scale));
+    uint2 packed;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.x) : "f"(acc.y * scale), "f"(acc.x * scale));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.y) : "f"(acc.w * scale), "f"(acc.z * scale));
     const int64_t head = static_cast<int64_t>(r) * p.heads + head0 + h;
-    reinterpret_cast<uint4*>(p.out + head * 512)[d8] = packed;
-    if (d8 == 0 && p.lse != nullptr)
+    reinterpret_cast<uint2*>(p.out + head * 512)[d4] = packed;
+    if (d4 == 0 && p.lse != nullptr)
       p.lse[head] = mmax != -INFINITY ? (mmax + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+    // The 8 lanes that read one 128-byte line of a partial row have used it:
+    // drop the line from L2 instead of writing it back.
+    __syncwarp();
+    if ((d4 & 7) == 0) {
+#pragma unroll
+      for (int c = 0; c < kMaxSplits; ++c)
+        if (c < nsplit) discard_l2_line(rows0 + (c * kHeads + h) * 512 + d4 * 4);
+    }
   }
   cluster_sync();  // keep this CTA's shared memory alive until every reader is done
   if (warp == 1) {
@@ -516,6 +508,14 @@ bool plan_mla_decode_tc(DecodeParams& p) {
   return true;
 }
 
+size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
+  int n = (topk + kTok - 1) / kTok;
+  if (n > kMaxSplits) return 0;
+  if (n < 1) n = 1;
+  const size_t groups = static_cast<size_t>((heads + kHeads - 1) / kHeads);
+  return static_cast<size_t>(rows) * groups * n * kHeads * 512 * sizeof(float);
+}
+
 cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -542,3 +542,57 @@ cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream) {
 }
 
 }  // namespace dsa
+
+// ------------------------------------------------------------------------------------------
+// Allocation-free gather-attend.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// attend: code that runs while a stream is being captured into a CUDA graph
+// (an allocation there would either fail or be baked into the graph), code
+// whose device memory is owned by another allocator that it may not call, and
+// serving loops that must not pay cudaMalloc's implicit device synchronisation
+// on the decode path.  This entry point runs the same kernel as
+// dsa_mla_decode_fp8 with the split partials in this file-scope device array
+// instead of a caller-provided workspace.  The array is
+// DSA_NOALLOC_SCRATCH_BYTES long and every GPU that loads the library keeps it
+// until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[64] = {};
+}  // namespace
+
+extern "C" size_t dsa_noalloc_scratch_bytes(int32_t rows, int32_t heads, int32_t topk) {
+  if (rows < 1 || heads < 1 || topk < 1) return 0;
+  return dsa::mla_decode_tc_workspace_bytes(rows, heads, topk);
+}
+
+extern "C" dsa_status dsa_mla_decode_fp8_noalloc(const dsa_rows* rows, const uint16_t* q,
+                                                 const uint8_t* pool, int64_t nslots,
+                                                 const int32_t* sel, int32_t topk, int32_t heads,
+                                                 int32_t latent_dim, float kv_scale,
+                                                 float sm_scale, uint16_t* out,
+                                                 float* lse_or_null, void* stream) {
+  if (rows == nullptr || rows->rows < 1 || heads < 1 || topk < 1) return DSA_ERR_INVALID_ARG;
+  if (dsa_noalloc_scratch_bytes(rows->rows, heads, topk) > DSA_NOALLOC_SCRATCH_BYTES)
+    return DSA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    // Host code cannot take the array's address directly (its name is a host
+    // stand-in); ask the runtime once per device, with that device current.
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
+        return DSA_ERR_CUDA;
+      g_noalloc_addr[dev] = addr;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  return dsa_mla_decode_fp8(rows, q, pool, nslots, sel, topk, heads, latent_dim, kv_scale,
+                            sm_scale, out, lse_or_null, scratch, DSA_NOALLOC_SCRATCH_BYTES,
+                            stream);
+}

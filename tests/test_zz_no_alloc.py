@@ -2,9 +2,8 @@
 
 dsa_mla_decode_fp8_noalloc serves callers that cannot allocate device memory
 where they run the attend (stream capture, foreign allocators, allocator-free
-serving loops) and cannot use thread-block clusters; its two kernels keep their
-split partials in the library's device array.  Through the C ABI, two calls in
-a row -- on
+serving loops): it keeps the split partials in the library's own device array
+instead of a caller workspace.  Through the C ABI, two calls in a row -- on
 two different workloads, so the second cannot pass on the first's leftovers
 in the shared device array -- must match the workspace entry point within the
 parity tolerances used everywhere else; a shape whose partials exceed the
