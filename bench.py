@@ -57,6 +57,7 @@ def _args():
     ap.add_argument("--workload", default="single", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch every step eagerly (no CUDA graph)")
     return ap.parse_args()
 
 
@@ -195,7 +196,7 @@ def run_ours(args):
         __graft_entry__.build()
     if world > 1:
         torch.distributed.barrier()
-    from sparse_attention_mla_dsa_gb300 import api, path, workloads
+    from sparse_attention_mla_dsa_gb300 import api, path, shard, workloads
 
     wl = workloads.named(args.workload)
     sb, key_tokens = stage_bytes(wl)
@@ -206,29 +207,29 @@ def run_ours(args):
     touched = max(alg_bytes, 1)
     n_rep = max(2, min(64, math.ceil(2.0 * l2 / touched) + 1))
     reps = [first] + [first.clone() for _ in range(n_rep - 1)]
-    stream = torch.cuda.current_stream()
     stages = (["latent_write"] if wl.has_write else []) + ["index_scores", "select_topk", "mla_decode"]
 
     def one_step(dw, evs=None):
+        s = torch.cuda.current_stream()
         if evs is not None:
-            evs[0].record(stream)
+            evs[0].record(s)
         k = 1
         if wl.has_write:
             dw.latent_write()
             if evs is not None:
-                evs[k].record(stream)
+                evs[k].record(s)
                 k += 1
         dw.index_scores()
         if evs is not None:
-            evs[k].record(stream)
+            evs[k].record(s)
             k += 1
         dw.select_topk()
         if evs is not None:
-            evs[k].record(stream)
+            evs[k].record(s)
             k += 1
         dw.mla_decode()
         if evs is not None:
-            evs[k].record(stream)
+            evs[k].record(s)
 
     for i in range(max(3, args.warmup)):
         one_step(reps[i % n_rep])
@@ -237,8 +238,31 @@ def run_ours(args):
     if code != 0:
         raise RuntimeError(f"device error during warm-up: {api.DEVERR.get(code)} row {row}")
 
+    # One CUDA graph per input replica holding one whole step, with timing
+    # events recorded between the stages inside the graph.
+    graphs, mode = [], "eager"
+    if not args.eager:
+        try:
+            for dw in reps:
+                evs = [torch.cuda.Event(enable_timing=True, external=True)
+                       for _ in range(len(stages) + 1)]
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    one_step(dw, evs)
+                graphs.append((g, evs))
+            for g, _ in graphs:
+                g.replay()
+            torch.cuda.synchronize()
+            mode = "cuda-graph"
+        except (TypeError, RuntimeError) as ex:
+            graphs = []
+            torch.cuda.synchronize()
+            print(f"cuda graph capture unavailable ({ex}); timing eager launches", file=sys.stderr)
+
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    stream = torch.cuda.current_stream()
+    eager_evs = None if graphs else [[torch.cuda.Event(enable_timing=True)
+                                      for _ in range(len(stages) + 1)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -246,18 +270,19 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         start.record(stream)
         for i in range(K):
-            one_step(reps[i % n_rep], evs[i])
+            if graphs:
+                graphs[i % n_rep][0].replay()
+            else:
+                one_step(reps[i % n_rep], eager_evs[i])
         end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(end)
-    stage_ms = {s: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+    ev_sets = [evs for _, evs in graphs] if graphs else eager_evs
+    stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev_sets)
                 for j, s in enumerate(stages)}
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = shard.max_over_ranks(elapsed_ms)
     code, row, _ = api.dsa_get_error(reset=True)
     if code != 0:
         raise RuntimeError(f"device error during the timed steps: {api.DEVERR.get(code)} row {row}")
@@ -279,7 +304,8 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        del reps
+        del graphs, reps
+        torch.cuda.synchronize()
         torch.cuda.empty_cache()
         dec = path.DsaDecoder(wl, dev, replicas=n_rep)
         dec.stage(wl)
@@ -296,10 +322,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = shard.max_over_ranks(ems)
         e2e = {"value": round(K * wl.rows * world / (ems / 1e3), 2), "unit": UNIT,
                "h2d_bytes_per_step": dec.h2d_bytes, "d2h_bytes_per_step": dec.d2h_bytes}
 
@@ -317,7 +340,8 @@ def run_ours(args):
                    "l2": f"rotating {n_rep} input replicas at distinct addresses "
                          f"({n_rep * alg_bytes / 1e6:.0f} MB of touched inputs per rotation, "
                          f"L2 {l2 / 1e6:.0f} MB)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "launch": mode},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": K * launches_per_step, "clocks": clk.summary(),
     }

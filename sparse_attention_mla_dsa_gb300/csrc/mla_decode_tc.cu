@@ -51,7 +51,7 @@ struct __align__(8) Ctl {
   uint32_t tmem_base;
   int abort_flag;
   int64_t slot[kTok];
-  float qexp[kHeads], m[kHeads], l[kHeads];
+  float qexp[kHeads], m[kHeads], l[kHeads];  // qexp: per-head logit scale
 };
 constexpr uint32_t kCtlOff = kTileBytes + kQBytes + kPBytes;
 constexpr uint32_t kSmemBytes = kCtlOff + sizeof(Ctl) + 1024;  // + alignment slack
@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     if (amax > 0.0f) frexpf(amax, &e);  // amax < 2^e
     const int sh = max(-100, min(100, 14 - e));
     const float scale = ldexpf(1.0f, sh);
-    if (q == 0) ctl->qexp[h] = static_cast<float>(sh);
+    // Logit scale of this head: sm_scale * kv_scale * log2(e) / 2^sh.
+    if (q == 0)
+      ctl->qexp[h] = p.sm_scale * p.kv_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {  // 8 elements = one 16-byte chunk of the operand
       const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
@@ -304,12 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     float v[32];
     tmem_load32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + hh, v);
     const bool valid = tok < nj && ctl->slot[tok] >= 0;
-    const float base_scale = p.sm_scale * p.kv_scale * 1.4426950408889634f;
     __syncthreads();  // every thread has read Q's region as an MMA operand (bar_s) -> reuse it
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int h = hh + i;
-      sm_s[h * kTok + tok] = valid ? v[i] * base_scale * exp2f(-ctl->qexp[h]) : -INFINITY;
+      sm_s[h * kTok + tok] = valid ? v[i] * ctl->qexp[h] : -INFINITY;
     }
   }
   __syncthreads();

@@ -1,0 +1,53 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports every
+entry point include/dsa.h declares (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_four_path_calls():
+    names = _declared()
+    for need in ("dsa_latent_write", "dsa_index_scores", "dsa_select_topk", "dsa_mla_decode_fp8"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol():
+    from sparse_attention_mla_dsa_gb300 import build
+    path = build.build()
+    lib = ctypes.CDLL(path)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    lib.dsa_abi_version.restype = ctypes.c_int32
+    assert lib.dsa_abi_version() == 1
+
+
+def test_host_helpers_without_gpu():
+    from sparse_attention_mla_dsa_gb300 import build
+    lib = ctypes.CDLL(build.build())
+    lib.dsa_bt_entries_needed.restype = ctypes.c_int64
+    lib.dsa_bt_entries_needed.argtypes = [ctypes.c_int64] * 3
+    assert lib.dsa_bt_entries_needed(20, 3, 16) == 3        # layer.rs bt_trim_tests value
+    assert lib.dsa_bt_entries_needed(8, 1, 0) == 11
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    assert lib.dsa_status_string(5).startswith(b"workspace")
+    lib.dsa_workspace_bytes.restype = ctypes.c_size_t
+    lib.dsa_workspace_bytes.argtypes = [ctypes.c_int32] * 3
+    assert lib.dsa_workspace_bytes(1, 64, 2048) == 1 * 1 * 16 * 64 * 512 * 4
+    assert lib.dsa_workspace_bytes(0, 64, 2048) == 0
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "sparse_attention_mla_dsa_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "dsa_oracle" not in text, f
