@@ -81,6 +81,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   return false;
 }
 
+// ------------------------------------------------------------------ dependent launch
+// With programmatic stream serialisation a kernel may start while the one
+// before it in the stream is still running.  grid_dep_wait() blocks until the
+// previous kernel has completed and its writes are visible; every kernel here
+// calls it before it reads a predecessor's output or overwrites a buffer a
+// predecessor may still read.  grid_dep_launch() lets the next kernel start.
+// Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

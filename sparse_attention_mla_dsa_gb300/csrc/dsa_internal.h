@@ -11,6 +11,15 @@
 
 namespace dsa {
 
+// Launch attribute that lets a kernel start before its stream predecessor
+// finishes (it then waits with griddepcontrol.wait where it needs to).
+inline cudaLaunchAttribute dependent_launch_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // Device address of the sticky error word on the current device (nullptr on
 // failure); kernels receive it as an argument.
 int* device_error_word();

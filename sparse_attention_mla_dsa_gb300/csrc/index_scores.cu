@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_launch();
 
   // ---------------------------------------------------------------- layout
   const int npad = p.npad;
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const int heads = p.heads;
     const int cols_per_row = (heads % 16 == 0) ? heads : npad;  // heads%16 != 0 -> one row
+    grid_dep_wait();  // the previous top-k may still read the scores buffer
     for (int i = 0; i < ntiles; ++i) {
       if (__shfl_sync(0xFFFFFFFFu, aborted(ctl) ? 1 : 0, 0)) break;
       const int a = i & 1;
@@ -349,18 +351,18 @@ cudaError_t launch_index_scores(const IndexParams& p, const CUtensorMap& kmap,
   if (chunks > 0x7FFFFFFF || groups > 65535) return cudaErrorInvalidConfiguration;
   dim3 grid(static_cast<unsigned>(chunks), static_cast<unsigned>(groups));
   cudaError_t e;
-  if (p.dim == 64) {
-    e = cudaFuncSetAttribute(index_scores_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             p.smem_bytes);
-    if (e != cudaSuccess) return e;
-    index_scores_kernel<64><<<grid, kThreads, p.smem_bytes, stream>>>(kmap, p);
-  } else {
-    e = cudaFuncSetAttribute(index_scores_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             p.smem_bytes);
-    if (e != cudaSuccess) return e;
-    index_scores_kernel<128><<<grid, kThreads, p.smem_bytes, stream>>>(kmap, p);
-  }
-  return cudaGetLastError();
+  auto kernel = p.dim == 64 ? index_scores_kernel<64> : index_scores_kernel<128>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {dependent_launch_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, kmap, p);
 }
 
 }  // namespace dsa

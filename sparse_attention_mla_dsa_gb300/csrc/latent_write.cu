@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kThreads) latent_write_kernel(LatentWriteParam
   const int tid = threadIdx.x;
   __shared__ double warp_sum[kThreads / 32];
   __shared__ int skip;
+  grid_dep_launch();
 
   if (tid == 0) {
     int bad = 0;
@@ -94,14 +95,21 @@ __global__ void __launch_bounds__(kThreads) latent_write_kernel(LatentWriteParam
     packed |= static_cast<uint32_t>(encode_e4m3_rne(y * inv)) << (8 * i);
   }
   const int64_t slot = p.rows.slots[r];
+  grid_dep_wait();  // the previous gather-attend may still read the pool
   reinterpret_cast<uint32_t*>(p.pool + slot * 512)[tid] = packed;
 }
 
 }  // namespace
 
 cudaError_t launch_latent_write(const LatentWriteParams& p, cudaStream_t stream) {
-  latent_write_kernel<<<p.rows.rows, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.rows.rows, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {dependent_launch_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, latent_write_kernel, p);
 }
 
 }  // namespace dsa

@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
   const int head0 = hg * kHeads;
   const int nheads = min(kHeads, p.heads - head0);
 
+  grid_dep_launch();
   int len = p.rows.seq_lens[r];
   if (len < 0) {
     if (report && split == 0 && tid == 0) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
 #pragma unroll
     for (int j = 0; j < 16; ++j) qraw[j] = real ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
   }
+  grid_dep_wait();  // the selection comes from the kernel before
   if (tid < kTok) {
     int64_t slot = -1;
     if (tid < nj) {
@@ -532,13 +534,14 @@ cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = dependent_launch_attr();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, p);
 }
 

@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_topk_kernel(const TopkPara
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_rank();
   const int C = p.cluster;
+  grid_dep_wait();  // the scores come from the kernel before
+  grid_dep_launch();
 
   int len = p.seq_lens[r];
   if (len < 0 || len > p.max_len) {
@@ -308,13 +310,14 @@ cudaError_t launch_select_topk(const TopkParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = dependent_launch_attr();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, select_topk_kernel, p);
 }
 
