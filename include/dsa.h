@@ -163,12 +163,11 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  *   q   [rows][heads][latent_dim] bf16       pool [nslots][latent_dim] FP8
  *   sel [rows][topk] int32                   out  [rows][heads][latent_dim] bf16
  * latent_dim must be 512; heads a multiple of 16.  A row's selection is cut
- * into at most 16 splits whose count depends only on topk, so each row's
- * result is bit-identical whatever the other rows of the call are.  The
- * splits of a (row, 64 heads) run as one thread-block cluster; their partial
- * outputs pass through the workspace (L2-resident, discarded after use), which
- * must hold dsa_workspace_bytes(rows, heads, topk) bytes, 256-byte aligned
- * (DSA_ERR_WORKSPACE otherwise).
+ * into splits of at most 128 entries whose count depends only on topk, so each
+ * row's result is bit-identical whatever the other rows of the call are.  The
+ * splits' partial outputs pass through the workspace (L2-resident, discarded
+ * after the merge), which must hold dsa_workspace_bytes(rows, heads, topk)
+ * bytes, 256-byte aligned (DSA_ERR_WORKSPACE otherwise).
  */
 dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,
                               int64_t nslots, const int32_t *sel, int32_t topk, int32_t heads,

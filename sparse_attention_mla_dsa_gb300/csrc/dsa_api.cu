@@ -225,15 +225,12 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   p.err = dev->err;
   p.kv_scale = kv_scale;
   p.sm_scale = sm_scale;
-  if (plan_mla_decode_tc(p)) {
-    const size_t need = mla_decode_tc_workspace_bytes(rows->rows, heads, topk);
-    if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
-      return DSA_ERR_WORKSPACE;
-    p.part_o = static_cast<float*>(workspace);
-    return launched(launch_mla_decode_tc(p, static_cast<cudaStream_t>(stream)));
-  }
-  plan_mla_decode_cluster(p);
-  return launched(launch_mla_decode_cluster(p, static_cast<cudaStream_t>(stream)));
+  plan_mla_decode_tc(p);
+  const size_t need = mla_decode_tc_workspace_bytes(rows->rows, heads, topk);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return DSA_ERR_WORKSPACE;
+  mla_decode_tc_bind_workspace(p, workspace);
+  return launched(launch_mla_decode_tc(p, static_cast<cudaStream_t>(stream)));
 }
 
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {

@@ -90,6 +90,7 @@ struct DecodeParams {
   uint16_t* out;
   float* lse;
   float* part_o;    // workspace: [rows][head groups][splits][64][512] partial O
+  float* part_ml;   // workspace: [rows][head groups][splits][64] (max, sum)
   int* err;
   int32_t topk;
   int32_t heads;
@@ -98,13 +99,11 @@ struct DecodeParams {
   float kv_scale;
   float sm_scale;
 };
-// Tensor-core form (tcgen05, <= 16 splits of <= 128 entries); returns false
-// when the shape or the device does not allow it.
-bool plan_mla_decode_tc(DecodeParams& p);
+// Split count / length of the gather-attend (a function of topk only).
+void plan_mla_decode_tc(DecodeParams& p);
 size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
+void mla_decode_tc_bind_workspace(DecodeParams& p, void* workspace);
+// Split kernel (tcgen05) followed by the merge kernel.
 cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream);
-// Cluster form on warp-level MMAs (splits merged through distributed shared memory).
-void plan_mla_decode_cluster(DecodeParams& p);
-cudaError_t launch_mla_decode_cluster(const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace dsa

@@ -8,9 +8,9 @@
 // head:  z_j = sm_scale * kv_scale * (Q . e4m3(latent_j)),  p = softmax(z),
 //        out = kv_scale * sum_j p_j e4m3(latent_j),  lse = log sum_j exp(z_j).
 //
-// A row's selection is cut into n <= 16 splits of at most 128 entries (n is a
-// function of topk alone).  The n CTAs of one (row, 64-head group) form a
-// cluster; each CTA (8 warps) handles one split:
+// A row's selection is cut into n splits of at most 128 entries (n is a
+// function of topk alone); each CTA (8 warps) handles one split of one
+// (row, 64-head group):
 //   1. gathers its <= 128 selected latent rows (16-byte loads) and widens FP8
 //      to f16 (exact) into a 128 x 512 tile in the 128-byte-swizzled layout;
 //      loads Q (64 heads, each scaled by a power of two so its bf16 values are
@@ -21,10 +21,11 @@
 //      the tile), P^T written as a 64 x 128 K-major f16 operand;
 //   4. O^T = V^T P^T: V^T is the same latent tile read as an MN-major operand
 //      (dims contiguous), 4 x 8 tcgen05.mma (M=128 dims, N=64 heads, K=16);
-//   5. every CTA writes its unnormalised O rows from TMEM to the workspace
-//      (coalesced, L2-resident); after one cluster barrier the CTA that owns
-//      a head merges it over the n splits in fixed split order and then
-//      discards the L2 lines it consumed, so the partials never reach HBM.
+//   5. the split's unnormalised O rows and its (max, sum) go to the workspace
+//      (staged through shared memory, 16-byte coalesced stores, L2-resident).
+// A merge kernel, chained by programmatic dependent launch, combines the n
+// splits of every (row, head) in fixed split order and discards the L2 lines
+// it consumed, so the partials never reach HBM.
 #include <mutex>
 
 #include "dsa_device.cuh"
@@ -36,7 +37,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kHeads = 64;             // heads per CTA (MMA N)
 constexpr int kTok = 128;              // tokens per split (MMA M of S^T)
-constexpr int kMaxSplits = 16;
+constexpr int kMergeThreads = 128;     // merge kernel: one CTA per (row, head), 4 dims per thread
 constexpr uint32_t kTileBytes = kTok * 512 * 2;        // latent tile, f16: 8 sub-tiles of 16 KB
 constexpr uint32_t kSubTok = kTok * 128;               // one 64-dim sub-tile of the latent tile
 constexpr uint32_t kQBytes = kHeads * 512 * 2;         // Q operand, f16: 8 sub-tiles of 8 KB
@@ -51,7 +52,7 @@ struct __align__(8) Ctl {
   uint32_t tmem_base;
   int abort_flag;
   int64_t slot[kTok];
-  float qexp[kHeads], m[kHeads], l[kHeads];  // qexp: per-head logit scale
+  float qexp[kHeads];  // per-head logit scale
 };
 constexpr uint32_t kCtlOff = kTileBytes + kQBytes + kPBytes;
 constexpr uint32_t kSmemBytes = kCtlOff + sizeof(Ctl) + 1024;  // + alignment slack
@@ -88,25 +89,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool a_mn_major) 
   return (1u << 4) | (a_mn_major ? (1u << 15) : 0u) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-__device__ __forceinline__ uint32_t remote_addr(const void* local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float ld_remote_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
 // Drop a 128-byte L2 line without writing it back (its contents become
 // undefined); used on partials that have been consumed.
 __device__ __forceinline__ void discard_l2_line(const void* p) {
@@ -141,10 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
   float* sm_s = reinterpret_cast<float*>(qop);     // logits [64 heads][128 tok] after S^T
 
   const int hg = blockIdx.y, r = blockIdx.z;
-  const uint32_t split = cluster_rank();
+  const int split = blockIdx.x;
   const int nsplit = p.splits;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j0 = static_cast<int>(split) * p.split_len;
+  const int j0 = split * p.split_len;
   const int nj = max(0, min(p.split_len, p.topk - j0));
   const bool report = hg == 0;
   const int head0 = hg * kHeads;
@@ -341,10 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     }
     sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
     sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-    if (q == 0) {
-      ctl->m[h] = mx;
-      ctl->l[h] = sum;
-    }
+    if (q == 0)
+      reinterpret_cast<float2*>(p.part_ml)[((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) *
+                                               kHeads + h] = make_float2(mx, sum);
     // P^T row h: tokens q*32 .. q*32+31 = 4 chunks of 8 in sub-tile (q*32)/64.
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -387,11 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     }
     tc_fence_after();
     // Warp w reads lane quarter w%4 (dims 32*(w%4) + lane of each block) of
-    // blocks mb = 2*(w/4), 2*(w/4)+1, all 64 heads, and writes them to this
-    // split's partial rows [64 heads][512] (32 lanes = 128 contiguous bytes).
+    // blocks mb = 2*(w/4), 2*(w/4)+1, all 64 heads, into the free tile region
+    // as rows [64 heads][512 dims] (consecutive lanes -> consecutive floats).
+    float* stage = reinterpret_cast<float*>(tile);
     const int dl = (warp & 3) * 32 + lane;
-    float* mine = p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) *
-                                 (kHeads * 512);
 #pragma unroll
     for (int bb = 0; bb < 2; ++bb) {
       const int mb = (warp >> 2) * 2 + bb;
@@ -400,123 +380,111 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
         float v[32];
         tmem_load32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 64 + mb * 64 + hc * 32,
                     v);
+        if (bb == 0 && hc == 0) __syncthreads();  // every thread is past bar_o: the tile is free
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mine[(hc * 32 + i) * 512 + mb * 128 + dl] = v[i];
+        for (int i = 0; i < 32; ++i) stage[(hc * 32 + i) * 512 + mb * 128 + dl] = v[i];
       }
     }
     tc_fence_before();
+    __syncthreads();
+    // This split's partial rows, 16-byte coalesced stores (512 B per thread).
+    float4* dst = reinterpret_cast<float4*>(
+        p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) * (kHeads * 512));
+    const float4* src = reinterpret_cast<const float4*>(stage);
+#pragma unroll 8
+    for (int i = tid; i < kHeads * 128; i += kThreads) dst[i] = src[i];
   }
-  cluster_sync();  // every split's partial rows (global) and (m, l) (shared) are visible
-
-  // ---- merge of the owned heads h = split, split + n, ... over the n splits;
-  // 128 threads per head, 4 dims each, all loads in flight before any use.
-  const float* rows0 = p.part_o + (static_cast<int64_t>(r) * gridDim.y + hg) * nsplit * (kHeads * 512);
-  const int per_cta = (kHeads + nsplit - 1) / nsplit;
-  for (int item = tid; item < per_cta * 128; item += kThreads) {
-    const int row = item >> 7, d4 = item & 127;
-    const int h = static_cast<int>(split) + row * nsplit;
-    if (h >= nheads) continue;  // uniform over each group of 128 threads
-    float mc[kMaxSplits], lc[kMaxSplits];
-    float4 vc[kMaxSplits];
-#pragma unroll
-    for (int c = 0; c < kMaxSplits; ++c)
-      if (c < nsplit) {
-        mc[c] = ld_remote_f32(remote_addr(&ctl->m[h], c));
-        lc[c] = ld_remote_f32(remote_addr(&ctl->l[h], c));
-        vc[c] = __ldcg(reinterpret_cast<const float4*>(rows0 + (c * kHeads + h) * 512) + d4);
-      }
-    float mmax = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kMaxSplits; ++c)
-      if (c < nsplit) mmax = fmaxf(mmax, mc[c]);
-    float lsum = 0.0f;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (mmax != -INFINITY) {
-#pragma unroll
-      for (int c = 0; c < kMaxSplits; ++c)
-        if (c < nsplit) {
-          const float f = exp2f(mc[c] - mmax);
-          lsum += lc[c] * f;
-          acc.x += vc[c].x * f;
-          acc.y += vc[c].y * f;
-          acc.z += vc[c].z * f;
-          acc.w += vc[c].w * f;
-        }
-    }
-    const float scale = mmax != -INFINITY ? p.kv_scale / lsum : 0.0f;
-    uint2 packed;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.x) : "f"(acc.y * scale), "f"(acc.x * scale));
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.y) : "f"(acc.w * scale), "f"(acc.z * scale));
-    const int64_t head = static_cast<int64_t>(r) * p.heads + head0 + h;
-    reinterpret_cast<uint2*>(p.out + head * 512)[d4] = packed;
-    if (d4 == 0 && p.lse != nullptr)
-      p.lse[head] = mmax != -INFINITY ? (mmax + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
-    // The 8 lanes that read one 128-byte line of a partial row have used it:
-    // drop the line from L2 instead of writing it back.
-    __syncwarp();
-    if ((d4 & 7) == 0) {
-#pragma unroll
-      for (int c = 0; c < kMaxSplits; ++c)
-        if (c < nsplit) discard_l2_line(rows0 + (c * kHeads + h) * 512 + d4 * 4);
-    }
-  }
-  cluster_sync();  // keep this CTA's shared memory alive until every reader is done
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-int g_tc_cluster16[64] = {0};  // 1: 16-CTA clusters schedulable, -1: not
+// Merge of the n splits of one (row, head): 128 threads, 4 dims each, splits
+// in fixed order; the consumed partial lines are discarded from L2.
+__global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const DecodeParams p) {
+  const int h = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+  const int groups = (p.heads + kHeads - 1) / kHeads;
+  const int hg = h / kHeads, hl = h % kHeads;
+  const int nsplit = p.splits;
+  const int64_t base = (static_cast<int64_t>(r) * groups + hg) * nsplit;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  grid_dep_wait();  // the partials come from the kernel before
+  grid_dep_launch();
+  float mmax = -INFINITY;
+  for (int c = 0; c < nsplit; ++c) mmax = fmaxf(mmax, __ldcg(ml + (base + c) * kHeads + hl).x);
+  float lsum = 0.0f;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (mmax != -INFINITY) {
+    int c = 0;
+    for (; c + 8 <= nsplit; c += 8) {  // eight splits' loads in flight at a time
+      float2 mlc[8];
+      float4 vc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        mlc[u] = __ldcg(ml + (base + c + u) * kHeads + hl);
+        vc[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((base + c + u) * kHeads + hl) * 512) + tid);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float f = exp2f(mlc[u].x - mmax);
+        lsum += mlc[u].y * f;
+        acc.x += vc[u].x * f;
+        acc.y += vc[u].y * f;
+        acc.z += vc[u].z * f;
+        acc.w += vc[u].w * f;
+      }
+    }
+    for (; c < nsplit; ++c) {
+      const float2 mlc = __ldcg(ml + (base + c) * kHeads + hl);
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((base + c) * kHeads + hl) * 512) + tid);
+      const float f = exp2f(mlc.x - mmax);
+      lsum += mlc.y * f;
+      acc.x += v.x * f;
+      acc.y += v.y * f;
+      acc.z += v.z * f;
+      acc.w += v.w * f;
+    }
+  }
+  const float scale = mmax != -INFINITY ? p.kv_scale / lsum : 0.0f;
+  uint2 packed;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.x) : "f"(acc.y * scale), "f"(acc.x * scale));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.y) : "f"(acc.w * scale), "f"(acc.z * scale));
+  const int64_t head = static_cast<int64_t>(r) * p.heads + h;
+  reinterpret_cast<uint2*>(p.out + head * 512)[tid] = packed;
+  if (tid == 0 && p.lse != nullptr)
+    p.lse[head] = mmax != -INFINITY ? (mmax + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+  // Every lane has used its partial values: drop the consumed 128-byte lines
+  // (8 lanes share one) from L2 instead of writing them back.
+  __syncwarp();
+  if ((tid & 7) == 0)
+    for (int c = 0; c < nsplit; ++c)
+      discard_l2_line(p.part_o + ((base + c) * kHeads + hl) * 512 + tid * 4);
+}
 
 }  // namespace
 
-bool plan_mla_decode_tc(DecodeParams& p) {
+void plan_mla_decode_tc(DecodeParams& p) {
   int n = (p.topk + kTok - 1) / kTok;
-  if (n > kMaxSplits) return false;  // more than 16 x 128 entries: not this kernel
   if (n < 1) n = 1;
-  if (n > 8) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return false;
-    if (g_tc_cluster16[dev] == 0) {
-      int ok = -1;
-      if (cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                               1) == cudaSuccess &&
-          cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kSmemBytes)) == cudaSuccess) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(16, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kSmemBytes;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 16;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, mla_decode_tc_kernel, &cfg) == cudaSuccess &&
-            clusters > 0)
-          ok = 1;
-      }
-      cudaGetLastError();
-      g_tc_cluster16[dev] = ok;
-    }
-    if (g_tc_cluster16[dev] != 1) return false;
-  }
   p.splits = n;
   p.split_len = (p.topk + n - 1) / n;
-  return true;
 }
 
 size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
   int n = (topk + kTok - 1) / kTok;
-  if (n > kMaxSplits) return 0;
   if (n < 1) n = 1;
-  const size_t groups = static_cast<size_t>((heads + kHeads - 1) / kHeads);
-  return static_cast<size_t>(rows) * groups * n * kHeads * 512 * sizeof(float);
+  const size_t units = static_cast<size_t>(rows) * ((heads + kHeads - 1) / kHeads) * n * kHeads;
+  const size_t o_bytes = (units * 512 * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  return o_bytes + units * 2 * sizeof(float);
+}
+
+void mla_decode_tc_bind_workspace(DecodeParams& p, void* workspace) {
+  const size_t units =
+      static_cast<size_t>(p.rows.rows) * ((p.heads + kHeads - 1) / kHeads) * p.splits * kHeads;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                       ((units * 512 * sizeof(float) + 255) & ~static_cast<size_t>(255)));
 }
 
 cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream) {
@@ -524,25 +492,23 @@ cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  if (p.splits > 8) {
-    e = cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                             1);
-    if (e != cudaSuccess) return e;
-  }
+  cudaLaunchAttribute attr[1] = {dependent_launch_attr()};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, (p.heads + kHeads - 1) / kHeads, p.rows.rows);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.splits;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1] = dependent_launch_attr();
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, p);
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, p);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(p.heads, p.rows.rows, 1);
+  mcfg.blockDim = dim3(kMergeThreads, 1, 1);
+  mcfg.stream = stream;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&mcfg, mla_decode_merge_kernel, p);
 }
 
 }  // namespace dsa

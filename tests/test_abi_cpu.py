@@ -40,7 +40,8 @@ def test_host_helpers_without_gpu():
     assert lib.dsa_status_string(5).startswith(b"workspace")
     lib.dsa_workspace_bytes.restype = ctypes.c_size_t
     lib.dsa_workspace_bytes.argtypes = [ctypes.c_int32] * 3
-    assert lib.dsa_workspace_bytes(1, 64, 2048) == 1 * 1 * 16 * 64 * 512 * 4
+    units = 1 * 1 * 16 * 64                                  # rows x head groups x splits x 64
+    assert lib.dsa_workspace_bytes(1, 64, 2048) == units * 512 * 4 + units * 8
     assert lib.dsa_workspace_bytes(0, 64, 2048) == 0
 
 
