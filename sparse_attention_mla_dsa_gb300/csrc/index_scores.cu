@@ -319,6 +319,10 @@ void plan_index_scores(IndexParams& p, int num_sms) {
   const int64_t groups = static_cast<int64_t>(p.rows / p.rows_per_seq) * p.subs_per_seq;
   const int64_t upper = tiles_max * groups;
   int64_t chunk = (upper + 16LL * num_sms - 1) / (16LL * num_sms);
+  // Each CTA builds its q hi/lo operand (npad x D) before streaming keys: on
+  // large launches give it at least npad/8 tiles so that build stays small
+  // next to the key bytes it serves.
+  if (upper >= 8LL * num_sms) chunk = chunk > p.npad / 8 ? chunk : p.npad / 8;
   chunk = chunk < 1 ? 1 : (chunk > 16 ? 16 : chunk);
   p.chunk_tiles = static_cast<int32_t>(chunk);
 

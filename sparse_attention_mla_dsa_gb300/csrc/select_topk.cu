@@ -4,8 +4,8 @@
 // the selection is taken under a total order (score DESC, then index ASC), so
 // the top-k set is unique; each row's result is a function of its own scores.
 //
-// One thread-block cluster of C CTAs per row (1024 threads each, C = 1 up to
-// 4k tokens, at most 8).  CTA c keeps tokens [c*S, (c+1)*S) of the row in
+// One thread-block cluster of C CTAs per row (512 threads each, two CTAs per
+// SM; C = 1 up to 4k tokens, at most 8).  CTA c keeps tokens [c*S, (c+1)*S) of the row in
 // shared memory as order-preserving 32-bit keys, read from global once.  A
 // four-digit radix select (8 bits per digit) finds the key T of the k-th
 // largest token.  Scores bunch into few high-order bins, so every histogram
@@ -23,7 +23,7 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;             // 8-bit digits
 constexpr int kItems = 8;              // consecutive tokens per thread in the output pass
@@ -76,13 +76,13 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total)
   if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = warp_tot[lane];
+    int s = lane < kWarps ? warp_tot[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xFFFFFFFFu, s, o);
       if (lane >= o) s += y;
     }
-    warp_tot[lane] = s;  // inclusive over warps
+    if (lane < kWarps) warp_tot[lane] = s;  // inclusive over warps
   }
   __syncthreads();
   const int before = warp ? warp_tot[warp - 1] : 0;
@@ -99,7 +99,7 @@ struct TopkShared {
   int found_bin, found_above;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) select_topk_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   TopkShared& sh = *reinterpret_cast<TopkShared*>(smem_raw);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkShared));
@@ -155,14 +155,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_topk_kernel(const TopkPara
       if ((key & prefix_mask) == prefix) atomicAdd(&sh.hist[((key >> shift) & 255u) * 32 + lane], 1);
     }
     __syncthreads();
-    // Bin totals: 4 threads per bin, 8 lane counters each.
+    // Bin totals: 2 threads per bin, 16 lane counters each.
     {
-      const int b = tid >> 2, q = tid & 3;
+      const int b = tid >> 1, q = tid & 1;
       int t = 0;
 #pragma unroll
-      for (int l = 0; l < 8; ++l) t += sh.hist[b * 32 + q * 8 + l];
+      for (int l = 0; l < 16; ++l) t += sh.hist[b * 32 + q * 16 + l];
       t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
-      t += __shfl_xor_sync(0xFFFFFFFFu, t, 2);
       if (q == 0) sh.bin_tot[pass][b] = t;
     }
     if (C > 1) cluster_sync();  // every CTA's totals of this pass are visible
@@ -216,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_topk_kernel(const TopkPara
 
   // ---- this CTA's counts, then its offsets from the CTAs before it
   int out_base = 0, eq_base = 0;
+  bool exit_arrived = false;
   if (C > 1) {
     int gt_n = 0, eq_n = 0;
 #pragma unroll 8
@@ -242,6 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_topk_kernel(const TopkPara
         out_base += v[c].x + min(v[c].y, max(0, take_equal - eq_base));
         eq_base += v[c].y;
       }
+    // Last remote read done: arrive now, wait just before leaving, so no CTA
+    // exits while another may still read its shared memory.
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    exit_arrived = true;
   }
 
   // ---- ordered output of this slice
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_topk_kernel(const TopkPara
     out_base += chunk_take;
   }
   for (int i = want + crank * kThreads + tid; i < p.topk; i += C * kThreads) out[i] = -1;
-  if (C > 1) cluster_sync();  // no CTA leaves while another may still read its shared memory
+  if (exit_arrived) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace
