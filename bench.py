@@ -340,7 +340,9 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, rows_target=None)
 
-    launches_per_step = len(stages) + 1   # the gather-attend is a split and a combine kernel
+    # The gather-attend is one kernel, plus a combine kernel when a row's
+    # selection is cut into more than one split.
+    launches_per_step = len(stages) + (1 if api.decode_splits(wl.heads, wl.topk) > 1 else 0)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 5), "higher_is_better": True,

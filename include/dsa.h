@@ -162,12 +162,14 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  * A row with nothing selected gets out = 0 and lse = -inf.
  *   q   [rows][heads][latent_dim] bf16       pool [nslots][latent_dim] FP8
  *   sel [rows][topk] int32                   out  [rows][heads][latent_dim] bf16
- * latent_dim must be 512; heads a multiple of 16.  A row's selection is cut
- * into splits of at most 128 entries whose count depends only on topk, so each
- * row's result is bit-identical whatever the other rows of the call are.  The
- * splits' partial outputs pass through the workspace (L2-resident, discarded
- * after the merge), which must hold dsa_workspace_bytes(rows, heads, topk)
- * bytes, 256-byte aligned (DSA_ERR_WORKSPACE otherwise).
+ * latent_dim must be 512; heads a multiple of 16; nslots below 2^31
+ * (DSA_ERR_UNSUPPORTED otherwise).  A row's selection is cut into splits of
+ * at most 256 entries (512 with more than 64 heads) whose count depends only
+ * on topk and heads, so each row's result is bit-identical whatever the other
+ * rows of the call are.  With more than one split the partial outputs pass
+ * through the workspace (L2-resident, discarded after the merge), which must
+ * hold dsa_workspace_bytes(rows, heads, topk) bytes, 256-byte aligned
+ * (DSA_ERR_WORKSPACE otherwise).
  */
 dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,
                               int64_t nslots, const int32_t *sel, int32_t topk, int32_t heads,

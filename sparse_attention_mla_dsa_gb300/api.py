@@ -201,6 +201,13 @@ def dsa_workspace_bytes(rows: int, heads: int, topk: int) -> int:
     return int(load().dsa_workspace_bytes(int(rows), int(heads), int(topk)))
 
 
+def decode_splits(heads: int, topk: int) -> int:
+    """Splits per (row, 64-head group) of the gather-attend, read back from the
+    workspace size (one split's partials are 64 x (512 + 2) floats)."""
+    groups = (int(heads) + 63) // 64
+    return dsa_workspace_bytes(1, heads, topk) // (groups * 64 * (512 + 2) * 4)
+
+
 def dsa_noalloc_scratch_bytes(rows: int, heads: int, topk: int) -> int:
     return int(load().dsa_noalloc_scratch_bytes(int(rows), int(heads), int(topk)))
 

@@ -206,7 +206,7 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   if (st != DSA_OK) return st;
   if (q == nullptr || pool == nullptr || sel == nullptr || out == nullptr || nslots < 1)
     return DSA_ERR_INVALID_ARG;
-  if (latent_dim != DSA_LATENT_DIM) return DSA_ERR_UNSUPPORTED;
+  if (latent_dim != DSA_LATENT_DIM || nslots > INT32_MAX) return DSA_ERR_UNSUPPORTED;
   if (heads < 16 || heads % 16 != 0 || heads > 4096) return DSA_ERR_UNSUPPORTED;
   if (topk < 1 || topk > 65536) return DSA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(out, 8)) return DSA_ERR_INVALID_ARG;

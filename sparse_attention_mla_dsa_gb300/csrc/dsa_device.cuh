@@ -89,6 +89,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
 // predecessor may still read.  grid_dep_launch() lets the next kernel start.
 // Both are no-ops for kernels launched without the attribute.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Data written by an earlier kernel of the chain must be read with loads the
+// compiler keeps after grid_dep_wait(): plain loads, or these.  The
+// read-only-path intrinsics (__ldg, __ldcg, ...) are treated as loads of
+// memory that never changes and may be hoisted above the wait.
+__device__ __forceinline__ float2 ld_dep_f2(const float2* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_dep_f4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void grid_dep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -193,59 +210,6 @@ __device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// ------------------------------------------------------------------ warp MMA (gather-attend)
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                              uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Two E4M3 codes (low byte = first element) -> two bf16 values, packed with
-// the first element in the low half.  Every E4M3 value is exactly
-// representable in f16, f32 and bf16, so all three conversions are exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes) {
-  uint32_t out;
-  asm("{\n\t.reg .b16 lo, hi;\n\t.reg .b32 h2;\n\t.reg .f32 flo, fhi;\n\t"
-      "cvt.rn.f16x2.e4m3x2 h2, %1;\n\t"
-      "mov.b32 {lo, hi}, h2;\n\t"
-      "cvt.f32.f16 flo, lo;\n\t"
-      "cvt.f32.f16 fhi, hi;\n\t"
-      "cvt.rn.bf16x2.f32 %0, fhi, flo;\n\t}"
-      : "=r"(out)
-      : "h"(codes));
-  return out;
-}
-
-// cp.async 16 B global -> shared; src_bytes 0 writes zeros.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 }  // namespace dsa

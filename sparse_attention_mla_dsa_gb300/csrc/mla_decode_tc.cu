@@ -8,24 +8,36 @@
 // head:  z_j = sm_scale * kv_scale * (Q . e4m3(latent_j)),  p = softmax(z),
 //        out = kv_scale * sum_j p_j e4m3(latent_j),  lse = log sum_j exp(z_j).
 //
-// A row's selection is cut into n splits of at most 128 entries (n is a
-// function of topk alone); each CTA (8 warps) handles one split of one
-// (row, 64-head group):
-//   1. gathers its <= 128 selected latent rows (16-byte loads) and widens FP8
-//      to f16 (exact) into a 128 x 512 tile in the 128-byte-swizzled layout;
-//      loads Q (64 heads, each scaled by a power of two so its bf16 values are
-//      exact in f16) as a 64 x 512 K-major operand;
+// A row's selection is cut into n splits of at most 256 entries (512 when the
+// row has more than 64 heads); n and the split length depend on topk and the
+// head count only, never on the number of rows, so a row's arithmetic is the
+// same in any launch.  Each CTA (8 warps) runs one split of one (row, 64-head
+// group) as a loop over 128-entry tiles, with an online softmax:
+//   0. resolves the slots of all its entries once, loads Q (64 heads, each
+//      scaled by a power of two so its bf16 values are exact in f16) as a
+//      64 x 512 K-major operand that stays resident;
+//   1. widens the tile's FP8 latent rows (already in registers) to f16
+//      (exact) into a 128 x 512 tile in the 128-byte-swizzled layout, then
+//      issues the 16-byte gathers of the next tile into the same registers,
+//      so their latency hides behind this tile's MMAs and softmax;
 //   2. S^T = Khat Q^T: one thread issues 32 tcgen05.mma (M=128 tokens, N=64
 //      heads, K=16 each) into TMEM;
-//   3. softmax over the tile's tokens per head, exact (the whole split is in
-//      the tile), P^T written as a 64 x 128 K-major f16 operand;
-//   4. O^T = V^T P^T: V^T is the same latent tile read as an MN-major operand
-//      (dims contiguous), 4 x 8 tcgen05.mma (M=128 dims, N=64 heads, K=16);
-//   5. the split's unnormalised O rows and its (max, sum) go to the workspace
-//      (staged through shared memory, 16-byte coalesced stores, L2-resident).
-// A merge kernel, chained by programmatic dependent launch, combines the n
-// splits of every (row, head) in fixed split order and discards the L2 lines
-// it consumed, so the partials never reach HBM.
+//   3. softmax: each thread holds one token's logits for 32 heads; per-head
+//      tile maxima come from a butterfly transpose-reduction across the warp
+//      and a 4-way exchange in shared memory.  The running maximum of a head
+//      only moves when a tile exceeds it by more than 2^8 (then the head's
+//      accumulated O columns and sum are rescaled in place); otherwise the
+//      stale maximum is kept, so the weights stay below 2^8 and exact math
+//      is unchanged.  P^T is written as a 128 x 64 MN-major f16 operand;
+//   4. O^T += V^T P^T: V^T is the same latent tile read as an MN-major
+//      operand (dims contiguous), 4 x 8 tcgen05.mma (M=128 dims, N=64 heads,
+//      K=16) accumulating in TMEM across the split's tiles;
+//   5. with one split the CTA normalises and writes the bf16 output (and
+//      lse) itself; otherwise the split's unnormalised O rows and its (max,
+//      sum) go to the workspace (staged through shared memory, 16-byte
+//      coalesced stores, L2-resident) and a merge kernel, chained by
+//      programmatic dependent launch, combines the n splits of every (row,
+//      head) in fixed split order and discards the L2 lines it consumed.
 #include <mutex>
 
 #include "dsa_device.cuh"
@@ -36,26 +48,31 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kHeads = 64;             // heads per CTA (MMA N)
-constexpr int kTok = 128;              // tokens per split (MMA M of S^T)
+constexpr int kTok = 128;              // entries per tile (MMA M of S^T)
+constexpr int kMaxTiles = 4;           // tiles per split
 constexpr int kMergeThreads = 128;     // merge kernel: one CTA per (row, head), 4 dims per thread
+constexpr float kRescaleLog2 = 8.0f;   // a head's running max moves only past this margin
 constexpr uint32_t kTileBytes = kTok * 512 * 2;        // latent tile, f16: 8 sub-tiles of 16 KB
 constexpr uint32_t kSubTok = kTok * 128;               // one 64-dim sub-tile of the latent tile
 constexpr uint32_t kQBytes = kHeads * 512 * 2;         // Q operand, f16: 8 sub-tiles of 8 KB
 constexpr uint32_t kSubQ = kHeads * 128;
-constexpr uint32_t kPBytes = kHeads * kTok * 2;        // P^T operand: 2 sub-tiles of 8 KB
-constexpr uint32_t kSubP = kHeads * 128;
+constexpr uint32_t kPBytes = kTok * kHeads * 2;        // P^T operand, MN-major: 128 rows of 128 B
 constexpr uint32_t kTmemCols = 512;                    // S^T: cols 0..63, O^T blocks: 64 + 64*mb
 constexpr uint64_t kWaitNs = 500ull * 1000ull * 1000ull;
 
-struct __align__(8) Ctl {
+struct __align__(16) Ctl {
   uint64_t bar_s, bar_o;
   uint32_t tmem_base;
-  int abort_flag;
-  int64_t slot[kTok];
-  float qexp[kHeads];  // per-head logit scale
+  int pad[3];
+  alignas(16) float qexp[kHeads];   // per-head logit scale
+  alignas(16) float red[4][kHeads]; // per lane quarter: head maxima, then sums
+  float lfin[kHeads];               // final per-head sums and maxima
+  float mfin[kHeads];
+  int32_t slot[kMaxTiles * kTok];   // -1: no latent row
 };
 constexpr uint32_t kCtlOff = kTileBytes + kQBytes + kPBytes;
 constexpr uint32_t kSmemBytes = kCtlOff + sizeof(Ctl) + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t out;
@@ -84,10 +101,11 @@ __device__ __forceinline__ uint64_t umma_desc_sw128_mnmajor(uint32_t saddr, uint
   d |= static_cast<uint64_t>(2) << 61;
   return d;
 }
-// kind::f16 instruction descriptor: f16 A and B, f32 D, A optionally MN-major.
-__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool a_mn_major) {
-  return (1u << 4) | (a_mn_major ? (1u << 15) : 0u) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
+// kind::f16 instruction descriptor: f16 A and B, f32 D; A and B each K-major
+// or MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (a_mn_major ? (1u << 15) : 0u) | (b_mn_major ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 // Drop a 128-byte L2 line without writing it back (its contents become
 // undefined); used on partials that have been consumed.
@@ -112,15 +130,112 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// The same columns written back from registers (the caller waits with
+// tmem_store_wait before the values are used by an MMA).
+__device__ __forceinline__ void tmem_store32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_store_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// One butterfly step of a warp transpose-reduction: on entry v[0..2S) are
+// values of 2S heads in this lane; on exit v[0..S) hold, for the S heads
+// selected by lane bit S, the reduction over this lane and lane ^ S.  After
+// the steps S = 16, 8, 4, 2, 1, v[0] of lane l is the reduction of head l over
+// the 32 lanes, in an order fixed by the lane numbering.
+template <int S, bool kMax>
+__device__ __forceinline__ void butterfly_step(float* v, int lane) {
+  const bool up = (lane & S) != 0;
+#pragma unroll
+  for (int j = 0; j < S; ++j) {
+    const float send = up ? v[j] : v[j + S];
+    const float keep = up ? v[j + S] : v[j];
+    const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, S);
+    v[j] = kMax ? fmaxf(keep, recv) : keep + recv;
+  }
+}
+template <bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
+  butterfly_step<16, kMax>(v, lane);
+  butterfly_step<8, kMax>(v, lane);
+  butterfly_step<4, kMax>(v, lane);
+  butterfly_step<2, kMax>(v, lane);
+  butterfly_step<1, kMax>(v, lane);
+  return v[0];
+}
+
+// Bounded wait of a whole warp on an mbarrier phase; a timeout is recorded
+// once and later waits of this warp are skipped.
+__device__ __forceinline__ void warp_wait(uint64_t* bar, uint32_t parity, bool& alive, int lane,
+                                          int* err, int r) {
+  int ok = 1;
+  if (alive) {
+    if (lane == 0) ok = mbar_wait(bar, parity, kWaitNs) ? 1 : 0;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  }
+  if (alive && !ok) {
+    if (lane == 0) record_error(err, DSA_DEVERR_TIMEOUT, r);
+    alive = false;
+  }
+}
+
+// 16-byte gathers of one tile: warp w loads the latent rows of tokens
+// w, w+8, ..., w+120 of the tile, lane l their bytes 16l..16l+15.
+__device__ __forceinline__ void gather_tile(uint4 (&raw)[16], const int32_t* slot,
+                                            const uint8_t* pool, int e0, int nj, int warp,
+                                            int lane) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int e = e0 + warp + 8 * j;
+    const int s = e < nj ? slot[e] : -1;
+    raw[j] = s >= 0 ? __ldg(reinterpret_cast<const uint4*>(pool + static_cast<int64_t>(s) * 512) + lane)
+                    : make_uint4(0, 0, 0, 0);
+  }
+}
+// The same rows widened to f16 into the latent tile (token = row, dims
+// 16l..16l+15 = two 16-byte chunks of sub-tile l/4).
+__device__ __forceinline__ void store_tile(uint8_t* tile, const uint4 (&raw)[16], int warp,
+                                           int lane) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int tok = warp + 8 * j;
+    const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+    uint32_t cv[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      cv[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
+      cv[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16));
+    }
+    uint8_t* sub = tile + (lane >> 2) * kSubTok;
+    const int c16 = (lane & 3) * 2;
+    *reinterpret_cast<uint4*>(sub + sw128(tok, c16)) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
+    *reinterpret_cast<uint4*>(sub + sw128(tok, c16 + 1)) = make_uint4(cv[4], cv[5], cv[6], cv[7]);
+  }
+}
 
 __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* tile = smem;                 // Khat, f16, [128 tok] x [512 dims], 8 sub-tiles
   uint8_t* qop = smem + kTileBytes;     // Q, f16, [64 heads] x [512 dims], 8 sub-tiles
-  uint8_t* pop = qop + kQBytes;         // P^T, f16, [64 heads] x [128 tok], 2 sub-tiles
+  uint8_t* pop = qop + kQBytes;         // P^T, f16, [128 tok] x [64 heads], MN-major
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
-  float* sm_s = reinterpret_cast<float*>(qop);     // logits [64 heads][128 tok] after S^T
 
   const int hg = blockIdx.y, r = blockIdx.z;
   const int split = blockIdx.x;
@@ -128,9 +243,15 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j0 = split * p.split_len;
   const int nj = max(0, min(p.split_len, p.topk - j0));
+  const int ntiles = (nj + kTok - 1) / kTok;
   const bool report = hg == 0;
   const int head0 = hg * kHeads;
   const int nheads = min(kHeads, p.heads - head0);
+  // Softmax role: lane quarter (tokens 32*quarter + lane of a tile) and the
+  // 32 heads hh .. hh+31 this thread holds.
+  const int quarter = warp & 3;
+  const int hh = (warp >> 2) * 32;
+  const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
 
   grid_dep_launch();
   int len = p.rows.seq_lens[r];
@@ -139,12 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     len = 0;
   }
 
-  // ---- set-up: barriers, TMEM, slots of this split's entries
+  // ---- set-up: barriers, TMEM
   if (tid == 0) {
     mbar_init(&ctl->bar_s, 1);
     mbar_init(&ctl->bar_o, 1);
     fence_mbar_init();
-    ctl->abort_flag = 0;
   }
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -152,50 +272,59 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
   }
   // ---- Q operand: 4 threads per head, 128 elements each; power-of-two scale
   // per head so every bf16 value is exact in f16.  Heads past the row's count
-  // are zero.
-  // (Q loads are issued first: they do not depend on the slot lookups.)
+  // are zero.  (Q loads are issued first: they do not depend on the kernel
+  // before.)
   const int qh = tid >> 2, qq = tid & 3;
   uint4 qraw[16];
   {
-    const int h = qh, q = qq;
-    const bool real = h < nheads;
+    const bool real = qh < nheads;
     const uint4* src = reinterpret_cast<const uint4*>(
-        p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + q * 128);
+        p.q + (static_cast<int64_t>(r) * p.heads + head0 + qh) * 512 + qq * 128);
 #pragma unroll
     for (int j = 0; j < 16; ++j) qraw[j] = real ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
   }
   grid_dep_wait();  // the selection comes from the kernel before
-  if (tid < kTok) {
-    int64_t slot = -1;
-    if (tid < nj) {
-      const int idx = __ldg(p.sel + static_cast<int64_t>(r) * p.topk + j0 + tid);
-      if (idx != -1) {
-        if (idx < 0 || idx >= len) {
+
+  // ---- slots of every entry of this split (two dependent loads each)
+  {
+    constexpr int kPer = kMaxTiles * kTok / kThreads;
+    int idx[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
+      idx[i] = e < nj ? p.sel[static_cast<int64_t>(r) * p.topk + j0 + e] : -1;  // (after the wait)
+    }
+    const int32_t* bt = p.rows.block_table + static_cast<int64_t>(r) * p.rows.bt_stride;
+    const int bs = p.rows.block_size;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
+      if (e >= kMaxTiles * kTok) break;
+      int32_t slot = -1;
+      const int t = idx[i];
+      if (t != -1) {
+        if (t < 0 || t >= len) {
           if (report) record_error(p.err, DSA_DEVERR_SELECT, r);
         } else {
-          const int32_t* bt = p.rows.block_table + static_cast<int64_t>(r) * p.rows.bt_stride;
-          const int bs = p.rows.block_size;
-          const int blk = idx / bs;
+          const int blk = t / bs;
           const int phys = blk < p.rows.max_blocks_per_seq ? __ldg(bt + blk) : -1;
-          const int64_t s = static_cast<int64_t>(phys) * bs + idx % bs;
+          const int64_t s = static_cast<int64_t>(phys) * bs + t % bs;
           if (phys < 0 || s >= p.nslots) {
             if (report) record_error(p.err, DSA_DEVERR_BLOCK, r);
           } else {
-            slot = s;
+            slot = static_cast<int32_t>(s);
           }
         }
       }
+      ctl->slot[e] = slot;
     }
-    ctl->slot[tid] = slot;
   }
 
   {
-    const int h = qh, q = qq;
-    const uint4* raw = qraw;
     float amax = 0.0f;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+      const uint32_t w[4] = {qraw[j].x, qraw[j].y, qraw[j].z, qraw[j].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
@@ -209,190 +338,204 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     const int sh = max(-100, min(100, 14 - e));
     const float scale = ldexpf(1.0f, sh);
     // Logit scale of this head: sm_scale * kv_scale * log2(e) / 2^sh.
-    if (q == 0)
-      ctl->qexp[h] = p.sm_scale * p.kv_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
+    if (qq == 0)
+      ctl->qexp[qh] = p.sm_scale * p.kv_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {  // 8 elements = one 16-byte chunk of the operand
-      const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+      const uint32_t w[4] = {qraw[j].x, qraw[j].y, qraw[j].z, qraw[j].w};
       uint32_t o4[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         o4[i] = pack_f16x2(__uint_as_float(w[i] << 16) * scale,
                            __uint_as_float(w[i] & 0xFFFF0000u) * scale);
-      const int d0 = q * 128 + j * 8;  // first of the 8 dims
-      *reinterpret_cast<uint4*>(qop + (d0 >> 6) * kSubQ + sw128(h, (d0 & 63) >> 3)) =
+      const int d0 = qq * 128 + j * 8;  // first of the 8 dims
+      *reinterpret_cast<uint4*>(qop + (d0 >> 6) * kSubQ + sw128(qh, (d0 & 63) >> 3)) =
           make_uint4(o4[0], o4[1], o4[2], o4[3]);
     }
   }
-  __syncthreads();  // slots visible
-
-  // ---- latent tile: 128 tokens x 32 chunks of 16 B, 16 chunks per thread
-  {
-    uint4 raw[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int c = tid + j * kThreads;
-      const int tok = c >> 5, k = c & 31;
-      const int64_t slot = ctl->slot[tok];
-      raw[j] = slot >= 0 ? __ldg(reinterpret_cast<const uint4*>(p.pool + slot * 512) + k)
-                         : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int c = tid + j * kThreads;
-      const int tok = c >> 5, k = c & 31;  // dims 16k .. 16k+15
-      const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-      uint32_t cv[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        cv[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
-        cv[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16));
-      }
-      uint8_t* sub = tile + (k >> 2) * kSubTok;
-      const int c16 = (k & 3) * 2;
-      *reinterpret_cast<uint4*>(sub + sw128(tok, c16)) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
-      *reinterpret_cast<uint4*>(sub + sw128(tok, c16 + 1)) = make_uint4(cv[4], cv[5], cv[6], cv[7]);
-    }
-  }
-  fence_proxy_async_smem();  // generic-proxy operand writes -> visible to the tensor core
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  __syncthreads();  // slots, qexp visible
   const uint32_t tmem = ctl->tmem_base;
 
-  // ---- S^T = Khat Q^T (M = 128 tokens, N = 64 heads, K = 512)
-  if (tid == 0) {
-    const uint32_t idesc = idesc_f16(kTok, kHeads, false);
-    const uint32_t a0 = smem_u32(tile), b0 = smem_u32(qop);
-#pragma unroll
-    for (int kk = 0; kk < 32; ++kk) {
-      const uint32_t a = a0 + (kk >> 2) * kSubTok + (kk & 3) * 32;
-      const uint32_t b = b0 + (kk >> 2) * kSubQ + (kk & 3) * 32;
-      umma_bf16(tmem, umma_desc_sw128_kmajor(a), umma_desc_sw128_kmajor(b), idesc, kk != 0);
-    }
-    umma_commit(&ctl->bar_s);
-  }
+  uint4 raw[16];
+  gather_tile(raw, ctl->slot, p.pool, 0, nj, warp, lane);
 
-  // ---- softmax over the tile's tokens, per head
-  {
-    // Warps w and w+4 read TMEM lane quarter w%4 (tokens 32*(w%4) + lane),
-    // heads 32*(w/4) .. +31, scale them and store the logits transposed.
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(&ctl->bar_s, 0, kWaitNs) ? 1 : 0;
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok && lane == 0) {
-      record_error(p.err, DSA_DEVERR_TIMEOUT, r);
-      ctl->abort_flag = 1;
-    }
+  bool alive = true;
+  float m_run = -INFINITY;  // running max of head hh + lane (log2 units)
+  float l_part = 0.0f;      // its sum over this lane quarter's tokens
+  for (int it = 0; it < ntiles; ++it) {
+    // ---- the tile buffer and P^T are free once the previous O^T MMAs are done
+    if (it > 0) warp_wait(&ctl->bar_o, (it - 1) & 1, alive, lane, p.err, r);
+    store_tile(tile, raw, warp, lane);
+    if (it + 1 < ntiles) gather_tile(raw, ctl->slot, p.pool, (it + 1) * kTok, nj, warp, lane);
+    fence_proxy_async_smem();  // generic-proxy operand writes -> visible to the tensor core
+    tc_fence_before();
+    __syncthreads();
     tc_fence_after();
-    const int tok = (warp & 3) * 32 + lane;
-    const int hh = (warp >> 2) * 32;
-    float v[32];
-    tmem_load32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + hh, v);
-    const bool valid = tok < nj && ctl->slot[tok] >= 0;
-    __syncthreads();  // every thread has read Q's region as an MMA operand (bar_s) -> reuse it
+
+    // ---- S^T = Khat Q^T (M = 128 tokens, N = 64 heads, K = 512)
+    if (tid == 0) {
+      const uint32_t idesc = idesc_f16(kTok, kHeads, false, false);
+      const uint32_t a0 = smem_u32(tile), b0 = smem_u32(qop);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int h = hh + i;
-      sm_s[h * kTok + tok] = valid ? v[i] * ctl->qexp[h] : -INFINITY;
+      for (int kk = 0; kk < 32; ++kk) {
+        const uint32_t a = a0 + (kk >> 2) * kSubTok + (kk & 3) * 32;
+        const uint32_t b = b0 + (kk >> 2) * kSubQ + (kk & 3) * 32;
+        umma_bf16(tmem, umma_desc_sw128_kmajor(a), umma_desc_sw128_kmajor(b), idesc, kk != 0);
+      }
+      umma_commit(&ctl->bar_s);
     }
-  }
-  __syncthreads();
-  {
-    // 4 threads per head, 32 tokens each.
-    const int h = tid >> 2, q = tid & 3;
+
+    // ---- softmax of this tile
+    warp_wait(&ctl->bar_s, it & 1, alive, lane, p.err, r);
+    tc_fence_after();
+    const int tok = quarter * 32 + lane;
+    const int e = it * kTok + tok;
+    const bool valid = e < nj && ctl->slot[e] >= 0;
     float z[32];
+    tmem_load32(tmem + lane_base + hh, z);
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
-      const float4 t4 = *reinterpret_cast<const float4*>(sm_s + h * kTok + q * 32 + i);
-      z[i] = t4.x;
-      z[i + 1] = t4.y;
-      z[i + 2] = t4.z;
-      z[i + 3] = t4.w;
+      const float4 qe = *reinterpret_cast<const float4*>(&ctl->qexp[hh + i]);
+      z[i] = valid ? z[i] * qe.x : -INFINITY;
+      z[i + 1] = valid ? z[i + 1] * qe.y : -INFINITY;
+      z[i + 2] = valid ? z[i + 2] * qe.z : -INFINITY;
+      z[i + 3] = valid ? z[i + 3] * qe.w : -INFINITY;
     }
-    float mx = -INFINITY;
+    {
+      float w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, z[i]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-    float sum = 0.0f;
+      for (int i = 0; i < 32; ++i) w[i] = z[i];
+      ctl->red[quarter][hh + lane] = warp_transpose_reduce<true>(w, lane);
+    }
+    __syncthreads();
+    const float tm = fmaxf(fmaxf(ctl->red[0][hh + lane], ctl->red[1][hh + lane]),
+                           fmaxf(ctl->red[2][hh + lane], ctl->red[3][hh + lane]));
+    float alpha = 1.0f;
+    if (tm > m_run + kRescaleLog2) {  // also the first finite maximum (m_run = -inf)
+      alpha = exp2f(m_run - tm);      // 0 while nothing was accumulated
+      m_run = tm;
+      l_part *= alpha;
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      z[i] = mx != -INFINITY ? exp2f(z[i] - mx) : 0.0f;
-      sum += z[i];
+      const float m = __shfl_sync(0xFFFFFFFFu, m_run, i);
+      z[i] = z[i] == -INFINITY ? 0.0f : exp2f(z[i] - m);
     }
-    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-    if (q == 0)
-      reinterpret_cast<float2*>(p.part_ml)[((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) *
-                                               kHeads + h] = make_float2(mx, sum);
-    // P^T row h: tokens q*32 .. q*32+31 = 4 chunks of 8 in sub-tile (q*32)/64.
+    {
+      // P^T row `tok`: heads hh .. hh+31 = 16-byte chunks hh/8 .. hh/8+3.
+      uint8_t* row = pop + tok * 128;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int t0 = q * 32 + c * 8;
-      uint8_t* sub = pop + (t0 >> 6) * kSubP;
-      *reinterpret_cast<uint4*>(sub + sw128(h, (t0 & 63) >> 3)) =
-          make_uint4(pack_f16x2(z[c * 8], z[c * 8 + 1]), pack_f16x2(z[c * 8 + 2], z[c * 8 + 3]),
-                     pack_f16x2(z[c * 8 + 4], z[c * 8 + 5]), pack_f16x2(z[c * 8 + 6], z[c * 8 + 7]));
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(row + (((hh >> 3) + c) ^ (tok & 7)) * 16) =
+            make_uint4(pack_f16x2(z[8 * c], z[8 * c + 1]), pack_f16x2(z[8 * c + 2], z[8 * c + 3]),
+                       pack_f16x2(z[8 * c + 4], z[8 * c + 5]), pack_f16x2(z[8 * c + 6], z[8 * c + 7]));
+    }
+    l_part += warp_transpose_reduce<false>(z, lane);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    const int rescale = __syncthreads_or(it > 0 && alpha != 1.0f);
+    tc_fence_after();
+    if (rescale) {
+      // O^T columns of the heads whose maximum moved, scaled in place.
+      float a[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a[i] = __shfl_sync(0xFFFFFFFFu, alpha, i);
+#pragma unroll 1
+      for (int mb = 0; mb < 4; ++mb) {
+        float v[32];
+        const uint32_t taddr = tmem + lane_base + 64 + mb * 64 + hh;
+        tmem_load32(taddr, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= a[i];
+        tmem_store32(taddr, v);
+      }
+      tmem_store_wait();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    }
+
+    // ---- O^T += V^T P^T (4 blocks of M = 128 dims, N = 64 heads, K = 128 tokens)
+    if (tid == 0) {
+      const uint32_t idesc = idesc_f16(128, kHeads, true, true);
+      const uint32_t a0 = smem_u32(tile), b0 = smem_u32(pop);
+#pragma unroll
+      for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+        for (int kk = 0; kk < kTok / 16; ++kk) {
+          // A: dims 128mb.. (two 64-dim sub-tiles, kSubTok apart), tokens 16kk..
+          // B: tokens 16kk.. of P^T (one 64-head chunk per 128-byte row).
+          const uint32_t a = a0 + (2 * mb) * kSubTok + kk * 2048;
+          const uint32_t b = b0 + kk * 2048;
+          umma_bf16(tmem + 64 + mb * 64, umma_desc_sw128_mnmajor(a, kSubTok),
+                    umma_desc_sw128_mnmajor(b, kPBytes), idesc, (it > 0 || kk != 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(&ctl->bar_o);
     }
   }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
+  if (ntiles > 0) warp_wait(&ctl->bar_o, (ntiles - 1) & 1, alive, lane, p.err, r);
   tc_fence_after();
 
-  // ---- O^T = V^T P^T (4 blocks of M = 128 dims, N = 64 heads, K = 128 tokens)
-  if (tid == 0) {
-    const uint32_t idesc = idesc_f16(128, kHeads, true);
-    const uint32_t a0 = smem_u32(tile), b0 = smem_u32(pop);
-#pragma unroll
-    for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-      for (int kk = 0; kk < kTok / 16; ++kk) {
-        // A: dims 128mb.. (two 64-dim sub-tiles, kSubTok apart), tokens 16kk..
-        const uint32_t a = a0 + (2 * mb) * kSubTok + kk * 2048;
-        const uint32_t b = b0 + (kk >> 2) * kSubP + (kk & 3) * 32;
-        umma_bf16(tmem + 64 + mb * 64, umma_desc_sw128_mnmajor(a, kSubTok),
-                  umma_desc_sw128_kmajor(b), idesc, kk != 0);
-      }
-    }
-    umma_commit(&ctl->bar_o);
+  // ---- per-head sums over the four lane quarters, in fixed order
+  ctl->red[quarter][hh + lane] = l_part;
+  __syncthreads();
+  if (quarter == 0) {
+    const int h = hh + lane;
+    const float l = ((ctl->red[0][h] + ctl->red[1][h]) + ctl->red[2][h]) + ctl->red[3][h];
+    ctl->lfin[h] = l;
+    ctl->mfin[h] = m_run;
+    if (nsplit > 1)
+      reinterpret_cast<float2*>(p.part_ml)[((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit +
+                                            split) * kHeads + h] = make_float2(m_run, l);
+    else if (p.lse != nullptr && h < nheads)
+      p.lse[static_cast<int64_t>(r) * p.heads + head0 + h] =
+          m_run != -INFINITY ? (m_run + log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
+
+  // ---- O^T from TMEM, staged as rows [64 heads][512 dims] in the tile region
   {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(&ctl->bar_o, 0, kWaitNs) ? 1 : 0;
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok && lane == 0) {
-      record_error(p.err, DSA_DEVERR_TIMEOUT, r);
-      ctl->abort_flag = 1;
-    }
-    tc_fence_after();
     // Warp w reads lane quarter w%4 (dims 32*(w%4) + lane of each block) of
-    // blocks mb = 2*(w/4), 2*(w/4)+1, all 64 heads, into the free tile region
-    // as rows [64 heads][512 dims] (consecutive lanes -> consecutive floats).
+    // blocks mb = 2*(w/4), 2*(w/4)+1, all 64 heads (consecutive lanes ->
+    // consecutive floats).
     float* stage = reinterpret_cast<float*>(tile);
-    const int dl = (warp & 3) * 32 + lane;
+    const int dl = quarter * 32 + lane;
 #pragma unroll
     for (int bb = 0; bb < 2; ++bb) {
       const int mb = (warp >> 2) * 2 + bb;
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         float v[32];
-        tmem_load32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 64 + mb * 64 + hc * 32,
-                    v);
-        if (bb == 0 && hc == 0) __syncthreads();  // every thread is past bar_o: the tile is free
+        tmem_load32(tmem + lane_base + 64 + mb * 64 + hc * 32, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) stage[(hc * 32 + i) * 512 + mb * 128 + dl] = v[i];
+        for (int i = 0; i < 32; ++i)  // (no tile ran: nothing was accumulated)
+          stage[(hc * 32 + i) * 512 + mb * 128 + dl] = ntiles > 0 ? v[i] : 0.0f;
       }
     }
     tc_fence_before();
     __syncthreads();
-    // This split's partial rows, 16-byte coalesced stores (512 B per thread).
-    float4* dst = reinterpret_cast<float4*>(
-        p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) * (kHeads * 512));
     const float4* src = reinterpret_cast<const float4*>(stage);
+    if (nsplit > 1) {
+      // This split's partial rows, 16-byte coalesced stores (512 B per thread).
+      float4* dst = reinterpret_cast<float4*>(
+          p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) * (kHeads * 512));
 #pragma unroll 8
-    for (int i = tid; i < kHeads * 128; i += kThreads) dst[i] = src[i];
+      for (int i = tid; i < kHeads * 128; i += kThreads) dst[i] = src[i];
+    } else {
+      // The only split: normalise, round to bf16, write the output rows.
+#pragma unroll 4
+      for (int i = tid; i < nheads * 128; i += kThreads) {
+        const int h = i >> 7;
+        const float l = ctl->lfin[h];
+        const float scale = ctl->mfin[h] != -INFINITY ? p.kv_scale / l : 0.0f;
+        const float4 v = src[i];
+        uint2 packed;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.x) : "f"(v.y * scale), "f"(v.x * scale));
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.y) : "f"(v.w * scale), "f"(v.z * scale));
+        reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512)[i & 127] =
+            packed;
+      }
+    }
   }
   if (warp == 1) {
     tc_fence_after();
@@ -412,7 +555,7 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
   grid_dep_wait();  // the partials come from the kernel before
   grid_dep_launch();
   float mmax = -INFINITY;
-  for (int c = 0; c < nsplit; ++c) mmax = fmaxf(mmax, __ldcg(ml + (base + c) * kHeads + hl).x);
+  for (int c = 0; c < nsplit; ++c) mmax = fmaxf(mmax, ld_dep_f2(ml + (base + c) * kHeads + hl).x);
   float lsum = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (mmax != -INFINITY) {
@@ -422,8 +565,8 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
       float4 vc[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        mlc[u] = __ldcg(ml + (base + c + u) * kHeads + hl);
-        vc[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((base + c + u) * kHeads + hl) * 512) + tid);
+        mlc[u] = ld_dep_f2(ml + (base + c + u) * kHeads + hl);
+        vc[u] = ld_dep_f4(reinterpret_cast<const float4*>(p.part_o + ((base + c + u) * kHeads + hl) * 512) + tid);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -436,8 +579,8 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
       }
     }
     for (; c < nsplit; ++c) {
-      const float2 mlc = __ldcg(ml + (base + c) * kHeads + hl);
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((base + c) * kHeads + hl) * 512) + tid);
+      const float2 mlc = ld_dep_f2(ml + (base + c) * kHeads + hl);
+      const float4 v = ld_dep_f4(reinterpret_cast<const float4*>(p.part_o + ((base + c) * kHeads + hl) * 512) + tid);
       const float f = exp2f(mlc.x - mmax);
       lsum += mlc.y * f;
       acc.x += v.x * f;
@@ -465,15 +608,23 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
 }  // namespace
 
 void plan_mla_decode_tc(DecodeParams& p) {
-  int n = (p.topk + kTok - 1) / kTok;
+  const int target = (p.heads > kHeads ? 4 : 2) * kTok;
+  int n = (p.topk + target - 1) / target;
   if (n < 1) n = 1;
   p.splits = n;
   p.split_len = (p.topk + n - 1) / n;
 }
 
+static int decode_splits(int32_t heads, int32_t topk) {
+  DecodeParams p = {};
+  p.heads = heads;
+  p.topk = topk;
+  plan_mla_decode_tc(p);
+  return p.splits;
+}
+
 size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
-  int n = (topk + kTok - 1) / kTok;
-  if (n < 1) n = 1;
+  const int n = decode_splits(heads, topk);
   const size_t units = static_cast<size_t>(rows) * ((heads + kHeads - 1) / kHeads) * n * kHeads;
   const size_t o_bytes = (units * 512 * sizeof(float) + 255) & ~static_cast<size_t>(255);
   return o_bytes + units * 2 * sizeof(float);
@@ -488,6 +639,7 @@ void mla_decode_tc_bind_workspace(DecodeParams& p, void* workspace) {
 }
 
 cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream) {
+  if (p.split_len > kMaxTiles * kTok) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
@@ -501,7 +653,7 @@ cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, p);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || p.splits == 1) return e;
   cudaLaunchConfig_t mcfg = {};
   mcfg.gridDim = dim3(p.heads, p.rows.rows, 1);
   mcfg.blockDim = dim3(kMergeThreads, 1, 1);

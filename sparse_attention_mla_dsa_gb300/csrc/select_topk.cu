@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int i = base + j * kThreads + tid;
-      v[j] = i < n ? __ldg(row + i) : 0.0f;
+      v[j] = i < n ? row[i] : 0.0f;  // plain load: stays after the wait
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {

@@ -87,3 +87,31 @@ def test_fullsize_verify_rows_bit_identical_to_serial(dsa):
         assert torch.equal(batch.out[r], one.out[0])
         del one
     assert api.dsa_get_error(reset=True)[0] == 0
+
+
+@pytest.mark.parametrize("name", ["batched", "verify"])
+def test_chain_never_reads_a_stale_intermediate(dsa, name):
+    """Each kernel of the chain starts before the one ahead of it finishes and
+    waits before it reads that kernel's output.  Poison every intermediate
+    (scores, selection, split partials, output) before each step: a read
+    issued ahead of the wait would show up as a device error or as a result
+    that differs from a clean step."""
+    api, path = dsa
+    wl = workloads.named(name)
+    dw = path.DeviceWorkload(wl)
+    dw.step()
+    torch.cuda.synchronize()
+    assert api.dsa_get_error(reset=True)[0] == 0
+    ref_sel, ref_out, ref_lse = dw.sel.clone(), dw.out.clone(), dw.lse.clone()
+    for _ in range(5):
+        dw.scores.fill_(float("-inf"))
+        dw.sel.fill_(0x40000000)                   # outside every row's range
+        dw.workspace.fill_(0xFF)                   # NaN partials
+        dw.out.fill_(0x7FC0)
+        dw.step()
+        torch.cuda.synchronize()
+        code, row, count = api.dsa_get_error(reset=True)
+        assert code == 0, f"device error {api.DEVERR.get(code)} row {row} count {count}"
+        assert torch.equal(dw.sel, ref_sel)
+        assert torch.equal(dw.out, ref_out)
+        assert torch.equal(dw.lse.view(torch.int32), ref_lse.view(torch.int32))
