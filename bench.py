@@ -289,7 +289,8 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(end)
-    ev_sets = [evs for _, evs in staged] if staged else eager_evs
+    # only the replicas the K steps replayed hold recorded events
+    ev_sets = [evs for _, evs in staged[:min(K, n_rep)]] if staged else eager_evs
     stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev_sets)
                 for j, s in enumerate(stages)}
     elapsed_ms = shard.max_over_ranks(elapsed_ms)
