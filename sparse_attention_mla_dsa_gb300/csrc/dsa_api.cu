@@ -230,7 +230,22 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
     return DSA_ERR_WORKSPACE;
   mla_decode_tc_bind_workspace(p, workspace);
-  return launched(launch_mla_decode_tc(p, static_cast<cudaStream_t>(stream)));
+  auto encode = encode_tiled();
+  if (encode == nullptr) return DSA_ERR_CUDA;
+  // Latent pool [nslots][512] bytes; the gather reads 128-byte x 1-row boxes
+  // (tile::gather4: four rows per copy) with the 128-byte swizzle; rows
+  // outside the pool read as zero.
+  CUtensorMap pmap;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(DSA_LATENT_DIM), static_cast<cuuint64_t>(nslots)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(DSA_LATENT_DIM)};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult cr = encode(&pmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(pool), gdim,
+                       gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return DSA_ERR_INVALID_ARG;
+  return launched(launch_mla_decode_tc(p, pmap, static_cast<cudaStream_t>(stream)));
 }
 
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {

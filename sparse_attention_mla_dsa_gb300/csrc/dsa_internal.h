@@ -103,7 +103,9 @@ struct DecodeParams {
 void plan_mla_decode_tc(DecodeParams& p);
 size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 void mla_decode_tc_bind_workspace(DecodeParams& p, void* workspace);
-// Split kernel (tcgen05) followed by the merge kernel.
-cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream);
+// Split kernel (tcgen05) followed by the merge kernel.  `pmap` describes the
+// latent pool [nslots][512] bytes for 128-byte x 1-row TMA gathers.
+cudaError_t launch_mla_decode_tc(const DecodeParams& p, const CUtensorMap& pmap,
+                                 cudaStream_t stream);
 
 }  // namespace dsa

@@ -1,5 +1,6 @@
 // mla_decode_tc.cu -- S3 on the 5th-generation tensor cores: absorbed NoPE
-// MLA gather-attend with tcgen05 MMAs, accumulators in TMEM.
+// MLA gather-attend with FP8 (kind::f8f6f4) tcgen05 MMAs, TMA row gathers and
+// accumulators in TMEM.
 //
 // "glm5next_dsa/layer.rs": module header trap 4 (Q arrives absorbed into the
 // 512-wide latent space), attend_rows (one launch for all rows, each with its
@@ -8,36 +9,40 @@
 // head:  z_j = sm_scale * kv_scale * (Q . e4m3(latent_j)),  p = softmax(z),
 //        out = kv_scale * sum_j p_j e4m3(latent_j),  lse = log sum_j exp(z_j).
 //
-// A row's selection is cut into n splits of at most 256 entries (512 when the
-// row has more than 64 heads); n and the split length depend on topk and the
-// head count only, never on the number of rows, so a row's arithmetic is the
-// same in any launch.  Each CTA (8 warps) runs one split of one (row, 64-head
-// group) as a loop over 128-entry tiles, with an online softmax:
-//   0. resolves the slots of all its entries once, loads Q (64 heads, each
-//      scaled by a power of two so its bf16 values are exact in f16) as a
-//      64 x 512 K-major operand that stays resident;
-//   1. widens the tile's FP8 latent rows (already in registers) to f16
-//      (exact) into a 128 x 512 tile in the 128-byte-swizzled layout, then
-//      issues the 16-byte gathers of the next tile into the same registers,
-//      so their latency hides behind this tile's MMAs and softmax;
-//   2. S^T = Khat Q^T: one thread issues 32 tcgen05.mma (M=128 tokens, N=64
-//      heads, K=16 each) into TMEM;
-//   3. softmax: each thread holds one token's logits for 32 heads; per-head
-//      tile maxima come from a butterfly transpose-reduction across the warp
-//      and a 4-way exchange in shared memory.  The running maximum of a head
-//      only moves when a tile exceeds it by more than 2^8 (then the head's
-//      accumulated O columns and sum are rescaled in place); otherwise the
-//      stale maximum is kept, so the weights stay below 2^8 and exact math
-//      is unchanged.  P^T is written as a 128 x 64 MN-major f16 operand;
-//   4. O^T += V^T P^T: V^T is the same latent tile read as an MN-major
-//      operand (dims contiguous), 4 x 8 tcgen05.mma (M=128 dims, N=64 heads,
-//      K=16) accumulating in TMEM across the split's tiles;
-//   5. with one split the CTA normalises and writes the bf16 output (and
-//      lse) itself; otherwise the split's unnormalised O rows and its (max,
-//      sum) go to the workspace (staged through shared memory, 16-byte
-//      coalesced stores, L2-resident) and a merge kernel, chained by
-//      programmatic dependent launch, combines the n splits of every (row,
-//      head) in fixed split order and discards the L2 lines it consumed.
+// A row's selection is cut into n splits of at most 512 entries; n depends on
+// topk only, never on the number of rows, so a row's arithmetic is the same in
+// any launch.  One CTA (12 warps) runs one split of one (row, 64-head group)
+// as a pipeline over 128-entry tiles:
+//   - the latent stays FP8: TMA tile::gather4 copies the selected 512-byte
+//     rows (4 rows x one 128-byte column block per copy, rows that are not
+//     there zero-filled) straight into a 128-byte-swizzled tile, two tiles in
+//     flight.  A warp issues these copies one after another, ~100 cycles
+//     each, so three producer warps share the 128 copies of a tile (measured
+//     with one tile in flight: one issuing warp reaches ~10 GB/s per SM, two
+//     ~18, four ~30, where latency rather than issue is the limit);
+//   - Q is held as two E4M3 terms per element, hi = e4m3(q*2^s) and
+//     lo = e4m3(q*2^s - hi), which represent a bf16 q exactly (bf16 has 8
+//     significant bits, each term 4, and the residual is a multiple of q's
+//     last bit); the two terms are the N = 128 rows of one operand, so
+//     S^T = Khat [Qhi|Qlo]^T is one M = 128 (tokens) x N = 128 x K = 512 MMA
+//     chain whose two column halves add up to the exact logits (warp 3);
+//   - S is double-buffered in TMEM, so the MMAs of tile t+1 run while eight
+//     softmax warps (one token x 32 heads per thread) work on tile t;
+//   - softmax: the running maximum m of a head only moves when a logit would
+//     push p = 2^(z-m) past 2^8.75 (below the E4M3 maximum 448); it is then
+//     set 8 below the new tile maximum (the O columns and sums of that head
+//     are rescaled in TMEM).  p enters the O MMAs as two E4M3 terms (about
+//     the precision of a bf16 p: relative error <= 2^-8, and values below
+//     2^-10, i.e. 18 octaves under the head's maximum, drop out); the row
+//     sums add the unrounded p;
+//   - O^T += V^T P^T: V^T is the same FP8 tile read as an MN-major operand,
+//     P^T the two 64-byte halves (hi, lo) of each 128-byte token row, two
+//     accumulating MMA chains into the same TMEM columns.
+// With one split the CTA normalises and writes the bf16 output (and lse)
+// itself; otherwise the split's unnormalised O rows and its (max, sum) go to
+// the workspace (L2-resident) and a merge kernel, chained by programmatic
+// dependent launch, combines the n splits of every (row, head) in fixed split
+// order and discards the L2 lines it consumed.
 #include <mutex>
 
 #include "dsa_device.cuh"
@@ -46,52 +51,57 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kHeads = 64;             // heads per CTA (MMA N)
+constexpr int kThreads = 384;          // warps 0-2 gather, warp 3 MMA, warps 4-11 softmax
+constexpr int kProducerWarps = 3;      // (12 warps keep 168 registers per thread)
+constexpr int kMmaWarp = 3;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kHeads = 64;             // heads per CTA
 constexpr int kTok = 128;              // entries per tile (MMA M of S^T)
-constexpr int kMaxTiles = 4;           // tiles per split
+constexpr int kTilesPerSplit = 4;      // split length target (tiles)
+constexpr int kMaxTiles = 4;           // tiles per split the CTA can hold slots for
 constexpr int kMergeThreads = 128;     // merge kernel: one CTA per (row, head), 4 dims per thread
-constexpr float kRescaleLog2 = 8.0f;   // a head's running max moves only past this margin
-constexpr uint32_t kTileBytes = kTok * 512 * 2;        // latent tile, f16: 8 sub-tiles of 16 KB
-constexpr uint32_t kSubTok = kTok * 128;               // one 64-dim sub-tile of the latent tile
-constexpr uint32_t kQBytes = kHeads * 512 * 2;         // Q operand, f16: 8 sub-tiles of 8 KB
-constexpr uint32_t kSubQ = kHeads * 128;
-constexpr uint32_t kPBytes = kTok * kHeads * 2;        // P^T operand, MN-major: 128 rows of 128 B
-constexpr uint32_t kTmemCols = 512;                    // S^T: cols 0..63, O^T blocks: 64 + 64*mb
+constexpr float kPMaxLog2 = 8.75f;     // p = 2^(z - m) stays below 2^8.75 < 448
+constexpr float kPResetLog2 = 8.0f;    // a reset maps the tile maximum to p = 2^8
+constexpr uint32_t kSub = kTok * 128;              // one 128-dim column block: 128 rows x 128 B
+constexpr uint32_t kTileBytes = 4 * kSub;          // FP8 latent tile: 64 KB
+constexpr uint32_t kQBytes = 4 * kSub;             // Q operand: 128 rows (hi | lo) x 512 B
+constexpr uint32_t kPBytes = kTok * 128;           // P^T: 128 token rows x (64 hi + 64 lo) B
+constexpr uint32_t kTmemCols = 512;                // S buffers: cols 0..255, O^T: 256 + 64*mb
+constexpr uint32_t kOCol = 256;
 constexpr uint64_t kWaitNs = 500ull * 1000ull * 1000ull;
 
 struct __align__(16) Ctl {
-  uint64_t bar_s, bar_o;
+  uint64_t full[2], empty[2], sfull[2], sfree[2];
+  uint64_t pready, odone, drain;
   uint32_t tmem_base;
-  int pad[3];
-  alignas(16) float qexp[kHeads];   // per-head logit scale
-  alignas(16) float red[4][kHeads]; // per lane quarter: head maxima, then sums
-  float lfin[kHeads];               // final per-head sums and maxima
-  float mfin[kHeads];
-  int32_t slot[kMaxTiles * kTok];   // -1: no latent row
+  int abort_flag;
+  alignas(16) float qexp[kHeads];    // per-head logit scale (log2 units)
+  alignas(16) float red[4][kHeads];  // per lane quarter: head maxima, then sums
+  alignas(16) float mrun[kHeads];    // running maximum of each head (log2 units)
+  int32_t slot[kMaxTiles * kTok];    // -1: no latent row (zero-filled by the gather)
 };
-constexpr uint32_t kCtlOff = kTileBytes + kQBytes + kPBytes;
+constexpr uint32_t kCtlOff = 2 * kTileBytes + kQBytes + kPBytes;
 constexpr uint32_t kSmemBytes = kCtlOff + sizeof(Ctl) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  uint32_t out;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(hi), "f"(lo));
+// Two floats to two E4M3 codes (round to nearest even, saturating): `lo` in
+// the low byte.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t out;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(hi), "f"(lo));
   return out;
 }
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
-  uint32_t out;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(codes));
-  return out;
+// The two codes decoded back to float (exact: E4M3 values are f16 values).
+__device__ __forceinline__ float2 e4m3x2_decode(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+  return __half22float2(h);
 }
-// Byte offset of 16-byte chunk `c` (0..7) of row `row` inside a 128-byte
-// swizzled sub-tile (1024-byte aligned): chunks of 8 rows are XOR-permuted.
-__device__ __forceinline__ uint32_t sw128(int row, int c) {
-  return static_cast<uint32_t>(row) * 128u + static_cast<uint32_t>((c ^ (row & 7)) * 16);
-}
-// Descriptor of an MN-major operand in the 128-byte swizzled layout: 64
-// contiguous MN elements per 128-byte row, K rows 128 B apart; the next 64 MN
-// elements lie `lbo` bytes on, the next 8 K rows 1024 bytes on.
+// Descriptor of an MN-major operand in the 128-byte swizzled layout: 128
+// contiguous bytes of MN per K row, K rows 128 B apart, the next 8 K rows
+// 1024 bytes on, the next 128 bytes of MN `lbo` bytes on.
 __device__ __forceinline__ uint64_t umma_desc_sw128_mnmajor(uint32_t saddr, uint32_t lbo) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
@@ -101,11 +111,34 @@ __device__ __forceinline__ uint64_t umma_desc_sw128_mnmajor(uint32_t saddr, uint
   d |= static_cast<uint64_t>(2) << 61;
   return d;
 }
-// kind::f16 instruction descriptor: f16 A and B, f32 D; A and B each K-major
-// or MN-major.
-__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor, kind::f8f6f4 with E4M3 A and B (format code 0),
+// F32 accumulate; A and B each K-major or MN-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (a_mn_major ? (1u << 15) : 0u) | (b_mn_major ? (1u << 16) : 0u) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+// D[tmem] (+)= A[smem] * B[smem]^T on E4M3 operands, issued by one thread.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Four 128-byte rows (rows y0..y3, bytes x..x+127 of each) gathered by TMA
+// into 512 consecutive bytes of shared memory (swizzled by address); rows
+// outside the tensor are zero-filled.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                            int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "r"(smem_u32(bar))
+      : "memory");
 }
 // Drop a 128-byte L2 line without writing it back (its contents become
 // undefined); used on partials that have been consumed.
@@ -153,6 +186,23 @@ __device__ __forceinline__ void tmem_store32(uint32_t taddr, const float (&v)[32
 __device__ __forceinline__ void tmem_store_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// Named barrier of the 256 softmax threads (id 1); the second form returns
+// whether any of them passed a true predicate.
+__device__ __forceinline__ void softmax_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+}
+__device__ __forceinline__ bool softmax_sync_or(bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(pred ? 1u : 0u), "n"(kSoftmaxThreads)
+      : "memory");
+  return out != 0;
+}
 
 // One butterfly step of a warp transpose-reduction: on entry v[0..2S) are
 // values of 2S heads in this lane; on exit v[0..S) hold, for the S heads
@@ -180,61 +230,43 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
   return v[0];
 }
 
-// Bounded wait of a whole warp on an mbarrier phase; a timeout is recorded
-// once and later waits of this warp are skipped.
-__device__ __forceinline__ void warp_wait(uint64_t* bar, uint32_t parity, bool& alive, int lane,
+__device__ __forceinline__ void set_abort(Ctl* c) {
+  *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
+}
+__device__ __forceinline__ bool aborted(Ctl* c) {
+  return *reinterpret_cast<volatile int*>(&c->abort_flag) != 0;
+}
+// Bounded wait of a whole warp on an mbarrier phase (lane 0 polls).  A
+// timeout is recorded, the CTA is marked aborted and false is returned.
+__device__ __forceinline__ bool warp_wait(Ctl* c, uint64_t* bar, uint32_t parity, int lane,
                                           int* err, int r) {
   int ok = 1;
-  if (alive) {
-    if (lane == 0) ok = mbar_wait(bar, parity, kWaitNs) ? 1 : 0;
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-  }
-  if (alive && !ok) {
-    if (lane == 0) record_error(err, DSA_DEVERR_TIMEOUT, r);
-    alive = false;
-  }
-}
-
-// 16-byte gathers of one tile: warp w loads the latent rows of tokens
-// w, w+8, ..., w+120 of the tile, lane l their bytes 16l..16l+15.
-__device__ __forceinline__ void gather_tile(uint4 (&raw)[16], const int32_t* slot,
-                                            const uint8_t* pool, int e0, int nj, int warp,
-                                            int lane) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int e = e0 + warp + 8 * j;
-    const int s = e < nj ? slot[e] : -1;
-    raw[j] = s >= 0 ? __ldg(reinterpret_cast<const uint4*>(pool + static_cast<int64_t>(s) * 512) + lane)
-                    : make_uint4(0, 0, 0, 0);
-  }
-}
-// The same rows widened to f16 into the latent tile (token = row, dims
-// 16l..16l+15 = two 16-byte chunks of sub-tile l/4).
-__device__ __forceinline__ void store_tile(uint8_t* tile, const uint4 (&raw)[16], int warp,
-                                           int lane) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int tok = warp + 8 * j;
-    const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-    uint32_t cv[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      cv[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
-      cv[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16));
+  if (lane == 0) {
+    ok = aborted(c) ? 0 : (mbar_wait(bar, parity, kWaitNs) ? 1 : 0);
+    if (!ok && !aborted(c)) {
+      record_error(err, DSA_DEVERR_TIMEOUT, r);
+      set_abort(c);
     }
-    uint8_t* sub = tile + (lane >> 2) * kSubTok;
-    const int c16 = (lane & 3) * 2;
-    *reinterpret_cast<uint4*>(sub + sw128(tok, c16)) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
-    *reinterpret_cast<uint4*>(sub + sw128(tok, c16 + 1)) = make_uint4(cv[4], cv[5], cv[6], cv[7]);
   }
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+// Single-thread form (the MMA issuer).
+__device__ __forceinline__ bool thread_wait(Ctl* c, uint64_t* bar, uint32_t parity, int* err,
+                                            int r) {
+  if (aborted(c)) return false;
+  if (mbar_wait(bar, parity, kWaitNs)) return true;
+  record_error(err, DSA_DEVERR_TIMEOUT, r);
+  set_abort(c);
+  return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap pmap, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* tile = smem;                 // Khat, f16, [128 tok] x [512 dims], 8 sub-tiles
-  uint8_t* qop = smem + kTileBytes;     // Q, f16, [64 heads] x [512 dims], 8 sub-tiles
-  uint8_t* pop = qop + kQBytes;         // P^T, f16, [128 tok] x [64 heads], MN-major
+  uint8_t* tiles = smem;                       // 2 x FP8 latent tile [128 tok][512 B]
+  uint8_t* qop = smem + 2 * kTileBytes;        // [Qhi 64 rows | Qlo 64 rows] x 512 B
+  uint8_t* pop = qop + kQBytes;                // P^T: [128 tok][64 hi | 64 lo] B
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
 
   const int hg = blockIdx.y, r = blockIdx.z;
@@ -247,14 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
   const bool report = hg == 0;
   const int head0 = hg * kHeads;
   const int nheads = min(kHeads, p.heads - head0);
-  // Softmax role: lane quarter (tokens 32*quarter + lane of a tile) and the
-  // 32 heads hh .. hh+31 this thread holds.
-  const int quarter = warp & 3;
-  const int hh = (warp >> 2) * 32;
-  const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
 
   grid_dep_launch();
-  int len = p.rows.seq_lens[r];
+  int len = __ldg(p.rows.seq_lens + r);
   if (len < 0) {
     if (report && split == 0 && tid == 0) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
     len = 0;
@@ -262,37 +289,51 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
 
   // ---- set-up: barriers, TMEM
   if (tid == 0) {
-    mbar_init(&ctl->bar_s, 1);
-    mbar_init(&ctl->bar_o, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+      mbar_init(&ctl->sfull[s], 1);
+      mbar_init(&ctl->sfree[s], kSoftmaxThreads / 32);
+    }
+    mbar_init(&ctl->pready, kSoftmaxThreads / 32);
+    mbar_init(&ctl->odone, 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort_flag = 0;
     fence_mbar_init();
+    tma_prefetch_map(&pmap);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  // ---- Q operand: 4 threads per head, 128 elements each; power-of-two scale
-  // per head so every bf16 value is exact in f16.  Heads past the row's count
-  // are zero.  (Q loads are issued first: they do not depend on the kernel
-  // before.)
-  const int qh = tid >> 2, qq = tid & 3;
-  uint4 qraw[16];
-  {
-    const bool real = qh < nheads;
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.q + (static_cast<int64_t>(r) * p.heads + head0 + qh) * 512 + qq * 128);
+  if (tid < kHeads) ctl->mrun[tid] = -INFINITY;
+  // ---- Q: warp w converts heads w, w+10, ...; lane l dims 16l..16l+15.  The
+  // loads are issued first: they do not depend on the kernel before.
+  constexpr int kQPer = (kHeads + kThreads / 32 - 1) / (kThreads / 32);
+  uint4 qa[kQPer], qb[kQPer];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) qraw[j] = real ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+  for (int j = 0; j < kQPer; ++j) {
+    const int h = warp + j * (kThreads / 32);
+    if (h < nheads) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + lane * 16);
+      qa[j] = __ldg(src);
+      qb[j] = __ldg(src + 1);
+    } else {
+      qa[j] = make_uint4(0, 0, 0, 0);
+      qb[j] = make_uint4(0, 0, 0, 0);
+    }
   }
   grid_dep_wait();  // the selection comes from the kernel before
 
   // ---- slots of every entry of this split (two dependent loads each)
   {
-    constexpr int kPer = kMaxTiles * kTok / kThreads;
+    constexpr int kPer = (kMaxTiles * kTok + kThreads - 1) / kThreads;
     int idx[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int e = tid + i * kThreads;
-      idx[i] = e < nj ? p.sel[static_cast<int64_t>(r) * p.topk + j0 + e] : -1;  // (after the wait)
+      idx[i] = e < nj ? p.sel[static_cast<int64_t>(r) * p.topk + j0 + e] : -1;  // plain load
     }
     const int32_t* bt = p.rows.block_table + static_cast<int64_t>(r) * p.rows.bt_stride;
     const int bs = p.rows.block_size;
@@ -320,224 +361,327 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     }
   }
 
-  {
+  // ---- Q operand: q*2^s = hi + lo (E4M3 each), s a power of two per head
+  // putting the head's largest |q| in [128, 256).  Row h holds hi, row 64+h lo.
+#pragma unroll
+  for (int j = 0; j < kQPer; ++j) {
+    const int h = warp + j * (kThreads / 32);
+    if (h >= kHeads) break;
+    const uint32_t w[8] = {qa[j].x, qa[j].y, qa[j].z, qa[j].w, qb[j].x, qb[j].y, qb[j].z, qb[j].w};
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
     float amax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t w[4] = {qraw[j].x, qraw[j].y, qraw[j].z, qraw[j].w};
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
-        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
-      }
-    }
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     int e = 0;
     if (amax > 0.0f) frexpf(amax, &e);  // amax < 2^e
-    const int sh = max(-100, min(100, 14 - e));
+    const int sh = max(-100, min(100, 8 - e));
     const float scale = ldexpf(1.0f, sh);
-    // Logit scale of this head: sm_scale * kv_scale * log2(e) / 2^sh.
-    if (qq == 0)
-      ctl->qexp[qh] = p.sm_scale * p.kv_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
+    if (lane == 0)
+      ctl->qexp[h] = p.sm_scale * p.kv_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
+    uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {  // 8 elements = one 16-byte chunk of the operand
-      const uint32_t w[4] = {qraw[j].x, qraw[j].y, qraw[j].z, qraw[j].w};
-      uint32_t o4[4];
+    for (int i = 0; i < 4; ++i) {
+      uint16_t hc[2], lc[2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        o4[i] = pack_f16x2(__uint_as_float(w[i] << 16) * scale,
-                           __uint_as_float(w[i] & 0xFFFF0000u) * scale);
-      const int d0 = qq * 128 + j * 8;  // first of the 8 dims
-      *reinterpret_cast<uint4*>(qop + (d0 >> 6) * kSubQ + sw128(qh, (d0 & 63) >> 3)) =
-          make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      for (int k = 0; k < 2; ++k) {
+        const float a0 = x[4 * i + 2 * k] * scale, a1 = x[4 * i + 2 * k + 1] * scale;
+        hc[k] = e4m3x2(a0, a1);
+        const float2 hv = e4m3x2_decode(hc[k]);
+        lc[k] = e4m3x2(a0 - hv.x, a1 - hv.y);
+      }
+      hw[i] = static_cast<uint32_t>(hc[0]) | (static_cast<uint32_t>(hc[1]) << 16);
+      lw[i] = static_cast<uint32_t>(lc[0]) | (static_cast<uint32_t>(lc[1]) << 16);
     }
+    // Dims 16l..16l+15 = 16-byte chunk l%8 of column block l/8.
+    uint8_t* blk = qop + (lane >> 3) * kSub;
+    const uint32_t c = static_cast<uint32_t>(((lane & 7) ^ (h & 7)) * 16);
+    *reinterpret_cast<uint4*>(blk + h * 128 + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(blk + (h + kHeads) * 128 + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
-  __syncthreads();  // slots, qexp visible
+  fence_proxy_async_smem();  // generic-proxy operand writes -> visible to the tensor core
+  tc_fence_before();
+  __syncthreads();           // slots, qexp, Q operand, barriers, TMEM address
+  tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  uint4 raw[16];
-  gather_tile(raw, ctl->slot, p.pool, 0, nj, warp, lane);
-
-  bool alive = true;
-  float m_run = -INFINITY;  // running max of head hh + lane (log2 units)
-  float l_part = 0.0f;      // its sum over this lane quarter's tokens
-  for (int it = 0; it < ntiles; ++it) {
-    // ---- the tile buffer and P^T are free once the previous O^T MMAs are done
-    if (it > 0) warp_wait(&ctl->bar_o, (it - 1) & 1, alive, lane, p.err, r);
-    store_tile(tile, raw, warp, lane);
-    if (it + 1 < ntiles) gather_tile(raw, ctl->slot, p.pool, (it + 1) * kTok, nj, warp, lane);
-    fence_proxy_async_smem();  // generic-proxy operand writes -> visible to the tensor core
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- S^T = Khat Q^T (M = 128 tokens, N = 64 heads, K = 512)
-    if (tid == 0) {
-      const uint32_t idesc = idesc_f16(kTok, kHeads, false, false);
-      const uint32_t a0 = smem_u32(tile), b0 = smem_u32(qop);
-#pragma unroll
-      for (int kk = 0; kk < 32; ++kk) {
-        const uint32_t a = a0 + (kk >> 2) * kSubTok + (kk & 3) * 32;
-        const uint32_t b = b0 + (kk >> 2) * kSubQ + (kk & 3) * 32;
-        umma_bf16(tmem, umma_desc_sw128_kmajor(a), umma_desc_sw128_kmajor(b), idesc, kk != 0);
+  if (warp < kProducerWarps) {
+    // ================================================================ gather
+    // Copy g (0..127) of a tile moves rows 4(g/4) .. 4(g/4)+3 of the tile,
+    // column block g%4; lane l of producer warp w issues copies 32w + l and,
+    // below 128, 32w + l + 96.  Warp 0 lane 0 posts the tile's byte count;
+    // other copies may land before it does (the transaction count may run
+    // ahead of the expectation).
+    int issued = 0;
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t & 1;
+      if (t >= 2 && !warp_wait(ctl, &ctl->empty[s], ((t - 2) >> 1) & 1, lane, p.err, r)) break;
+      if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&ctl->full[s], kTileBytes);
+      for (int g = warp * 32 + lane; g < 128; g += kProducerWarps * 32) {
+        const int rg = g >> 2, sb = g & 3;
+        const int32_t* sl = ctl->slot + t * kTok + 4 * rg;
+        tma_gather4(smem_u32(tiles + s * kTileBytes + sb * kSub + rg * 512), &pmap, &ctl->full[s],
+                    sb * 128, sl[0], sl[1], sl[2], sl[3]);
       }
-      umma_commit(&ctl->bar_s);
+      issued = t + 1;
     }
-
-    // ---- softmax of this tile
-    warp_wait(&ctl->bar_s, it & 1, alive, lane, p.err, r);
-    tc_fence_after();
-    const int tok = quarter * 32 + lane;
-    const int e = it * kTok + tok;
-    const bool valid = e < nj && ctl->slot[e] >= 0;
-    float z[32];
-    tmem_load32(tmem + lane_base + hh, z);
+    // Never leave with a copy in flight: wait (bounded) for the last gathers
+    // (already complete unless the pipeline gave up).
+    if (warp == 0 && lane == 0)
+      for (int t = max(0, issued - 2); t < issued; ++t)
+        mbar_wait(&ctl->full[t & 1], (t >> 1) & 1, kWaitNs);
+  } else if (warp == kMmaWarp) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_e4m3(kTok, 2 * kHeads, false, false);
+      const uint32_t idesc_o = idesc_e4m3(128, kHeads, true, true);
+      const uint32_t q0 = smem_u32(qop), p0 = smem_u32(pop);
+      auto issue_o = [&](int u) {
+        const uint32_t a0 = smem_u32(tiles + (u & 1) * kTileBytes);
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      const float4 qe = *reinterpret_cast<const float4*>(&ctl->qexp[hh + i]);
-      z[i] = valid ? z[i] * qe.x : -INFINITY;
-      z[i + 1] = valid ? z[i + 1] * qe.y : -INFINITY;
-      z[i + 2] = valid ? z[i + 2] * qe.z : -INFINITY;
-      z[i + 3] = valid ? z[i + 3] * qe.w : -INFINITY;
-    }
-    {
-      float w[32];
+        for (int term = 0; term < 2; ++term)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = z[i];
-      ctl->red[quarter][hh + lane] = warp_transpose_reduce<true>(w, lane);
-    }
-    __syncthreads();
-    const float tm = fmaxf(fmaxf(ctl->red[0][hh + lane], ctl->red[1][hh + lane]),
-                           fmaxf(ctl->red[2][hh + lane], ctl->red[3][hh + lane]));
-    float alpha = 1.0f;
-    if (tm > m_run + kRescaleLog2) {  // also the first finite maximum (m_run = -inf)
-      alpha = exp2f(m_run - tm);      // 0 while nothing was accumulated
-      m_run = tm;
-      l_part *= alpha;
-    }
+          for (int mb = 0; mb < 4; ++mb)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float m = __shfl_sync(0xFFFFFFFFu, m_run, i);
-      z[i] = z[i] == -INFINITY ? 0.0f : exp2f(z[i] - m);
-    }
-    {
-      // P^T row `tok`: heads hh .. hh+31 = 16-byte chunks hh/8 .. hh/8+3.
-      uint8_t* row = pop + tok * 128;
+            for (int kk = 0; kk < kTok / 32; ++kk) {
+              // A: dims 128mb.. (one 128-byte column block), tokens 32kk..
+              // B: tokens 32kk.. of P^T, heads as the hi or lo 64 bytes.
+              const uint32_t a = a0 + mb * kSub + kk * 4096;
+              const uint32_t b = p0 + kk * 4096 + term * 64;
+              umma_e4m3(tmem + kOCol + mb * kHeads, umma_desc_sw128_mnmajor(a, kSub),
+                        umma_desc_sw128_mnmajor(b, kPBytes), idesc_o,
+                        (u > 0 || term > 0 || kk > 0) ? 1u : 0u);
+            }
+      };
+      bool ok = true;
+      for (int t = 0; t < ntiles && ok; ++t) {
+        const int s = t & 1;
+        ok = thread_wait(ctl, &ctl->full[s], (t >> 1) & 1, p.err, r);
+        if (ok && t >= 2) ok = thread_wait(ctl, &ctl->sfree[s], ((t - 2) >> 1) & 1, p.err, r);
+        if (!ok) break;
+        tc_fence_after();
+        // S^T (cols 128s..): M = 128 tokens, N = 128 (64 heads hi | 64 lo), K = 512
+        const uint32_t a0 = smem_u32(tiles + s * kTileBytes);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(row + (((hh >> 3) + c) ^ (tok & 7)) * 16) =
-            make_uint4(pack_f16x2(z[8 * c], z[8 * c + 1]), pack_f16x2(z[8 * c + 2], z[8 * c + 3]),
-                       pack_f16x2(z[8 * c + 4], z[8 * c + 5]), pack_f16x2(z[8 * c + 6], z[8 * c + 7]));
-    }
-    l_part += warp_transpose_reduce<false>(z, lane);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    const int rescale = __syncthreads_or(it > 0 && alpha != 1.0f);
-    tc_fence_after();
-    if (rescale) {
-      // O^T columns of the heads whose maximum moved, scaled in place.
-      float a[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) a[i] = __shfl_sync(0xFFFFFFFFu, alpha, i);
-#pragma unroll 1
-      for (int mb = 0; mb < 4; ++mb) {
-        float v[32];
-        const uint32_t taddr = tmem + lane_base + 64 + mb * 64 + hh;
-        tmem_load32(taddr, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= a[i];
-        tmem_store32(taddr, v);
-      }
-      tmem_store_wait();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-    }
-
-    // ---- O^T += V^T P^T (4 blocks of M = 128 dims, N = 64 heads, K = 128 tokens)
-    if (tid == 0) {
-      const uint32_t idesc = idesc_f16(128, kHeads, true, true);
-      const uint32_t a0 = smem_u32(tile), b0 = smem_u32(pop);
-#pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-        for (int kk = 0; kk < kTok / 16; ++kk) {
-          // A: dims 128mb.. (two 64-dim sub-tiles, kSubTok apart), tokens 16kk..
-          // B: tokens 16kk.. of P^T (one 64-head chunk per 128-byte row).
-          const uint32_t a = a0 + (2 * mb) * kSubTok + kk * 2048;
-          const uint32_t b = b0 + kk * 2048;
-          umma_bf16(tmem + 64 + mb * 64, umma_desc_sw128_mnmajor(a, kSubTok),
-                    umma_desc_sw128_mnmajor(b, kPBytes), idesc, (it > 0 || kk != 0) ? 1u : 0u);
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint32_t a = a0 + (kk >> 2) * kSub + (kk & 3) * 32;
+          const uint32_t b = q0 + (kk >> 2) * kSub + (kk & 3) * 32;
+          umma_e4m3(tmem + s * 2 * kHeads, umma_desc_sw128_kmajor(a), umma_desc_sw128_kmajor(b),
+                    idesc_s, kk != 0);
+        }
+        umma_commit(&ctl->sfull[s]);
+        if (t >= 1) {
+          ok = thread_wait(ctl, &ctl->pready, (t - 1) & 1, p.err, r);
+          if (!ok) break;
+          tc_fence_after();
+          issue_o(t - 1);
+          umma_commit(&ctl->empty[(t - 1) & 1]);
+          umma_commit(&ctl->odone);
         }
       }
-      umma_commit(&ctl->bar_o);
+      if (ok && ntiles > 0) {
+        ok = thread_wait(ctl, &ctl->pready, (ntiles - 1) & 1, p.err, r);
+        if (ok) {
+          tc_fence_after();
+          issue_o(ntiles - 1);
+          umma_commit(&ctl->empty[(ntiles - 1) & 1]);
+          umma_commit(&ctl->odone);
+        }
+      }
+      // Every MMA issued by this thread is complete before TMEM is released.
+      umma_commit(&ctl->drain);
+      mbar_wait(&ctl->drain, 0, kWaitNs);
+    }
+    __syncwarp();
+  } else if (warp >= kSoftmaxWarp0) {
+    // ================================================================ softmax
+    // Every softmax warp passes the same named barriers in the same order
+    // whatever happens (a timed-out wait only makes the warp skip work), so a
+    // timeout can never leave a barrier short of threads.
+    const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. = tokens
+    const int hh = ((warp - kSoftmaxWarp0) >> 2) * 32;  // heads hh .. hh+31
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int tok = quarter * 32 + lane;
+    float ls[32];                                 // this token lane's share of each head's sum
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ls[i] = 0.0f;
+    float m_lane = -INFINITY;  // running maximum of head hh + lane (log2 units)
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int b = t & 1;
+      float z[32];
+      if (ok) ok = warp_wait(ctl, &ctl->sfull[b], (t >> 1) & 1, lane, p.err, r);
+      if (ok) {
+        float zl[32];
+        tc_fence_after();
+        tmem_load32(tmem + lane_base + b * 2 * kHeads + hh, z);
+        tmem_load32(tmem + lane_base + b * 2 * kHeads + kHeads + hh, zl);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->sfree[b]);
+        const int e = t * kTok + tok;
+        const bool valid = e < nj && ctl->slot[e] >= 0;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 qe = *reinterpret_cast<const float4*>(&ctl->qexp[hh + i]);
+          z[i] = valid ? (z[i] + zl[i]) * qe.x : -INFINITY;
+          z[i + 1] = valid ? (z[i + 1] + zl[i + 1]) * qe.y : -INFINITY;
+          z[i + 2] = valid ? (z[i + 2] + zl[i + 2]) * qe.z : -INFINITY;
+          z[i + 3] = valid ? (z[i + 3] + zl[i + 3]) * qe.w : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = -INFINITY;
+      }
+      bool exceed = false;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 mr = *reinterpret_cast<const float4*>(&ctl->mrun[hh + i]);
+        exceed |= z[i] > mr.x + kPMaxLog2;
+        exceed |= z[i + 1] > mr.y + kPMaxLog2;
+        exceed |= z[i + 2] > mr.z + kPMaxLog2;
+        exceed |= z[i + 3] > mr.w + kPMaxLog2;
+      }
+      bool waited_o = false;
+      if (softmax_sync_or(exceed)) {
+        // Tile maximum of every head, then the new running maxima.
+        {
+          float w[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = z[i];
+          ctl->red[quarter][hh + lane] = warp_transpose_reduce<true>(w, lane);
+        }
+        softmax_sync();
+        const float tm = fmaxf(fmaxf(ctl->red[0][hh + lane], ctl->red[1][hh + lane]),
+                               fmaxf(ctl->red[2][hh + lane], ctl->red[3][hh + lane]));
+        float alpha = 1.0f;
+        if (tm > m_lane + kPMaxLog2) {
+          const float mn = tm - kPResetLog2;
+          alpha = exp2f(m_lane - mn);  // 0 while nothing was accumulated
+          m_lane = mn;
+        }
+        float a[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          a[i] = __shfl_sync(0xFFFFFFFFu, alpha, i);
+          ls[i] *= a[i];
+        }
+        if (ok && t > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+          // O^T columns of the heads whose maximum moved, scaled in place once
+          // the previous tile's O MMAs are complete.
+          ok = warp_wait(ctl, &ctl->odone, (t - 1) & 1, lane, p.err, r);
+          waited_o = true;
+          if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int mb = 0; mb < 4; ++mb) {
+              float v[32];
+              const uint32_t taddr = tmem + lane_base + kOCol + mb * kHeads + hh;
+              tmem_load32(taddr, v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= a[i];
+              tmem_store32(taddr, v);
+            }
+            tmem_store_wait();
+          }
+        }
+        softmax_sync();                        // every warp has read red[] and the old mrun
+        if (quarter == 0) ctl->mrun[hh + lane] = m_lane;
+        softmax_sync();                        // the new mrun is visible
+      }
+      // p = 2^(z - m) as two E4M3 terms (hi, lo); the sums add the unrounded p.
+      uint32_t hiw[8], low[8];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 mr = *reinterpret_cast<const float4*>(&ctl->mrun[hh + i]);
+        const float mm[4] = {mr.x, mr.y, mr.z, mr.w};
+        uint16_t hc[2], lc[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int j = i + 2 * k;
+          const float p0 = z[j] == -INFINITY ? 0.0f : exp2f(z[j] - mm[2 * k]);
+          const float p1 = z[j + 1] == -INFINITY ? 0.0f : exp2f(z[j + 1] - mm[2 * k + 1]);
+          hc[k] = e4m3x2(p0, p1);
+          const float2 hv = e4m3x2_decode(hc[k]);
+          lc[k] = e4m3x2(p0 - hv.x, p1 - hv.y);
+          ls[j] += p0;
+          ls[j + 1] += p1;
+        }
+        hiw[i >> 2] = static_cast<uint32_t>(hc[0]) | (static_cast<uint32_t>(hc[1]) << 16);
+        low[i >> 2] = static_cast<uint32_t>(lc[0]) | (static_cast<uint32_t>(lc[1]) << 16);
+      }
+      // The P buffer is free once the previous tile's O MMAs are complete.
+      if (ok && t > 0 && !waited_o) ok = warp_wait(ctl, &ctl->odone, (t - 1) & 1, lane, p.err, r);
+      if (ok) {
+        // P^T row `tok`: hi bytes of heads hh.. = chunks hh/16, +1; lo = 4 + hh/16, +1.
+        uint8_t* row = pop + tok * 128;
+        const int c0 = hh >> 4, sw = tok & 7;
+        *reinterpret_cast<uint4*>(row + ((c0 ^ sw) * 16)) = make_uint4(hiw[0], hiw[1], hiw[2], hiw[3]);
+        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ sw) * 16)) = make_uint4(hiw[4], hiw[5], hiw[6], hiw[7]);
+        *reinterpret_cast<uint4*>(row + (((c0 + 4) ^ sw) * 16)) = make_uint4(low[0], low[1], low[2], low[3]);
+        *reinterpret_cast<uint4*>(row + (((c0 + 5) ^ sw) * 16)) = make_uint4(low[4], low[5], low[6], low[7]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->pready);
+      }
+    }
+
+    // ---- epilogue: the last O MMAs, per-head sums in fixed order, output
+    if (ok && ntiles > 0) ok = warp_wait(ctl, &ctl->odone, (ntiles - 1) & 1, lane, p.err, r);
+    tc_fence_after();
+    const float l_quarter = warp_transpose_reduce<false>(ls, lane);
+    ctl->red[quarter][hh + lane] = l_quarter;
+    softmax_sync();
+    const int hl = hh + lane;
+    const float l_lane = ((ctl->red[0][hl] + ctl->red[1][hl]) + ctl->red[2][hl]) + ctl->red[3][hl];
+    if (quarter == 0) {
+      if (nsplit > 1)
+        reinterpret_cast<float2*>(p.part_ml)[((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit +
+                                              split) * kHeads + hl] = make_float2(m_lane, l_lane);
+      else if (p.lse != nullptr && hl < nheads)
+        p.lse[static_cast<int64_t>(r) * p.heads + head0 + hl] =
+            m_lane != -INFINITY ? (m_lane + log2f(l_lane)) * 0.69314718055994531f : -INFINITY;
+    }
+    // O^T: lane = dim 128mb + 32*quarter + lane, column = head.  For a fixed
+    // head the 32 lanes write 32 consecutive dims.
+    const float sc_lane = (m_lane != -INFINITY && l_lane > 0.0f) ? p.kv_scale / l_lane : 0.0f;
+    float sc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, sc_lane, i);
+#pragma unroll 1
+    for (int mb = 0; mb < 4; ++mb) {
+      float v[32];
+      tmem_load32(tmem + lane_base + kOCol + mb * kHeads + hh, v);
+      const int d = mb * 128 + quarter * 32 + lane;
+      if (!ok || ntiles == 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      }
+      if (nsplit > 1) {
+        float* dst = p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) *
+                                    (kHeads * 512) + d;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dst[(hh + i) * 512] = v[i];
+      } else {
+        uint16_t* dst = p.out + (static_cast<int64_t>(r) * p.heads + head0) * 512 + d;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (hh + i < nheads)
+            dst[(hh + i) * 512] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i] * sc[i]));
+      }
     }
   }
-  if (ntiles > 0) warp_wait(&ctl->bar_o, (ntiles - 1) & 1, alive, lane, p.err, r);
-  tc_fence_after();
 
-  // ---- per-head sums over the four lane quarters, in fixed order
-  ctl->red[quarter][hh + lane] = l_part;
+  tc_fence_before();
   __syncthreads();
-  if (quarter == 0) {
-    const int h = hh + lane;
-    const float l = ((ctl->red[0][h] + ctl->red[1][h]) + ctl->red[2][h]) + ctl->red[3][h];
-    ctl->lfin[h] = l;
-    ctl->mfin[h] = m_run;
-    if (nsplit > 1)
-      reinterpret_cast<float2*>(p.part_ml)[((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit +
-                                            split) * kHeads + h] = make_float2(m_run, l);
-    else if (p.lse != nullptr && h < nheads)
-      p.lse[static_cast<int64_t>(r) * p.heads + head0 + h] =
-          m_run != -INFINITY ? (m_run + log2f(l)) * 0.69314718055994531f : -INFINITY;
-  }
-
-  // ---- O^T from TMEM, staged as rows [64 heads][512 dims] in the tile region
-  {
-    // Warp w reads lane quarter w%4 (dims 32*(w%4) + lane of each block) of
-    // blocks mb = 2*(w/4), 2*(w/4)+1, all 64 heads (consecutive lanes ->
-    // consecutive floats).
-    float* stage = reinterpret_cast<float*>(tile);
-    const int dl = quarter * 32 + lane;
-#pragma unroll
-    for (int bb = 0; bb < 2; ++bb) {
-      const int mb = (warp >> 2) * 2 + bb;
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        float v[32];
-        tmem_load32(tmem + lane_base + 64 + mb * 64 + hc * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)  // (no tile ran: nothing was accumulated)
-          stage[(hc * 32 + i) * 512 + mb * 128 + dl] = ntiles > 0 ? v[i] : 0.0f;
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-    const float4* src = reinterpret_cast<const float4*>(stage);
-    if (nsplit > 1) {
-      // This split's partial rows, 16-byte coalesced stores (512 B per thread).
-      float4* dst = reinterpret_cast<float4*>(
-          p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) * (kHeads * 512));
-#pragma unroll 8
-      for (int i = tid; i < kHeads * 128; i += kThreads) dst[i] = src[i];
-    } else {
-      // The only split: normalise, round to bf16, write the output rows.
-#pragma unroll 4
-      for (int i = tid; i < nheads * 128; i += kThreads) {
-        const int h = i >> 7;
-        const float l = ctl->lfin[h];
-        const float scale = ctl->mfin[h] != -INFINITY ? p.kv_scale / l : 0.0f;
-        const float4 v = src[i];
-        uint2 packed;
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.x) : "f"(v.y * scale), "f"(v.x * scale));
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.y) : "f"(v.w * scale), "f"(v.z * scale));
-        reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512)[i & 127] =
-            packed;
-      }
-    }
-  }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -589,7 +733,7 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
       acc.w += v.w * f;
     }
   }
-  const float scale = mmax != -INFINITY ? p.kv_scale / lsum : 0.0f;
+  const float scale = (mmax != -INFINITY && lsum > 0.0f) ? p.kv_scale / lsum : 0.0f;
   uint2 packed;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.x) : "f"(acc.y * scale), "f"(acc.x * scale));
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.y) : "f"(acc.w * scale), "f"(acc.z * scale));
@@ -608,7 +752,7 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
 }  // namespace
 
 void plan_mla_decode_tc(DecodeParams& p) {
-  const int target = (p.heads > kHeads ? 4 : 2) * kTok;
+  const int target = kTilesPerSplit * kTok;
   int n = (p.topk + target - 1) / target;
   if (n < 1) n = 1;
   p.splits = n;
@@ -638,7 +782,8 @@ void mla_decode_tc_bind_workspace(DecodeParams& p, void* workspace) {
                                        ((units * 512 * sizeof(float) + 255) & ~static_cast<size_t>(255)));
 }
 
-cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_mla_decode_tc(const DecodeParams& p, const CUtensorMap& pmap,
+                                 cudaStream_t stream) {
   if (p.split_len > kMaxTiles * kTok) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -652,7 +797,7 @@ cudaError_t launch_mla_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, pmap, p);
   if (e != cudaSuccess || p.splits == 1) return e;
   cudaLaunchConfig_t mcfg = {};
   mcfg.gridDim = dim3(p.heads, p.rows.rows, 1);
