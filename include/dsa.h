@@ -163,10 +163,13 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  *   q   [rows][heads][latent_dim] bf16       pool [nslots][latent_dim] FP8
  *   sel [rows][topk] int32                   out  [rows][heads][latent_dim] bf16
  * latent_dim must be 512; heads a multiple of 16; nslots below 2^31
- * (DSA_ERR_UNSUPPORTED otherwise).  A row's selection is cut into splits of
- * at most 256 entries (512 with more than 64 heads) whose count depends only
- * on topk and heads, so each row's result is bit-identical whatever the other
- * rows of the call are.  With more than one split the partial outputs pass
+ * (DSA_ERR_UNSUPPORTED otherwise).  Numerics: the logits are the exact
+ * products of the bf16 q and the E4M3 latent accumulated in FP32 on the
+ * tensor cores; the softmax weights enter the weighted sum as two E4M3 terms
+ * (about bf16 precision; weights 2^18 below a head's largest drop out), the
+ * normalising sums and lse use the unrounded weights.  A row's selection is
+ * cut into splits of at most 512 entries whose count depends only on topk, so
+ * each row's result is bit-identical whatever the other rows of the call are.  With more than one split the partial outputs pass
  * through the workspace (L2-resident, discarded after the merge), which must
  * hold dsa_workspace_bytes(rows, heads, topk) bytes, 256-byte aligned
  * (DSA_ERR_WORKSPACE otherwise).
