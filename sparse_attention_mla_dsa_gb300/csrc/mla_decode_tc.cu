@@ -307,8 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (tid < kHeads) ctl->mrun[tid] = -INFINITY;
-  // ---- Q: warp w converts heads w, w+10, ...; lane l dims 16l..16l+15.  The
-  // loads are issued first: they do not depend on the kernel before.
+  // ---- Q: warp w converts heads w, w+12, ...; lane l dims 16l..16l+15.  Q
+  // does not depend on the kernels before, so its loads and conversion run
+  // before the dependency wait (overlapping the top-k under dependent launch).
   constexpr int kQPer = (kHeads + kThreads / 32 - 1) / (kThreads / 32);
   uint4 qa[kQPer], qb[kQPer];
 #pragma unroll
@@ -324,43 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       qb[j] = make_uint4(0, 0, 0, 0);
     }
   }
-  grid_dep_wait();  // the selection comes from the kernel before
-
-  // ---- slots of every entry of this split (two dependent loads each)
-  {
-    constexpr int kPer = (kMaxTiles * kTok + kThreads - 1) / kThreads;
-    int idx[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = tid + i * kThreads;
-      idx[i] = e < nj ? p.sel[static_cast<int64_t>(r) * p.topk + j0 + e] : -1;  // plain load
-    }
-    const int32_t* bt = p.rows.block_table + static_cast<int64_t>(r) * p.rows.bt_stride;
-    const int bs = p.rows.block_size;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = tid + i * kThreads;
-      if (e >= kMaxTiles * kTok) break;
-      int32_t slot = -1;
-      const int t = idx[i];
-      if (t != -1) {
-        if (t < 0 || t >= len) {
-          if (report) record_error(p.err, DSA_DEVERR_SELECT, r);
-        } else {
-          const int blk = t / bs;
-          const int phys = blk < p.rows.max_blocks_per_seq ? __ldg(bt + blk) : -1;
-          const int64_t s = static_cast<int64_t>(phys) * bs + t % bs;
-          if (phys < 0 || s >= p.nslots) {
-            if (report) record_error(p.err, DSA_DEVERR_BLOCK, r);
-          } else {
-            slot = static_cast<int32_t>(s);
-          }
-        }
-      }
-      ctl->slot[e] = slot;
-    }
-  }
-
   // ---- Q operand: q*2^s = hi + lo (E4M3 each), s a power of two per head
   // putting the head's largest |q| in [128, 256).  Row h holds hi, row 64+h lo.
 #pragma unroll
@@ -405,6 +369,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     *reinterpret_cast<uint4*>(blk + h * 128 + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     *reinterpret_cast<uint4*>(blk + (h + kHeads) * 128 + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
+  grid_dep_wait();  // the selection comes from the kernel before
+
+  // ---- slots of every entry of this split (two dependent loads each)
+  {
+    constexpr int kPer = (kMaxTiles * kTok + kThreads - 1) / kThreads;
+    int idx[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
+      idx[i] = e < nj ? p.sel[static_cast<int64_t>(r) * p.topk + j0 + e] : -1;  // plain load
+    }
+    const int32_t* bt = p.rows.block_table + static_cast<int64_t>(r) * p.rows.bt_stride;
+    const int bs = p.rows.block_size;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
+      if (e >= kMaxTiles * kTok) break;
+      int32_t slot = -1;
+      const int t = idx[i];
+      if (t != -1) {
+        if (t < 0 || t >= len) {
+          if (report) record_error(p.err, DSA_DEVERR_SELECT, r);
+        } else {
+          const int blk = t / bs;
+          const int phys = blk < p.rows.max_blocks_per_seq ? __ldg(bt + blk) : -1;
+          const int64_t s = static_cast<int64_t>(phys) * bs + t % bs;
+          if (phys < 0 || s >= p.nslots) {
+            if (report) record_error(p.err, DSA_DEVERR_BLOCK, r);
+          } else {
+            slot = static_cast<int32_t>(s);
+          }
+        }
+      }
+      ctl->slot[e] = slot;
+    }
+  }
+
   fence_proxy_async_smem();  // generic-proxy operand writes -> visible to the tensor core
   tc_fence_before();
   __syncthreads();           // slots, qexp, Q operand, barriers, TMEM address
@@ -414,16 +415,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProducerWarps) {
     // ================================================================ gather
     // Copy g (0..127) of a tile moves rows 4(g/4) .. 4(g/4)+3 of the tile,
-    // column block g%4; lane l of producer warp w issues copies 32w + l and,
-    // below 128, 32w + l + 96.  Warp 0 lane 0 posts the tile's byte count;
-    // other copies may land before it does (the transaction count may run
-    // ahead of the expectation).
+    // column block g%4; producer warp w issues copies w, w+3, w+6, ... (43,
+    // 43 and 42 of them), lane l the ones with index w + 3(l + 32j).  Warp 0
+    // lane 0 posts the tile's byte count; other copies may land before it
+    // does (the transaction count may run ahead of the expectation).
     int issued = 0;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t & 1;
       if (t >= 2 && !warp_wait(ctl, &ctl->empty[s], ((t - 2) >> 1) & 1, lane, p.err, r)) break;
       if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&ctl->full[s], kTileBytes);
-      for (int g = warp * 32 + lane; g < 128; g += kProducerWarps * 32) {
+      for (int g = warp + kProducerWarps * lane; g < 128; g += kProducerWarps * 32) {
         const int rg = g >> 2, sb = g & 3;
         const int32_t* sl = ctl->slot + t * kTok + 4 * rg;
         tma_gather4(smem_u32(tiles + s * kTileBytes + sb * kSub + rg * 512), &pmap, &ctl->full[s],
