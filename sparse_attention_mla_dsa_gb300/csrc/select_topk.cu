@@ -8,7 +8,8 @@
 // SM; C = 1 up to 4k tokens, at most 8).  CTA c keeps tokens [c*S, (c+1)*S) of the row in
 // shared memory as order-preserving 32-bit keys, read from global once.  A
 // four-digit radix select (8 bits per digit) finds the key T of the k-th
-// largest token.  Scores bunch into few high-order bins, so every histogram
+// largest token, stopping early once every key left in the threshold bin is
+// needed.  Scores bunch into few high-order bins, so every histogram
 // keeps one counter per (bin, lane): the 32 lanes of a warp never add to the
 // same address.  With C > 1 the per-CTA bin totals are summed through
 // distributed shared memory and every CTA takes the same decision.  The
@@ -91,13 +92,16 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total)
   return before + x - v;
 }
 
-struct TopkShared {
+// The keys follow this block in shared memory and are read as 16-byte
+// vectors: its size must stay a multiple of 16.
+struct alignas(16) TopkShared {
   int hist[kBins * 32];          // [bin][lane] counters of the current pass
   int bin_tot[4][kBins];         // per-pass bin totals of this CTA (read remotely)
   alignas(8) int counts[2];      // this CTA's (key > T, key == T) counts
   int warp_tot[kWarps];
-  int found_bin, found_above;
+  int found_bin, found_above, found_count;
 };
+static_assert(sizeof(TopkShared) % 16 == 0, "keys must start 16-byte aligned");
 
 __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
   // ---- radix select, 8 bits per pass from the top
   uint32_t prefix = 0, prefix_mask = 0;
   int remaining = want;
+  bool all_taken = false;  // (uniform) every key equal to the threshold prefix is taken
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
 #pragma unroll
@@ -202,31 +207,45 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
       if (above < remaining && above + c >= remaining) {
         sh.found_bin = kBins - 1 - (warp * 32 + lane);
         sh.found_above = above;
+        sh.found_count = c;
       }
     }
     __syncthreads();
     remaining -= sh.found_above;
     prefix |= static_cast<uint32_t>(sh.found_bin) << shift;
     prefix_mask |= 255u << shift;
+    all_taken = sh.found_count == remaining;
     __syncthreads();  // found_* / hist are rewritten by the next pass
+    // Every key in the threshold bin is needed: the selection is the keys
+    // whose top bits are >= the prefix found so far, whatever the lower bits.
+    if (all_taken) break;
   }
   const uint32_t thresh = prefix;
   const int take_equal = remaining;  // >= 1, counted over the whole row
 
-  // ---- this CTA's counts, then its offsets from the CTAs before it
+  // ---- this CTA's counts, then its offsets from the CTAs before it.  When
+  // every key at the threshold prefix is taken a key is selected iff its
+  // masked bits are >= the prefix (one count, one scan per chunk); otherwise
+  // keys above the threshold are taken and the tied ones by rank, lowest index
+  // first.
   int out_base = 0, eq_base = 0;
   bool exit_arrived = false;
   if (C > 1) {
     int gt_n = 0, eq_n = 0;
+    if (all_taken) {
 #pragma unroll 8
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = keys[i];
-      gt_n += key > thresh;
-      eq_n += key == thresh;
+      for (int i = tid; i < n; i += kThreads) gt_n += (keys[i] & prefix_mask) >= thresh;
+    } else {
+#pragma unroll 8
+      for (int i = tid; i < n; i += kThreads) {
+        const uint32_t key = keys[i];
+        gt_n += key > thresh;
+        eq_n += key == thresh;
+      }
     }
-    int gt_total, eq_total;
+    int gt_total, eq_total = 0;
     block_excl_scan(gt_n, sh.warp_tot, gt_total);
-    block_excl_scan(eq_n, sh.warp_tot, eq_total);
+    if (!all_taken) block_excl_scan(eq_n, sh.warp_tot, eq_total);
     if (tid == 0) {
       sh.counts[0] = gt_total;
       sh.counts[1] = eq_total;
@@ -251,7 +270,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
   // ---- ordered output of this slice
   for (int c0 = 0; c0 < n; c0 += kThreads * kItems) {
     const int t0 = c0 + tid * kItems;
-    uint32_t gt = 0, eq = 0;
     uint32_t kv[kItems];
     if (t0 + kItems <= n) {  // two 16-byte loads (t0 is a multiple of 8)
       const uint4 u0 = *reinterpret_cast<const uint4*>(keys + t0);
@@ -262,29 +280,36 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
 #pragma unroll
       for (int i = 0; i < kItems; ++i) kv[i] = t0 + i < n ? keys[t0 + i] : 0u;
     }
+    uint32_t take = 0;
+    if (all_taken) {
 #pragma unroll
-    for (int i = 0; i < kItems; ++i) {
-      if (t0 + i < n) {
-        gt |= static_cast<uint32_t>(kv[i] > thresh) << i;
-        eq |= static_cast<uint32_t>(kv[i] == thresh) << i;
-      }
-    }
-    int chunk_eq;
-    int rank = eq_base + block_excl_scan(__popc(eq), sh.warp_tot, chunk_eq);
-    uint32_t take = gt;
+      for (int i = 0; i < kItems; ++i)
+        if (t0 + i < n) take |= static_cast<uint32_t>((kv[i] & prefix_mask) >= thresh) << i;
+    } else {
+      uint32_t eq = 0;
 #pragma unroll
-    for (int i = 0; i < kItems; ++i) {
-      if ((eq >> i) & 1u) {
-        if (rank < take_equal) take |= 1u << i;
-        ++rank;
+      for (int i = 0; i < kItems; ++i) {
+        if (t0 + i < n) {
+          take |= static_cast<uint32_t>(kv[i] > thresh) << i;
+          eq |= static_cast<uint32_t>(kv[i] == thresh) << i;
+        }
       }
+      int chunk_eq;
+      int rank = eq_base + block_excl_scan(__popc(eq), sh.warp_tot, chunk_eq);
+#pragma unroll
+      for (int i = 0; i < kItems; ++i) {
+        if ((eq >> i) & 1u) {
+          if (rank < take_equal) take |= 1u << i;
+          ++rank;
+        }
+      }
+      eq_base += chunk_eq;
     }
     int chunk_take;
     int pos = out_base + block_excl_scan(__popc(take), sh.warp_tot, chunk_take);
 #pragma unroll
     for (int i = 0; i < kItems; ++i)
       if ((take >> i) & 1u) out[pos++] = lo + t0 + i;
-    eq_base += chunk_eq;
     out_base += chunk_take;
   }
   for (int i = want + crank * kThreads + tid; i < p.topk; i += C * kThreads) out[i] = -1;

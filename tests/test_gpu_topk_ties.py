@@ -1,0 +1,55 @@
+"""GPU top-k on crafted scores: exact ties at the threshold, all-equal rows,
+signed zeros and negatives, over row lengths that exercise one CTA and an
+eight-CTA cluster per row, against the oracle's full-sort selection
+("glm5next_dsa/layer.rs", notes on batch_select_enabled / select_rows_batched:
+score DESC, then index ASC).  Bit-exact: the selection is integer work.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_attention_mla_dsa_gb300 import api
+    api.load()
+    api.dsa_get_error(reset=True)
+    return api
+
+
+def _patterns(rng, n):
+    ints = rng.integers(0, 50, size=n).astype(np.float32)              # many exact ties
+    zeros = np.zeros(n, np.float32)                                      # one tie class
+    signed = rng.choice(np.array([-0.0, 0.0, -1.0, 2.0], np.float32), size=n)
+    cont = rng.standard_normal(n).astype(np.float32)
+    few = np.where(rng.random(n) < 0.01, 5.0, 1.0).astype(np.float32)   # ties above and at T
+    return {"ints": ints, "zeros": zeros, "signed": signed, "continuous": cont, "few": few}
+
+
+@pytest.mark.parametrize("max_len,lens", [
+    (3000, [1, 100, 2047, 2048, 2049, 3000]),          # one CTA per row
+    (70000, [2049, 5000, 40000, 70000]),               # clusters of eight CTAs
+])
+def test_topk_ties_match_oracle(api, oracle, max_len, lens):
+    rng = np.random.default_rng(11)
+    topk = 2048
+    for name, _ in _patterns(rng, 4).items():
+        R = len(lens)
+        scores = np.full((R, max_len), np.nan, np.float32)
+        for r, L in enumerate(lens):
+            scores[r, :L] = _patterns(np.random.default_rng(100 + r), L)[name]
+        seq_lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        rows = api.make_rows(seq_lens)
+        s_dev = torch.from_numpy(scores).cuda()
+        sel = torch.full((R, topk), -7, dtype=torch.int32, device="cuda")
+        api.dsa_select_topk(rows, s_dev, max_len, topk, sel)
+        torch.cuda.synchronize()
+        assert api.dsa_get_error(reset=True)[0] == 0
+        got = sel.cpu().numpy()
+        for r, L in enumerate(lens):
+            ref = oracle.select_topk_row(scores[r, :L].astype(np.float64), L, topk)
+            assert np.array_equal(got[r], ref), f"{name} max_len {max_len} row len {L}"
