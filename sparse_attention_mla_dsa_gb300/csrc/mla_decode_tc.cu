@@ -58,8 +58,9 @@ constexpr int kSoftmaxWarp0 = 4;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kHeads = 64;             // heads per CTA
 constexpr int kTok = 128;              // entries per tile (MMA M of S^T)
-constexpr int kTilesPerSplit = 4;      // split length target (tiles)
-constexpr int kMaxTiles = 4;           // tiles per split the CTA can hold slots for
+constexpr int kTilesPerSplit = 4;      // split length target (tiles), up to 64 heads
+constexpr int kTilesPerSplitWide = 16; // the same with more than 64 heads (two head-group CTAs)
+constexpr int kMaxTiles = 16;          // tiles per split the CTA can hold slots for
 constexpr int kMergeThreads = 128;     // merge kernel: one CTA per (row, head), 4 dims per thread
 constexpr float kPMaxLog2 = 8.75f;     // p = 2^(z - m) stays below 2^8.75 < 448
 constexpr float kPResetLog2 = 8.0f;    // a reset maps the tile maximum to p = 2^8
@@ -250,16 +251,6 @@ __device__ __forceinline__ bool warp_wait(Ctl* c, uint64_t* bar, uint32_t parity
   }
   return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
-// Single-thread form (the MMA issuer).
-__device__ __forceinline__ bool thread_wait(Ctl* c, uint64_t* bar, uint32_t parity, int* err,
-                                            int r) {
-  if (aborted(c)) return false;
-  if (mbar_wait(bar, parity, kWaitNs)) return true;
-  record_error(err, DSA_DEVERR_TIMEOUT, r);
-  set_abort(c);
-  return false;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ CUtensorMap pmap, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -385,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int e = tid + i * kThreads;
-      if (e >= kMaxTiles * kTok) break;
+      if (e >= ntiles * kTok) break;  // the tiles of this split only
       int32_t slot = -1;
       const int t = idx[i];
       if (t != -1) {
@@ -460,39 +451,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (u > 0 || term > 0 || kk > 0) ? 1u : 0u);
             }
       };
-      bool ok = true;
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const int s = t & 1;
-        ok = thread_wait(ctl, &ctl->full[s], (t >> 1) & 1, p.err, r);
-        if (ok && t >= 2) ok = thread_wait(ctl, &ctl->sfree[s], ((t - 2) >> 1) & 1, p.err, r);
-        if (!ok) break;
-        tc_fence_after();
-        // S^T (cols 128s..): M = 128 tokens, N = 128 (64 heads hi | 64 lo), K = 512
-        const uint32_t a0 = smem_u32(tiles + s * kTileBytes);
+      // Event-driven issue: O(u) goes out as soon as the softmax of tile u is
+      // done (it frees a ring stage for the gather), S(t) as soon as tile t has
+      // landed and its S buffer is free; neither waits behind the other.
+      int ns = 0, no = 0;  // next S and next O to issue
+      uint64_t t_last = global_ns();
+      uint32_t idle = 0;
+      while (no < ntiles) {
+        bool issued = false;
+        if (no < ns && mbar_try_wait(&ctl->pready, no & 1)) {
+          tc_fence_after();
+          issue_o(no);
+          umma_commit(&ctl->empty[no & 1]);
+          umma_commit(&ctl->odone);
+          ++no;
+          issued = true;
+        } else if (ns < ntiles && mbar_try_wait(&ctl->full[ns & 1], (ns >> 1) & 1) &&
+                   (ns < 2 || mbar_try_wait(&ctl->sfree[ns & 1], ((ns - 2) >> 1) & 1))) {
+          tc_fence_after();
+          // S^T (cols 128s..): M = 128 tokens, N = 128 (64 heads hi | 64 lo), K = 512
+          const int s = ns & 1;
+          const uint32_t a0 = smem_u32(tiles + s * kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const uint32_t a = a0 + (kk >> 2) * kSub + (kk & 3) * 32;
-          const uint32_t b = q0 + (kk >> 2) * kSub + (kk & 3) * 32;
-          umma_e4m3(tmem + s * 2 * kHeads, umma_desc_sw128_kmajor(a), umma_desc_sw128_kmajor(b),
-                    idesc_s, kk != 0);
+          for (int kk = 0; kk < 16; ++kk) {
+            const uint32_t a = a0 + (kk >> 2) * kSub + (kk & 3) * 32;
+            const uint32_t b = q0 + (kk >> 2) * kSub + (kk & 3) * 32;
+            umma_e4m3(tmem + s * 2 * kHeads, umma_desc_sw128_kmajor(a), umma_desc_sw128_kmajor(b),
+                      idesc_s, kk != 0);
+          }
+          umma_commit(&ctl->sfull[s]);
+          ++ns;
+          issued = true;
         }
-        umma_commit(&ctl->sfull[s]);
-        if (t >= 1) {
-          ok = thread_wait(ctl, &ctl->pready, (t - 1) & 1, p.err, r);
-          if (!ok) break;
-          tc_fence_after();
-          issue_o(t - 1);
-          umma_commit(&ctl->empty[(t - 1) & 1]);
-          umma_commit(&ctl->odone);
-        }
-      }
-      if (ok && ntiles > 0) {
-        ok = thread_wait(ctl, &ctl->pready, (ntiles - 1) & 1, p.err, r);
-        if (ok) {
-          tc_fence_after();
-          issue_o(ntiles - 1);
-          umma_commit(&ctl->empty[(ntiles - 1) & 1]);
-          umma_commit(&ctl->odone);
+        if (issued) {
+          idle = 0;
+          t_last = global_ns();
+        } else if ((++idle & 255u) == 0) {
+          if (aborted(ctl)) break;
+          if (global_ns() - t_last > kWaitNs) {
+            record_error(p.err, DSA_DEVERR_TIMEOUT, r);
+            set_abort(ctl);
+            break;
+          }
         }
       }
       // Every MMA issued by this thread is complete before TMEM is released.
@@ -753,7 +753,9 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
 }  // namespace
 
 void plan_mla_decode_tc(DecodeParams& p) {
-  const int target = kTilesPerSplit * kTok;
+  // A function of topk and heads only, so a row's arithmetic does not depend
+  // on the other rows of the launch.
+  const int target = (p.heads > kHeads ? kTilesPerSplitWide : kTilesPerSplit) * kTok;
   int n = (p.topk + target - 1) / target;
   if (n < 1) n = 1;
   p.splits = n;
