@@ -45,7 +45,7 @@ DESCRIPTIONS = {
             "topk 2048, latent write of the new row",
 }
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "index_scores_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
 def _args():
@@ -137,27 +137,30 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _source_hash():
-    p = os.path.join(ROOT, "sparse_attention_mla_dsa_gb300", "csrc", "index_scores.cu")
+def _source_hash(name):
+    p = os.path.join(ROOT, "sparse_attention_mla_dsa_gb300", "csrc", name)
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def _traffic_per_unit(workload):
-    """DRAM bytes per key token of the indexer from the committed ncu summary,
-    valid only while index_scores.cu is unchanged since the capture."""
+def _traffic(workload, stage):
+    """DRAM bytes (read + write) per launch of a stage from the committed ncu
+    table, valid only while the stage's kernel source is unchanged since the
+    capture; None otherwise."""
     try:
-        kv = {}
         with open(TRAFFIC_FILE) as f:
             for ln in f:
-                if ":" in ln and not ln.lstrip().startswith("#"):
-                    k, v = ln.split(":", 1)
-                    kv[k.strip()] = v.strip()
-        if kv.get("source_sha256_16") != _source_hash():
-            return None
-        return float(kv["dram_bytes_per_key_token"])
-    except (OSError, KeyError, ValueError):
+                parts = ln.split()
+                if not parts or parts[0].startswith("#") or len(parts) < 6:
+                    continue
+                w, st, src, sha, rd, wr = parts[:6]
+                if w == workload and st == stage:
+                    if _source_hash(src) != sha:
+                        return None
+                    return int(rd) + int(wr)
+    except (OSError, ValueError):
         return None
+    return None
 
 
 def stage_bytes(wl):
@@ -302,11 +305,7 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     dominant = max(stages, key=lambda s: stage_ms[s])
     ach = sb[dominant] / (stage_ms[dominant] / 1e3) / 1e9
-    traffic = None
-    if dominant == "index_scores":
-        per_tok = _traffic_per_unit(args.workload)
-        if per_tok is not None:
-            traffic = per_tok * key_tokens
+    traffic = _traffic(args.workload, dominant)
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
                 "traffic": traffic, "algorithmic_bytes": sb[dominant],
