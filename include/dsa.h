@@ -168,7 +168,7 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  * tensor cores; the softmax weights enter the weighted sum as two E4M3 terms
  * (about bf16 precision; weights 2^18 below a head's largest drop out), the
  * normalising sums and lse use the unrounded weights.  A row's selection is
- * cut into splits of at most 512 entries (2048 with more than 64 heads) whose
+ * cut into splits of at most 256 entries (2048 with more than 64 heads) whose
  * count depends only on topk and heads, so each row's result is bit-identical
  * whatever the other rows of the call are.  With more than one split the partial outputs pass
  * through the workspace (L2-resident, discarded after the merge), which must

@@ -9,9 +9,9 @@
 // head:  z_j = sm_scale * kv_scale * (Q . e4m3(latent_j)),  p = softmax(z),
 //        out = kv_scale * sum_j p_j e4m3(latent_j),  lse = log sum_j exp(z_j).
 //
-// A row's selection is cut into n splits of at most 512 entries; n depends on
-// topk only, never on the number of rows, so a row's arithmetic is the same in
-// any launch.  One CTA (12 warps) runs one split of one (row, 64-head group)
+// A row's selection is cut into n splits of at most 256 entries (2048 with
+// more than 64 heads); n depends on topk and heads only, never on the number
+// of rows, so a row's arithmetic is the same in any launch.  One CTA (12 warps) runs one split of one (row, 64-head group)
 // as a pipeline over 128-entry tiles:
 //   - the latent stays FP8: TMA tile::gather4 copies the selected 512-byte
 //     rows (4 rows x one 128-byte column block per copy, rows that are not
@@ -58,7 +58,7 @@ constexpr int kSoftmaxWarp0 = 4;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kHeads = 64;             // heads per CTA
 constexpr int kTok = 128;              // entries per tile (MMA M of S^T)
-constexpr int kTilesPerSplit = 4;      // split length target (tiles), up to 64 heads
+constexpr int kTilesPerSplit = 2;      // split length target (tiles), up to 64 heads
 constexpr int kTilesPerSplitWide = 16; // the same with more than 64 heads (two head-group CTAs)
 constexpr int kMaxTiles = 16;          // tiles per split the CTA can hold slots for
 constexpr int kMergeThreads = 128;     // merge kernel: one CTA per (row, head), 4 dims per thread

@@ -40,7 +40,7 @@ def test_host_helpers_without_gpu():
     assert lib.dsa_status_string(5).startswith(b"workspace")
     lib.dsa_workspace_bytes.restype = ctypes.c_size_t
     lib.dsa_workspace_bytes.argtypes = [ctypes.c_int32] * 3
-    units = 1 * 1 * 4 * 64                                   # rows x head groups x splits x 64
+    units = 1 * 1 * 8 * 64                                   # rows x head groups x splits x 64
     assert lib.dsa_workspace_bytes(1, 64, 2048) == units * 512 * 4 + units * 8
     units = 2 * 2 * 1 * 64                                   # 128 heads: two head groups, one split
     assert lib.dsa_workspace_bytes(2, 128, 2048) == units * 512 * 4 + units * 8
@@ -58,10 +58,10 @@ def test_product_path_does_not_import_the_oracle():
 
 def test_decode_split_plan_depends_on_topk_and_heads_only():
     from sparse_attention_mla_dsa_gb300 import api
-    assert api.decode_splits(64, 2048) == 4                 # splits of at most 512 entries
+    assert api.decode_splits(64, 2048) == 8                 # splits of at most 256 entries
     assert api.decode_splits(128, 2048) == 1                # above 64 heads: up to 2048 entries
     assert api.decode_splits(128, 4096) == 2
     assert api.decode_splits(16, 256) == 1
-    assert api.decode_splits(64, 513) == 2
+    assert api.decode_splits(64, 257) == 2
     for rows in (1, 7, 64):
         assert api.dsa_workspace_bytes(rows, 64, 2048) == rows * api.dsa_workspace_bytes(1, 64, 2048)

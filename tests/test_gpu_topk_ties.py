@@ -1,6 +1,6 @@
 """GPU top-k on crafted scores: exact ties at the threshold, all-equal rows,
-signed zeros and negatives, over row lengths that exercise one CTA and an
-eight-CTA cluster per row, against the oracle's full-sort selection
+signed zeros and negatives, over row lengths that exercise one CTA and
+clusters of five and eight CTAs per row, against the oracle's full-sort selection
 ("glm5next_dsa/layer.rs", notes on batch_select_enabled / select_rows_batched:
 score DESC, then index ASC).  Bit-exact: the selection is integer work.
 """
@@ -32,7 +32,9 @@ def _patterns(rng, n):
 
 @pytest.mark.parametrize("max_len,lens", [
     (3000, [1, 100, 2047, 2048, 2049, 3000]),          # one CTA per row
+    (20000, [2049, 5000, 20000]),                      # clusters of five CTAs
     (70000, [2049, 5000, 40000, 70000]),               # clusters of eight CTAs
+    (270000, [33000, 140000, 270000]),                 # eight CTAs, 34k keys each
 ])
 def test_topk_ties_match_oracle(api, oracle, max_len, lens):
     rng = np.random.default_rng(11)
