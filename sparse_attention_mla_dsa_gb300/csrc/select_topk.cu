@@ -160,12 +160,14 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
       if ((key & prefix_mask) == prefix) atomicAdd(&sh.hist[((key >> shift) & 255u) * 32 + lane], 1);
     }
     __syncthreads();
-    // Bin totals: 2 threads per bin, 16 lane counters each.
+    // Bin totals: 2 threads per bin, 16 lane counters each.  The 16 threads
+    // of a warp that share a half start at different counters (rotation by
+    // the bin), so each load of the warp touches 32 distinct banks.
     {
       const int b = tid >> 1, q = tid & 1;
       int t = 0;
 #pragma unroll
-      for (int l = 0; l < 16; ++l) t += sh.hist[b * 32 + q * 16 + l];
+      for (int l = 0; l < 16; ++l) t += sh.hist[b * 32 + q * 16 + ((l + b) & 15)];
       t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
       if (q == 0) sh.bin_tot[pass][b] = t;
     }
