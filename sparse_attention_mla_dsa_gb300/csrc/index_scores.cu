@@ -264,13 +264,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const int heads = p.heads;
     const int cols_per_row = (heads % 16 == 0) ? heads : npad;  // heads%16 != 0 -> one row
+    // Each tile's gate is loaded one tile ahead (the first before the
+    // dependency wait: gates are inputs, not a predecessor's output), so the
+    // load's DRAM latency hides behind the TMA and the MMAs.
+    const int max_len_group = ctl->max_len_group;
+    auto load_gate = [&](int i) {
+      const int t = (t_begin + i) * kTileM + lane_tok;
+      return (i < ntiles && t < max_len_group) ? __ldg(p.gate + base + t) : static_cast<uint16_t>(0);
+    };
+    uint16_t g_next = load_gate(0);
     grid_dep_wait();  // the previous top-k may still read the scores buffer
     for (int i = 0; i < ntiles; ++i) {
       if (__shfl_sync(0xFFFFFFFFu, aborted(ctl) ? 1 : 0, 0)) break;
       const int a = i & 1;
       const int t = (t_begin + i) * kTileM + lane_tok;
-      float g = 0.0f;
-      if (t < ctl->max_len_group) g = __bfloat162float(__ushort_as_bfloat16(__ldg(p.gate + base + t)));
+      const float g = __bfloat162float(__ushort_as_bfloat16(g_next));
+      g_next = load_gate(i + 1);
       // One lane polls; the warp then continues together (tcgen05.ld is
       // warp-collective), ordered after the wait by the warp sync + fence.
       int ok = 1;
