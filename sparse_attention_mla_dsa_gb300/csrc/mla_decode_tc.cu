@@ -373,6 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int32_t* bt = p.rows.block_table + static_cast<int64_t>(r) * p.rows.bt_stride;
     const int bs = p.rows.block_size;
+    // All table lookups in flight before any is used (one round trip).
+    int phys[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int t = idx[i];
+      const int blk = t >= 0 && t < len ? t / bs : -1;
+      phys[i] = (blk >= 0 && blk < p.rows.max_blocks_per_seq) ? __ldg(bt + blk) : -1;
+    }
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int e = tid + i * kThreads;
@@ -383,10 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < 0 || t >= len) {
           if (report) record_error(p.err, DSA_DEVERR_SELECT, r);
         } else {
-          const int blk = t / bs;
-          const int phys = blk < p.rows.max_blocks_per_seq ? __ldg(bt + blk) : -1;
-          const int64_t s = static_cast<int64_t>(phys) * bs + t % bs;
-          if (phys < 0 || s >= p.nslots) {
+          const int64_t s = static_cast<int64_t>(phys[i]) * bs + t % bs;
+          if (phys[i] < 0 || s >= p.nslots) {
             if (report) record_error(p.err, DSA_DEVERR_BLOCK, r);
           } else {
             slot = static_cast<int32_t>(s);
@@ -700,38 +706,70 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
   grid_dep_wait();  // the partials come from the kernel before
   grid_dep_launch();
   float mmax = -INFINITY;
-  for (int c = 0; c < nsplit; ++c) mmax = fmaxf(mmax, ld_dep_f2(ml + (base + c) * kHeads + hl).x);
   float lsum = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  if (mmax != -INFINITY) {
-    int c = 0;
-    for (; c + 8 <= nsplit; c += 8) {  // eight splits' loads in flight at a time
-      float2 mlc[8];
-      float4 vc[8];
+  if (nsplit <= 8) {
+    // Every split's (max, sum) and partial row in flight at once: one round trip.
+    float2 mlc[8];
+    float4 vc[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        mlc[u] = ld_dep_f2(ml + (base + c + u) * kHeads + hl);
-        vc[u] = ld_dep_f4(reinterpret_cast<const float4*>(p.part_o + ((base + c + u) * kHeads + hl) * 512) + tid);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float f = exp2f(mlc[u].x - mmax);
-        lsum += mlc[u].y * f;
-        acc.x += vc[u].x * f;
-        acc.y += vc[u].y * f;
-        acc.z += vc[u].z * f;
-        acc.w += vc[u].w * f;
+    for (int u = 0; u < 8; ++u) {
+      if (u < nsplit) {
+        mlc[u] = ld_dep_f2(ml + (base + u) * kHeads + hl);
+        vc[u] = ld_dep_f4(reinterpret_cast<const float4*>(p.part_o + ((base + u) * kHeads + hl) * 512) + tid);
+      } else {
+        mlc[u] = make_float2(-INFINITY, 0.0f);
+        vc[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
     }
-    for (; c < nsplit; ++c) {
-      const float2 mlc = ld_dep_f2(ml + (base + c) * kHeads + hl);
-      const float4 v = ld_dep_f4(reinterpret_cast<const float4*>(p.part_o + ((base + c) * kHeads + hl) * 512) + tid);
-      const float f = exp2f(mlc.x - mmax);
-      lsum += mlc.y * f;
-      acc.x += v.x * f;
-      acc.y += v.y * f;
-      acc.z += v.z * f;
-      acc.w += v.w * f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mmax = fmaxf(mmax, mlc[u].x);
+    if (mmax != -INFINITY) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (u < nsplit) {
+          const float f = exp2f(mlc[u].x - mmax);
+          lsum += mlc[u].y * f;
+          acc.x += vc[u].x * f;
+          acc.y += vc[u].y * f;
+          acc.z += vc[u].z * f;
+          acc.w += vc[u].w * f;
+        }
+      }
+    }
+  } else {
+    // Maxima first (eight loads in flight per round), then the rows.
+    for (int c0 = 0; c0 < nsplit; c0 += 8) {
+      float m8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        m8[u] = c0 + u < nsplit ? ld_dep_f2(ml + (base + c0 + u) * kHeads + hl).x : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mmax = fmaxf(mmax, m8[u]);
+    }
+    if (mmax != -INFINITY) {
+      for (int c0 = 0; c0 < nsplit; c0 += 8) {
+        float2 mlc[8];
+        float4 vc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (c0 + u < nsplit) {
+            mlc[u] = ld_dep_f2(ml + (base + c0 + u) * kHeads + hl);
+            vc[u] = ld_dep_f4(reinterpret_cast<const float4*>(p.part_o + ((base + c0 + u) * kHeads + hl) * 512) + tid);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (c0 + u < nsplit) {
+            const float f = exp2f(mlc[u].x - mmax);
+            lsum += mlc[u].y * f;
+            acc.x += vc[u].x * f;
+            acc.y += vc[u].y * f;
+            acc.z += vc[u].z * f;
+            acc.w += vc[u].w * f;
+          }
+        }
+      }
     }
   }
   const float scale = (mmax != -INFINITY && lsum > 0.0f) ? p.kv_scale / lsum : 0.0f;
