@@ -409,17 +409,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
+  // ---- the first two tiles (both ring stages are free) are gathered by every
+  // warp but the MMA warp: the softmax warps have nothing to do before the
+  // first S is ready, and each warp issues its copies one after another.
+  // Copy g of the pair is issued by warp g % 11, lane g / 11 (tile 0's copies
+  // come first in every warp).
+  const int first = min(ntiles, 2);
+  if (warp != kMmaWarp) {
+    constexpr int kIssuerWarps = kThreads / 32 - 1;
+    const int widx = warp < kMmaWarp ? warp : warp - 1;
+    if (widx == 0 && lane == 0)
+      for (int t = 0; t < first; ++t) mbar_arrive_expect_tx(&ctl->full[t], kTileBytes);
+    for (int g = widx + kIssuerWarps * lane; g < first * 128; g += kIssuerWarps * 32) {
+      const int t = g >> 7, gg = g & 127;
+      const int rg = gg >> 2, sb = gg & 3;
+      const int32_t* sl = ctl->slot + t * kTok + 4 * rg;
+      tma_gather4(smem_u32(tiles + t * kTileBytes + sb * kSub + rg * 512), &pmap, &ctl->full[t],
+                  sb * 128, sl[0], sl[1], sl[2], sl[3]);
+    }
+  }
+
   if (warp < kProducerWarps) {
     // ================================================================ gather
-    // Copy g (0..127) of a tile moves rows 4(g/4) .. 4(g/4)+3 of the tile,
-    // column block g%4; producer warp w issues copies w, w+3, w+6, ... (43,
-    // 43 and 42 of them), lane l the ones with index w + 3(l + 32j).  Warp 0
-    // lane 0 posts the tile's byte count; other copies may land before it
-    // does (the transaction count may run ahead of the expectation).
-    int issued = 0;
-    for (int t = 0; t < ntiles; ++t) {
+    // Tiles from the third on.  Copy g (0..127) of a tile moves rows
+    // 4(g/4) .. 4(g/4)+3 of the tile, column block g%4; producer warp w
+    // issues copies w, w+3, w+6, ... (43, 43 and 42 of them), lane l the ones
+    // with index w + 3(l + 32j).  Warp 0 lane 0 posts the tile's byte count;
+    // other copies may land before it does (the transaction count may run
+    // ahead of the expectation).
+    int issued = first;
+    for (int t = first; t < ntiles; ++t) {
       const int s = t & 1;
-      if (t >= 2 && !warp_wait(ctl, &ctl->empty[s], ((t - 2) >> 1) & 1, lane, p.err, r)) break;
+      if (!warp_wait(ctl, &ctl->empty[s], ((t - 2) >> 1) & 1, lane, p.err, r)) break;
       if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&ctl->full[s], kTileBytes);
       for (int g = warp + kProducerWarps * lane; g < 128; g += kProducerWarps * 32) {
         const int rg = g >> 2, sb = g & 3;
