@@ -163,32 +163,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   {
     const float* qsrc = p.q_idx + static_cast<int64_t>(r0) * p.heads * D;
     const int vec_per_row = D / 8;
-    for (int v = threadIdx.x; v < npad * vec_per_row; v += kThreads) {
-      const int n = v / vec_per_row, c8 = v % vec_per_row;
-      float x[8];
-      if (n < nreal) {
-        const float4* src = reinterpret_cast<const float4*>(qsrc + static_cast<int64_t>(n) * D + c8 * 8);
-        const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
-        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
-        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
-      } else {
+    const int nvec = npad * vec_per_row;
+    // Up to eight 8-float vectors per thread are loaded before any is used,
+    // so the operand costs one round trip per eight vectors, not per vector.
+    constexpr int kBatch = 8;
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += kBatch * kThreads) {
+      float4 u[kBatch][2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = 0.0f;
+      for (int k = 0; k < kBatch; ++k) {
+        const int v = v0 + k * kThreads;
+        const int n = v / vec_per_row, c8 = v % vec_per_row;
+        if (v < nvec && n < nreal) {
+          const float4* src = reinterpret_cast<const float4*>(qsrc + static_cast<int64_t>(n) * D + c8 * 8);
+          u[k][0] = __ldg(src);
+          u[k][1] = __ldg(src + 1);
+        } else {
+          u[k][0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          u[k][1] = u[k][0];
+        }
       }
-      uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(x[2 * i]);
-        const __nv_bfloat16 h1 = __float2bfloat16_rn(x[2 * i + 1]);
-        const float r0f = x[2 * i] - __bfloat162float(h0);
-        const float r1f = x[2 * i + 1] - __bfloat162float(h1);
-        hi[i] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-        lo[i] = pack_bf16x2(r0f, r1f);
+      for (int k = 0; k < kBatch; ++k) {
+        const int v = v0 + k * kThreads;
+        if (v >= nvec) break;
+        const int n = v / vec_per_row, c8 = v % vec_per_row;
+        const float x[8] = {u[k][0].x, u[k][0].y, u[k][0].z, u[k][0].w,
+                            u[k][1].x, u[k][1].y, u[k][1].z, u[k][1].w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(x[2 * i]);
+          const __nv_bfloat16 h1 = __float2bfloat16_rn(x[2 * i + 1]);
+          const float r0f = x[2 * i] - __bfloat162float(h0);
+          const float r1f = x[2 * i + 1] - __bfloat162float(h1);
+          hi[i] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
+          lo[i] = pack_bf16x2(r0f, r1f);
+        }
+        const int sb = (c8 * 8) / 64, chunk = c8 & 7;
+        const uint32_t off = sb * (npad * 128) + n * 128 + ((chunk ^ (n & 7)) * 16);
+        *reinterpret_cast<uint4*>(b_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(b_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      const int sb = (c8 * 8) / 64, chunk = c8 & 7;
-      const uint32_t off = sb * (npad * 128) + n * 128 + ((chunk ^ (n & 7)) * 16);
-      *reinterpret_cast<uint4*>(b_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(b_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     for (int n = threadIdx.x; n < npad; n += kThreads)
       w_s[n] = n < nreal ? __ldg(p.head_w + static_cast<int64_t>(r0) * p.heads + n) : 0.0f;
