@@ -319,7 +319,9 @@ def run_ours(args):
         torch.cuda.empty_cache()
         dec = path.DsaDecoder(wl, dev, replicas=n_rep)
         dec.stage(wl)
-        for i in range(max(3, args.warmup)):
+        # Every replica's step graph is captured on its first use: warm up over
+        # all of them so that no capture falls inside the timed steps.
+        for i in range(max(3, args.warmup, n_rep)):
             dec.decode()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -117,13 +117,20 @@ class DsaDecoder:
     """Host-facing decode: resident caches, per-step host inputs and outputs.
 
     The caches (key arena, gate, FP8 latent pool) live on the device; each
-    ``decode`` call stages the step's inputs in pinned host buffers, copies
-    them to the device, runs S0-S3 and copies the attention output back."""
+    ``decode`` call copies the step's inputs from pinned host buffers to the
+    device, runs S0-S3 and copies the attention output back.  With
+    ``graphs=True`` (the default) that whole sequence -- the host-to-device
+    copies, the four calls and the device-to-host copy -- is captured once per
+    cache replica as a CUDA graph and replayed, so a step costs one launch; the
+    pinned buffers and device tensors keep their addresses, so each replay
+    moves the current contents of the pinned inputs."""
 
-    def __init__(self, wl, device: str | torch.device = "cuda", replicas: int = 1):
+    def __init__(self, wl, device: str | torch.device = "cuda", replicas: int = 1,
+                 graphs: bool = True):
         first = DeviceWorkload(wl, device)
         self.replicas = [first] + [first.clone() for _ in range(replicas - 1)]
         self._next = 0
+        self._graphs = [None] * len(self.replicas) if graphs else None
         dw = first
         self._host_in = {}
         for name in ("q_idx", "head_w", "Q", "seq_lens", "positions", "slots", "block_table",
@@ -151,14 +158,29 @@ class DsaDecoder:
         for k, t in self._host_in.items():
             t.copy_(torch.from_numpy(np.ascontiguousarray(src[k])))
 
-    def decode(self, stream=None) -> torch.Tensor:
-        """Copy staged inputs in, run the path, copy the output out (async on
-        the stream; synchronise before reading ``host_out``).  Successive
-        calls rotate over the resident cache replicas."""
-        dw = self.replicas[self._next]
-        self._next = (self._next + 1) % len(self.replicas)
+    def _run(self, dw, stream=None) -> None:
         for k, t in self._host_in.items():
             getattr(dw, k).copy_(t, non_blocking=True)
         dw.step(stream)
         self.host_out.copy_(dw.out, non_blocking=True)
+
+    def decode(self, stream=None) -> torch.Tensor:
+        """Copy staged inputs in, run the path, copy the output out (async on
+        the current stream; synchronise before reading ``host_out``).
+        Successive calls rotate over the resident cache replicas."""
+        i = self._next
+        dw = self.replicas[i]
+        self._next = (self._next + 1) % len(self.replicas)
+        if self._graphs is None:
+            self._run(dw, stream)
+            return self.host_out
+        if self._graphs[i] is None:
+            self._run(dw, stream)              # first use of this replica runs eagerly
+            torch.cuda.current_stream().synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._run(dw)
+            self._graphs[i] = g
+            return self.host_out
+        self._graphs[i].replay()
         return self.host_out
