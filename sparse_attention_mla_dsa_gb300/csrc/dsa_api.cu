@@ -142,10 +142,13 @@ dsa_status dsa_index_scores(const dsa_rows* rows, const float* q_idx, const floa
   p.idx_tokens = idx_tokens;
   p.rows = rows->rows;
   p.rows_per_seq = rows_per_seq;
-  // Rows of one sequence share each key tile as long as their heads fit one
-  // MMA N (<= 256); a head count that is not a multiple of 16 runs one row
-  // per launch group so that no 16-column TMEM load straddles two rows.
-  int sub = 256 / index_heads;
+  // Rows of one sequence share each key tile in groups of at most 64 score
+  // columns (a wider group makes the per-token epilogue, not HBM, the limit,
+  // and its q operand leaves room for one CTA per SM; the groups of a
+  // sequence run side by side and share the key tiles through L2); a head
+  // count that is not a multiple of 16 runs one row per launch group so that
+  // no 16-column TMEM load straddles two rows.
+  int sub = 64 / index_heads;
   if (index_heads % 16 != 0) sub = 1;
   sub = sub < 1 ? 1 : (sub > 32 ? 32 : sub);
   if (sub > rows_per_seq) sub = rows_per_seq;

@@ -18,8 +18,10 @@
 //
 // CTA roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues the
 // MMAs (one thread), warps 2-5 are the epilogue (one TMEM lane quarter each).
-// A CTA handles `chunk_tiles` consecutive 128-token tiles of one launch group;
-// the grid is (chunks, launch groups) and CTAs past a group's length exit.
+// A CTA handles `chunk_tiles` consecutive 128-token tiles of one launch group
+// (at most 64 score columns: rows of a sequence beyond that form further
+// groups); the grid is (sub-group, chunk, sequence) and CTAs past a group's
+// length exit.
 // The arithmetic of every score is the same whichever CTA, chunk or launch
 // group computes it, so a row's scores do not depend on the other rows.
 #include "dsa_device.cuh"
@@ -82,8 +84,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   IndexCtl* ctl = reinterpret_cast<IndexCtl*>(w_s + npad);
 
   // ---------------------------------------------------------------- launch group
-  const int lg = blockIdx.y;
-  const int seq = lg / p.subs_per_seq, sub = lg % p.subs_per_seq;
+  // Grid (sub-group, chunk, sequence): the sub-groups of a sequence are
+  // adjacent in launch order, so they stream the same key tiles together and
+  // all but the first read them from L2.
+  const int seq = blockIdx.z, sub = blockIdx.x;
   const int seq_row0 = seq * p.rows_per_seq;
   const int r0 = seq_row0 + sub * p.sub_rows;
   const int nrows = min(p.sub_rows, seq_row0 + p.rows_per_seq - r0);
@@ -91,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Row lengths and arena bases: one load per row, all rows in parallel.
   if (threadIdx.x < 32) {
-    const bool report = blockIdx.x == 0;
+    const bool report = blockIdx.y == 0;
     const int j = threadIdx.x;
     const int64_t base = __ldg(p.idx_base + seq_row0);
     int len = 0;
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   const int tiles = (ctl->max_len_group + kTileM - 1) / kTileM;
-  const int t_begin = blockIdx.x * p.chunk_tiles;
+  const int t_begin = blockIdx.y * p.chunk_tiles;
   const int t_end = min(t_begin + p.chunk_tiles, tiles);
   if (t_begin >= t_end) return;  // uniform across the CTA, before any barrier or TMEM use
   const int ntiles = t_end - t_begin;
@@ -376,8 +380,11 @@ cudaError_t launch_index_scores(const IndexParams& p, const CUtensorMap& kmap,
   const int64_t chunks = (tiles_max + p.chunk_tiles - 1) / p.chunk_tiles;
   const int64_t groups = static_cast<int64_t>(p.rows / p.rows_per_seq) * p.subs_per_seq;
   if (chunks <= 0 || groups <= 0) return cudaSuccess;
-  if (chunks > 0x7FFFFFFF || groups > 65535) return cudaErrorInvalidConfiguration;
-  dim3 grid(static_cast<unsigned>(chunks), static_cast<unsigned>(groups));
+  const int64_t seqs = p.rows / p.rows_per_seq;
+  if (chunks > 65535 || seqs > 65535 || p.subs_per_seq > 65535)
+    return cudaErrorInvalidConfiguration;
+  dim3 grid(static_cast<unsigned>(p.subs_per_seq), static_cast<unsigned>(chunks),
+            static_cast<unsigned>(seqs));
   cudaError_t e;
   auto kernel = p.dim == 64 ? index_scores_kernel<64> : index_scores_kernel<128>;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
