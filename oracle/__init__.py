@@ -15,6 +15,9 @@ follows on the pages:
   (one gather-attend over all rows), the selection notes (total order score
   DESC, index ASC) and ``bt_entries_needed``.
 * "Struct Glm5NextDsaLayer" rustdoc page -- ``kv_scale`` (write takes 1/scale).
+* "glm5next_dsa/layer.rs" -- the ``gemm`` helper (C[M, N] = A[M, K] @ B[N, K]^T)
+  and the ``decode_k`` notes on the batched projections of the K-token verify
+  (``dense_mm``).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, brute force, exhaustive code tables, library routines) and by
@@ -79,6 +82,8 @@ def _load():
             lib.dsa_oracle_dense_mla_row.restype = i32
             lib.dsa_oracle_bt_entries_needed.argtypes = [i64, i64, i64]
             lib.dsa_oracle_bt_entries_needed.restype = i64
+            lib.dsa_oracle_dense_mm_row.argtypes = [i32, i32, P, P, P, P]
+            lib.dsa_oracle_dense_mm_row.restype = None
             _lib = lib
     return _lib
 
@@ -217,6 +222,29 @@ def bt_entries_needed(seq_len: int, k: int, block_size: int) -> int:
 
 
 # --------------------------------------------------------------------------- whole path
+def dense_mm(a: np.ndarray, b: np.ndarray):
+    """Batched projection c[m][n] = sum_k a[m][k] * b[n][k] (a: [M, K] bf16 bits,
+    b: [N, K] bf16 bits), one row of ``a`` at a time; returns (c, mag) in float64,
+    mag[m][n] = sum_k |a[m][k] * b[n][k]|.  ("glm5next_dsa/layer.rs", the gemm
+    helper and the decode_k notes on the batched projections.)"""
+    a = _c(a, np.uint16)
+    b = _c(b, np.uint16)
+    M, K = a.shape
+    N, K2 = b.shape
+    assert K == K2
+    c = np.zeros((M, N), np.float64)
+    mag = np.zeros((M, N), np.float64)
+    lib = _load()
+    for m in range(M):
+        row = np.ascontiguousarray(a[m])
+        cm = np.zeros(N, np.float64)
+        gm = np.zeros(N, np.float64)
+        lib.dsa_oracle_dense_mm_row(N, K, _ptr(row), _ptr(b), _ptr(cm), _ptr(gm))
+        c[m] = cm
+        mag[m] = gm
+    return c, mag
+
+
 def run_path_rows(wl, rows=None, threads: int = 1, sel_from=None):
     """Run S1 -> S2 -> S3 of the oracle for the given rows of a workload.
 

@@ -335,3 +335,28 @@ int64_t dsa_oracle_bt_entries_needed(int64_t seq_len, int64_t k, int64_t block_s
     int64_t bs = block_size > 0 ? block_size : 1;
     return (seq_len + k) / bs + 2;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Batched projection (the K-token verify's weight sweep)                    */
+/* ------------------------------------------------------------------------ */
+
+/* "glm5next_dsa/layer.rs", the gemm helper (C[M, N] = A[M, K] @ B[N, K]^T)
+ * and the notes on decode_k / dense_gemv_bf16_batchm: K rows of one sequence
+ * multiply the same weight, each row exactly as a single-row call would.
+ * One row of A against every row of B, accumulated in double in k order. */
+void dsa_oracle_dense_mm_row(int n, int k, const uint16_t *a_row, const uint16_t *b,
+                             double *c, double *mag)
+{
+    for (int j = 0; j < n; ++j) {
+        double acc = 0.0, m = 0.0;
+        for (int i = 0; i < k; ++i) {
+            double prod = dsa_oracle_bf16_value(a_row[i]) *
+                          dsa_oracle_bf16_value(b[(int64_t)j * k + i]);
+            acc += prod;
+            m += fabs(prod);
+        }
+        c[j] = acc;
+        if (mag)
+            mag[j] = m;
+    }
+}

@@ -108,6 +108,13 @@ int dsa_oracle_dense_mla_row(int heads, int dim, const uint16_t *Q,
  * A block size of 0 is treated as 1. */
 int64_t dsa_oracle_bt_entries_needed(int64_t seq_len, int64_t k, int64_t block_size);
 
+/* Batched projection, one row of A:
+ *   c[j]   = sum_i a_row[i] * b[j][i]       (a_row: [k] bf16, b: [n][k] bf16)
+ *   mag[j] = sum_i |a_row[i] * b[j][i]|     (optional; scale for tolerances)
+ * in double, i ascending. */
+void dsa_oracle_dense_mm_row(int n, int k, const uint16_t *a_row, const uint16_t *b,
+                             double *c, double *mag);
+
 #ifdef __cplusplus
 }
 #endif

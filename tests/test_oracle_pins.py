@@ -357,3 +357,73 @@ def test_bt_entries_cover_every_indexable_position(oracle):
         n = oracle.bt_entries_needed(seq_len, k, bs)
         highest = max(seq_len + k - 1, 0) // bs
         assert highest < n
+
+
+# ----------------------------------------------------------------------------- batched projection
+def test_dense_mm_brute_force_integers(oracle):
+    # Small integers are exact in bf16 and in every partial sum: the product
+    # must be the integer matrix product written out with Python ints.
+    rng = np.random.default_rng(5)
+    M, N, K = 3, 5, 7
+    ai = rng.integers(-8, 9, size=(M, K))
+    bi = rng.integers(-8, 9, size=(N, K))
+    c, mag = oracle.dense_mm(_bf16(ai), _bf16(bi))
+    for m in range(M):
+        for n in range(N):
+            exact = 0
+            total = 0
+            for k in range(K):
+                exact += int(ai[m, k]) * int(bi[n, k])
+                total += abs(int(ai[m, k]) * int(bi[n, k]))
+            assert c[m, n] == exact and mag[m, n] == total
+
+
+def test_dense_mm_one_hot_rows_select_weight_columns(oracle):
+    # a[m] = e_{k_m}: row m of the result is column k_m of the weight, exactly.
+    # A transposed operand or a wrong index picks other entries.
+    rng = np.random.default_rng(6)
+    M, N, K = 4, 9, 16
+    b = _bf16(rng.standard_normal((N, K)))
+    picks = [0, 5, 15, 7]
+    a = np.zeros((M, K), np.uint16)
+    for m, k in enumerate(picks):
+        a[m, k] = 0x3F80  # 1.0
+    c, _ = oracle.dense_mm(a, b)
+    for m, k in enumerate(picks):
+        want = np.array([oracle.bf16_value(int(b[n, k])) for n in range(N)])
+        assert np.array_equal(c[m], want)
+
+
+def test_dense_mm_power_of_two_scaling_and_transpose(oracle):
+    rng = np.random.default_rng(7)
+    M, N, K = 3, 4, 33
+    a = _bf16(rng.standard_normal((M, K)))
+    b = _bf16(rng.standard_normal((N, K)))
+    c, _ = oracle.dense_mm(a, b)
+    # Doubling row 1 of a (exponent + 1) doubles row 1 of c exactly and leaves
+    # the other rows alone: rows are independent.
+    a2 = a.copy()
+    a2[1] = (a2[1].astype(np.uint32) + 0x80).astype(np.uint16)
+    c2, _ = oracle.dense_mm(a2, b)
+    assert np.array_equal(c2[1], 2.0 * c[1])
+    assert np.array_equal(c2[[0, 2]], c[[0, 2]])
+    # Swapping the operands transposes the result (same k order, products commute).
+    ct, _ = oracle.dense_mm(b, a)
+    assert np.array_equal(ct, c.T)
+
+
+def test_planted_dense_mm_mistakes_are_caught(oracle):
+    # A dropped last term, or a weight read transposed, fails the one-hot pin.
+    rng = np.random.default_rng(8)
+    N, K = 6, 8
+    b = _bf16(rng.standard_normal((N, K)))
+    a = np.zeros((1, K), np.uint16)
+    a[0, K - 1] = 0x3F80
+    c, _ = oracle.dense_mm(a, b)
+    want = np.array([oracle.bf16_value(int(b[n, K - 1])) for n in range(N)])
+    dropped, _ = oracle.dense_mm(a[:, :K - 1], b[:, :K - 1])
+    assert np.array_equal(c[0], want) and not np.array_equal(dropped[0], want)
+    sq = _bf16(rng.standard_normal((K, K)))
+    cs, _ = oracle.dense_mm(a, sq)
+    cst, _ = oracle.dense_mm(a, np.ascontiguousarray(sq.T))
+    assert not np.array_equal(cs, cst)
