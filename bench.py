@@ -11,6 +11,7 @@ HBM.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference     # the FP64 CPU oracle on the host cores
+  python bench.py --workload proj_verify   # the K-token verify's batched projections
 
 Under torchrun each rank runs its own copy of the workload on its own GPU
 (weak scaling, no data exchange); timing is the max over ranks.
@@ -43,7 +44,11 @@ DESCRIPTIONS = {
               "index 32x128, topk 2048",
     "long": "long-context batch: 64 seqs x 1 row, len log-U[4096,131072], 128 heads, index 64x128, "
             "topk 2048, latent write of the new row",
+    "proj_verify": "K-token verify projections: 4 rows x (q_a 1536x4096, absorbed q_b 32768x1536, "
+                   "kv_a 512x4096, absorbed o 4096x32768) bf16, one weight sweep per step",
 }
+PROJ_METRIC = ("K-token verify projection rows/s (q_a, absorbed q_b, kv_a, absorbed o of one layer, "
+               "64 heads; one bf16 weight sweep per step); % HBM roofline")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
@@ -365,6 +370,226 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# --------------------------------------------------------------------------- projections
+def _proj_oracle_rows_per_s(pw, rows, threads):
+    """The oracle's batched projection, every projection of the set, for the
+    given activation rows (one task per row and projection)."""
+    import numpy as np
+    import oracle
+    tasks = [(j, r) for r in rows for j in range(len(pw.shapes))]
+
+    def one(t):
+        j, r = t
+        oracle.dense_mm(np.ascontiguousarray(pw.acts[j][r:r + 1]), pw.weights[j])
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, tasks))
+    return len(rows) / (time.perf_counter() - t0)
+
+
+def run_projections(args):
+    """One step = one layer's four projections for the 4 rows of a K-token
+    verify, each weight swept once (dsa_dense_mm_bf16, bf16 out)."""
+    import torch
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import __graft_entry__
+    from sparse_attention_mla_dsa_gb300 import build as _b
+    if rank == 0 and _b.is_stale():
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from sparse_attention_mla_dsa_gb300 import api, shard, workloads
+    api.load()
+    pw = workloads.make_projections()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    wbytes = pw.weight_bytes()
+    alg = pw.algorithmic_bytes()
+    n_rep = max(2, math.ceil(2.0 * l2 / wbytes) + 1)
+    names = [nm for nm, _, _ in pw.shapes]
+
+    def dev16(a):
+        return torch.from_numpy(a.view("int16")).to(dev)
+
+    weights = [dev16(w) for w in pw.weights]
+    reps = []
+    for i in range(n_rep):
+        ws = weights if i == 0 else [w.clone() for w in weights]
+        acts = [dev16(a) for a in pw.acts]
+        outs = [torch.empty((pw.rows, n), dtype=torch.int16, device=dev) for _, n, _ in pw.shapes]
+        wsp = [torch.empty(max(256, api.dsa_dense_mm_workspace_bytes(n, k)), dtype=torch.uint8,
+                           device=dev) for _, n, k in pw.shapes]
+        reps.append((ws, acts, outs, wsp))
+
+    def one_step(rep, evs=None):
+        ws, acts, outs, wsp = rep
+        s = torch.cuda.current_stream()
+        if evs is not None:
+            evs[0].record(s)
+        for j in range(len(ws)):
+            api.dsa_dense_mm_bf16(acts[j], ws[j], outs[j], wsp[j])
+            if evs is not None:
+                evs[j + 1].record(s)
+
+    for i in range(max(3, args.warmup)):
+        one_step(reps[i % n_rep])
+    torch.cuda.synchronize()
+    code, row, _ = api.dsa_get_error(reset=True)
+    if code != 0:
+        raise RuntimeError(f"device error during warm-up: {api.DEVERR.get(code)} ({row})")
+    graphs, staged = [], []
+    for rep in reps:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            one_step(rep)
+        graphs.append(g)
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
+        gs = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gs):
+            one_step(rep, evs)
+        staged.append((gs, evs))
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(K):
+            graphs[i % n_rep].replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+        for i in range(K):
+            staged[i % n_rep][0].replay()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = shard.max_over_ranks(start.elapsed_time(end))
+    ev_sets = [evs for _, evs in staged[:min(K, n_rep)]]
+    stage_ms = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev_sets)
+                for j, nm in enumerate(names)}
+    code, row, _ = api.dsa_get_error(reset=True)
+    if code != 0:
+        raise RuntimeError(f"device error during the timed steps: {api.DEVERR.get(code)} ({row})")
+
+    value = K * pw.rows * world / (elapsed_ms / 1e3)
+    peak, peak_kind = _peaks()
+    stage_bytes = {nm: n * k * 2 + pw.rows * (n + k) * 2 for nm, n, k in pw.shapes}
+    dominant = max(names, key=lambda nm: stage_ms[nm])
+    ach = stage_bytes[dominant] / (stage_ms[dominant] / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
+                "traffic": _traffic(args.workload, dominant), "algorithmic_bytes": stage_bytes[dominant],
+                "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+                "path_frac": round(alg / (elapsed_ms / K / 1e3) / 1e9 / peak, 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        # Host-facing: the step's activations from pinned host memory, the four
+        # projections, the outputs back to pinned host memory, one graph per replica.
+        h_in = [torch.from_numpy(a.view("int16")).pin_memory() for a in pw.acts]
+        h_out = [torch.empty((pw.rows, n), dtype=torch.int16).pin_memory() for _, n, _ in pw.shapes]
+
+        def host_step(rep):
+            ws, acts, outs, wsp = rep
+            for j in range(len(ws)):
+                acts[j].copy_(h_in[j], non_blocking=True)
+            one_step(rep)
+            for j in range(len(ws)):
+                h_out[j].copy_(outs[j], non_blocking=True)
+
+        hgraphs = []
+        for rep in reps:
+            host_step(rep)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                host_step(rep)
+            hgraphs.append(g)
+        for g in hgraphs:
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            hgraphs[i % n_rep].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = shard.max_over_ranks(e0.elapsed_time(e1))
+        e2e = {"value": round(K * pw.rows * world / (ems / 1e3), 2), "unit": UNIT,
+               "h2d_bytes_per_step": sum(t.numel() * 2 for t in h_in),
+               "d2h_bytes_per_step": sum(t.numel() * 2 for t in h_out)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cores = os.cpu_count() or 1
+        v = _proj_oracle_rows_per_s(pw, list(range(pw.rows)), cores)
+        cpu = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{pw.rows} rows x the four projections, one (row, projection) per "
+                         f"task over {cores} threads"}
+    launches = sum(1 + (1 if api.dsa_dense_mm_workspace_bytes(n, k) > 0 else 0)
+                   for _, n, k in pw.shapes)
+    line = {
+        "metric": PROJ_METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": pw.rows,
+                   "algorithmic_bytes_per_step": alg,
+                   "l2": f"rotating {n_rep} weight replicas ({n_rep * wbytes / 1e6:.0f} MB per "
+                         f"rotation, L2 {l2 / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "launch": "cuda-graph"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": K * launches, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_projections_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from sparse_attention_mla_dsa_gb300 import workloads
+    import oracle
+    oracle.build()
+    pw = workloads.make_projections()
+    cores = os.cpu_count() or 1
+    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(K):
+        _proj_oracle_rows_per_s(pw, list(range(pw.rows)), cores)
+    el = time.perf_counter() - t0
+    value = K * pw.rows / el
+    sample = f"{K} steps x {pw.rows} rows x the four projections over {cores} threads"
+    line = {"impl": "reference", "metric": PROJ_METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(el / K * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": pw.rows},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------------------- oracle (CPU)
 def _oracle_rows_per_s(wl, rows, threads):
     import oracle
@@ -426,7 +651,12 @@ def main():
     if args.impl == "reference":
         if args.steps > 20:
             args.steps = 20     # the oracle is slow; keep the run within minutes
-        run_reference(args)
+        if args.workload == "proj_verify":
+            run_projections_reference(args)
+        else:
+            run_reference(args)
+    elif args.workload == "proj_verify":
+        run_projections(args)
     else:
         run_ours(args)
 

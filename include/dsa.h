@@ -217,6 +217,36 @@ size_t dsa_noalloc_scratch_bytes(int32_t rows, int32_t heads, int32_t topk);
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 
 /*
+ * Batched projection for the K-token verify: the K rows of one sequence sweep
+ * a BF16 weight once ("glm5next_dsa/layer.rs": the gemm helper,
+ * C[M, N] = A[M, K] @ B[N, K]^T, and the decode_k notes on
+ * dense_gemv_bf16_batchm -- one weight read for 2..16 rows, each row
+ * bit-identical to a single-row call).
+ *   c[m][n] = sum_k a[m][k] * b[n][k]          m < m_rows, n < n_out
+ *   a [m_rows][k] bf16, row-major (k contiguous), 16-byte aligned
+ *   b [n_out][k]  bf16 weight, row-major, 16-byte aligned
+ *   c [m_rows][n_out] bf16 (c_fp32 = 0, round to nearest even) or fp32
+ *     (c_fp32 = 1), 4-byte aligned
+ * m_rows in [1, 16] (DSA_ERR_UNSUPPORTED above); k >= 8 and a multiple of 8
+ * (16-byte row strides); n_out >= 1; DSA_ERR_INVALID_ARG otherwise.
+ * Numerics: the bf16 products are exact and accumulate in FP32 on the tensor
+ * cores in 64-element blocks of k, in order; when the weight has few rows the
+ * k range is split (the split depends only on n_out, k and the device's SM
+ * count) and the FP32 partial sums are added in order.  A row's result is a
+ * function of that row of a and of b only: bit-identical whatever m_rows is
+ * and whatever the other rows hold.  The split partials pass through the
+ * caller's workspace of dsa_dense_mm_workspace_bytes(n_out, k) bytes (0: none
+ * needed), 256-byte aligned (DSA_ERR_WORKSPACE otherwise).
+ */
+dsa_status dsa_dense_mm_bf16(const uint16_t *a, const uint16_t *b, void *c, int32_t m_rows,
+                             int32_t n_out, int32_t k, int32_t c_fp32, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/* Workspace bytes dsa_dense_mm_bf16 needs on the current device for a weight
+ * of n_out x k (0 when it needs none or on bad arguments). */
+size_t dsa_dense_mm_workspace_bytes(int32_t n_out, int32_t k);
+
+/*
  * Read the sticky device error word of the current device: *code_out is the
  * first DSA_DEVERR_* recorded since the last reset (0 if none), *row_out the
  * row it concerned and *count_out how many errors were recorded.  Any out

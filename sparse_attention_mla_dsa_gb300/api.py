@@ -61,6 +61,7 @@ def load() -> ctypes.CDLL:
         "dsa_mla_decode_fp8": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, sz, P],
         "dsa_mla_decode_fp8_noalloc": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P],
         "dsa_get_error": [P, P, P, i32],
+        "dsa_dense_mm_bf16": [P, P, P, i32, i32, i32, i32, P, sz, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -70,6 +71,8 @@ def load() -> ctypes.CDLL:
     lib.dsa_workspace_bytes.restype = sz
     lib.dsa_noalloc_scratch_bytes.argtypes = [i32, i32, i32]
     lib.dsa_noalloc_scratch_bytes.restype = sz
+    lib.dsa_dense_mm_workspace_bytes.argtypes = [i32, i32]
+    lib.dsa_dense_mm_workspace_bytes.restype = sz
     lib.dsa_bt_entries_needed.argtypes = [i64, i64, i64]
     lib.dsa_bt_entries_needed.restype = i64
     lib.dsa_status_string.argtypes = [ctypes.c_int]
@@ -195,6 +198,30 @@ def dsa_mla_decode_fp8_noalloc(rows: Rows, q: torch.Tensor, pool: torch.Tensor, 
                                         _ptr(out, torch.uint16, "out"), _ptr(lse, torch.float32, "lse"),
                                         _stream(stream))
     _check("dsa_mla_decode_fp8_noalloc", st)
+
+
+def dsa_dense_mm_bf16(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor,
+                      workspace: torch.Tensor | None = None, stream=None) -> None:
+    """c[m][n] = sum_k a[m][k] * b[n][k]: a [M, K] bf16 (M <= 16), weight b [N, K]
+    bf16, c [M, N] bf16 or float32 (the output type picks the variant)."""
+    lib = load()
+    if c.dtype == torch.float32:
+        c_fp32, cp = 1, _ptr(c, torch.float32, "c")
+    else:
+        c_fp32, cp = 0, _ptr(c, torch.uint16, "c")
+    m, k = a.shape
+    n = b.shape[0]
+    if b.shape[1] != k or tuple(c.shape) != (m, n):
+        raise ValueError(f"shapes a {tuple(a.shape)}, b {tuple(b.shape)}, c {tuple(c.shape)}")
+    st = lib.dsa_dense_mm_bf16(_ptr(a, torch.uint16, "a"), _ptr(b, torch.uint16, "b"), cp, m, n, k,
+                               c_fp32, _ptr(workspace, None, "workspace"),
+                               0 if workspace is None else workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    _check("dsa_dense_mm_bf16", st)
+
+
+def dsa_dense_mm_workspace_bytes(n: int, k: int) -> int:
+    return int(load().dsa_dense_mm_workspace_bytes(int(n), int(k)))
 
 
 def dsa_workspace_bytes(rows: int, heads: int, topk: int) -> int:

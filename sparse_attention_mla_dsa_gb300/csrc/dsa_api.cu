@@ -256,6 +256,66 @@ size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
   return mla_decode_tc_workspace_bytes(rows, heads, topk);
 }
 
+size_t dsa_dense_mm_workspace_bytes(int32_t n_out, int32_t k) {
+  if (n_out < 1 || k < 8 || k % 8 != 0) return 0;
+  const DeviceInfo* dev = device_info();
+  if (dev == nullptr) return 0;
+  return dense_mm_workspace_bytes(n_out, k, dev->num_sms);
+}
+
+dsa_status dsa_dense_mm_bf16(const uint16_t* a, const uint16_t* b, void* c, int32_t m_rows,
+                             int32_t n_out, int32_t k, int32_t c_fp32, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (a == nullptr || b == nullptr || c == nullptr) return DSA_ERR_INVALID_ARG;
+  if (m_rows < 1 || n_out < 1 || k < 8 || k % 8 != 0) return DSA_ERR_INVALID_ARG;
+  if (m_rows > 16) return DSA_ERR_UNSUPPORTED;
+  if (c_fp32 != 0 && c_fp32 != 1) return DSA_ERR_INVALID_ARG;
+  if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c, 4)) return DSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = device_info();
+  if (dev == nullptr) return DSA_ERR_CUDA;
+  auto encode = encode_tiled();
+  if (encode == nullptr) return DSA_ERR_CUDA;
+
+  DenseMmParams p{};
+  p.a = a;
+  p.b = b;
+  p.c = c;
+  p.err = dev->err;
+  p.m = m_rows;
+  p.n = n_out;
+  p.k = k;
+  p.c_fp32 = c_fp32;
+  p.wait_ns = kDefaultWaitNs;
+  plan_dense_mm(p, dev->num_sms);
+  if (p.splits > 1) {
+    const size_t need = static_cast<size_t>(p.splits) * m_rows * static_cast<size_t>(n_out) * 4;
+    if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+      return DSA_ERR_WORKSPACE;
+    p.part = static_cast<float*>(workspace);
+  }
+
+  // Weight [n_out][k] and activations [m_rows][k], bf16, boxes of 64 of k
+  // (128 bytes, the swizzle span) by 128 weight rows / 16 activation rows;
+  // rows and columns past the tensors read as zero.
+  CUtensorMap wmap, amap;
+  cuuint64_t wdim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(n_out)};
+  cuuint64_t adim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m_rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k) * 2};
+  cuuint32_t wbox[2] = {64, 128};
+  cuuint32_t abox[2] = {64, 16};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult cr = encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(b), wdim,
+                       gstride, wbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return DSA_ERR_INVALID_ARG;
+  cr = encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a), adim, gstride,
+              abox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return DSA_ERR_INVALID_ARG;
+  return launched(launch_dense_mm(p, wmap, amap, static_cast<cudaStream_t>(stream)));
+}
+
 dsa_status dsa_get_error(int32_t* code_out, int32_t* row_out, int32_t* count_out, int32_t reset) {
   const DeviceInfo* dev = device_info();
   if (dev == nullptr) return DSA_ERR_CUDA;

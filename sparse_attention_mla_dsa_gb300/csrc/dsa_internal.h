@@ -81,6 +81,26 @@ int topk_cluster_size(int32_t max_len);
 size_t topk_smem_bytes(int32_t max_len, int cluster);
 cudaError_t launch_select_topk(const TopkParams& p, cudaStream_t stream);
 
+struct DenseMmParams {
+  const uint16_t* a;      // [m][k] bf16 activations
+  const uint16_t* b;      // [n][k] bf16 weight
+  void* c;                // [m][n] bf16 or fp32
+  float* part;            // workspace: [splits][m][n] fp32 partials (splits > 1)
+  int* err;
+  int32_t m, n, k;
+  int32_t c_fp32;
+  int32_t tiles;          // 128-row weight tiles
+  int32_t kblocks;        // 64-element K blocks
+  int32_t kb_per_split;   // K blocks per CTA
+  int32_t splits;         // K ranges per weight tile
+  uint64_t wait_ns;
+};
+// Fills in tiles / kblocks / kb_per_split / splits from (n, k) and the SM count.
+void plan_dense_mm(DenseMmParams& p, int num_sms);
+size_t dense_mm_workspace_bytes(int32_t n, int32_t k, int num_sms);
+cudaError_t launch_dense_mm(const DenseMmParams& p, const CUtensorMap& wmap,
+                            const CUtensorMap& amap, cudaStream_t stream);
+
 struct DecodeParams {
   dsa_rows rows;
   const uint16_t* q;

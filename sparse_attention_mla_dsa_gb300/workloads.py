@@ -274,3 +274,47 @@ def select_rows(wl: Workload, rows) -> Workload:
         block_table=bt, idx_base=wl.idx_base[rows], q_idx=wl.q_idx[rows],
         head_w=wl.head_w[rows], Q=wl.Q[rows],
         kv_a=None if wl.kv_a is None else wl.kv_a[rows])
+
+
+# --------------------------------------------------------------------------- batched projections
+# The weight-heavy projections of one layer that a K-token verify sweeps once
+# for its K rows ("glm5next_dsa/layer.rs", decode_k notes: q_a, the absorbed
+# q_b, kv_a and the absorbed o projection).  Shapes from the weight field notes
+# of the same page ([local_heads * kv_lora_rank, q_lora_rank] for the absorbed
+# q_b, [hidden, local_heads * kv_lora_rank] for the absorbed o) with 64 heads
+# (the decode configurations), kv_lora_rank 512 (the latent), q_lora_rank
+# 1536 and hidden 4096 (the notes on weights_proj: a read of cfg.hidden
+# elements of the 1536-wide q_resid ran 5120 bytes past its end).  Each entry
+# is (name, output width N, input width K): the weight is [N, K].
+PROJECTIONS = (("q_a", 1536, 4096), ("q_absorb", 64 * 512, 1536), ("kv_a", 512, 4096),
+               ("o_absorb", 4096, 64 * 512))
+
+
+@dataclasses.dataclass
+class ProjectionWorkload:
+    name: str
+    rows: int
+    shapes: tuple                 # ((name, N, K), ...)
+    weights: list                 # [N, K] bf16 bits each, ~ N(0, 1/K)
+    acts: list                    # [rows, K] bf16 bits each, ~ N(0, 1)
+
+    def weight_bytes(self) -> int:
+        return sum(n * k * 2 for _, n, k in self.shapes)
+
+    def algorithmic_bytes(self) -> int:
+        """Weights once plus every row's input and output, per sweep."""
+        return self.weight_bytes() + sum(self.rows * (n + k) * 2 for _, n, k in self.shapes)
+
+
+def make_projections(seed: int = 5, rows: int = 4, shapes=PROJECTIONS) -> ProjectionWorkload:
+    """Synthetic weights and activations for one sweep of ``shapes`` by
+    ``rows`` rows (draw order: per projection the weight, then the rows)."""
+    rng = np.random.default_rng(seed)
+    weights, acts = [], []
+    for _, n, k in shapes:
+        w = rng.standard_normal((n, k), dtype=np.float32)
+        w *= np.float32(1.0 / math.sqrt(k))
+        weights.append(_bf16_bits(w))
+        del w
+        acts.append(_bf16_bits(rng.standard_normal((rows, k), dtype=np.float32)))
+    return ProjectionWorkload(f"proj_k{rows}", rows, tuple(shapes), weights, acts)

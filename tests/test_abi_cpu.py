@@ -65,3 +65,21 @@ def test_decode_split_plan_depends_on_topk_and_heads_only():
     assert api.decode_splits(64, 257) == 2
     for rows in (1, 7, 64):
         assert api.dsa_workspace_bytes(rows, 64, 2048) == rows * api.dsa_workspace_bytes(1, 64, 2048)
+
+
+def test_dense_mm_host_checks_without_gpu():
+    # Argument errors return before any CUDA call (pointers are never touched).
+    from sparse_attention_mla_dsa_gb300 import build
+    lib = ctypes.CDLL(build.build())
+    f = lib.dsa_dense_mm_bf16
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    f.argtypes = [P, P, P, i32, i32, i32, i32, P, ctypes.c_size_t, P]
+    f.restype = ctypes.c_int
+    x = 1 << 20  # a dummy, 16-byte aligned address
+    assert f(x, x, x, 17, 64, 64, 0, None, 0, None) == 2          # more than 16 rows
+    assert f(x, x, x, 0, 64, 64, 0, None, 0, None) == 1           # no rows
+    assert f(x, x, x, 4, 64, 12, 0, None, 0, None) == 1           # k not a multiple of 8
+    assert f(x, x, x, 4, 0, 64, 0, None, 0, None) == 1            # no output columns
+    assert f(None, x, x, 4, 64, 64, 0, None, 0, None) == 1        # null activations
+    assert f(x, x, x, 4, 64, 64, 2, None, 0, None) == 1           # output type flag
+    assert f(x + 8, x, x, 4, 64, 64, 0, None, 0, None) == 1       # misaligned activations
