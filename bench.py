@@ -44,8 +44,8 @@ DESCRIPTIONS = {
               "index 32x128, topk 2048",
     "long": "long-context batch: 64 seqs x 1 row, len log-U[4096,131072], 128 heads, index 64x128, "
             "topk 2048, latent write of the new row",
-    "proj_verify": "K-token verify projections: 4 rows x (q_a 1536x4096, absorbed q_b 32768x1536, "
-                   "kv_a 512x4096, absorbed o 4096x32768) bf16, one weight sweep per step",
+    "proj_verify": "K-token verify projections: 4 rows x (q_a and kv_a stacked 2048x4096, absorbed q_b "
+                   "32768x1536, absorbed o 4096x32768) bf16, one weight sweep per step",
 }
 PROJ_METRIC = ("K-token verify projection rows/s (q_a, absorbed q_b, kv_a, absorbed o of one layer, "
                "64 heads; one bf16 weight sweep per step); % HBM roofline")
@@ -389,8 +389,9 @@ def _proj_oracle_rows_per_s(pw, rows, threads):
 
 
 def run_projections(args):
-    """One step = one layer's four projections for the 4 rows of a K-token
-    verify, each weight swept once (dsa_dense_mm_bf16, bf16 out)."""
+    """One step = one layer's four projections (q_a and kv_a stacked, they share
+    the layer input) for the 4 rows of a K-token verify, each weight swept once
+    (dsa_dense_mm_bf16, bf16 out)."""
     import torch
     rank, world, local = _dist()
     if world > 1:
@@ -539,7 +540,7 @@ def run_projections(args):
         cores = os.cpu_count() or 1
         v = _proj_oracle_rows_per_s(pw, list(range(pw.rows)), cores)
         cpu = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{pw.rows} rows x the four projections, one (row, projection) per "
+               "sample": f"{pw.rows} rows x the projections, one (row, projection) per "
                          f"task over {cores} threads"}
     launches = sum(1 + (1 if api.dsa_dense_mm_workspace_bytes(n, k) > 0 else 0)
                    for _, n, k in pw.shapes)
@@ -577,7 +578,7 @@ def run_projections_reference(args):
         _proj_oracle_rows_per_s(pw, list(range(pw.rows)), cores)
     el = time.perf_counter() - t0
     value = K * pw.rows / el
-    sample = f"{K} steps x {pw.rows} rows x the four projections over {cores} threads"
+    sample = f"{K} steps x {pw.rows} rows x the projections over {cores} threads"
     line = {"impl": "reference", "metric": PROJ_METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": round(el / K * 1e3, 3), "higher_is_better": True, "scaling": "weak",

@@ -101,8 +101,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // read by every weight tile of the launch (keep them).
       const uint64_t w_policy = l2_policy_evict_first();
       const uint64_t a_policy = l2_policy_evict_normal();
+      // The weight is an input no kernel writes: the first stages' weight
+      // tiles go out before the dependency wait (overlapping the tail of the
+      // kernel before), their activation tiles after it, on the same barrier.
+      const int early = min(nkb, kStages);
+      for (int i = 0; i < early; ++i) {
+        mbar_arrive_expect_tx(&ctl->full[i], kStageBytes);
+        tma_load_2d(smem + i * kStageBytes, &wmap, &ctl->full[i], (kb_begin + i) * kBlockK, n0,
+                    w_policy);
+      }
       grid_dep_wait();  // the activations may come from the kernel before
-      int issued = 0;
+      for (int i = 0; i < early; ++i)
+        tma_load_2d(smem + i * kStageBytes + kWBytes, &amap, &ctl->full[i], (kb_begin + i) * kBlockK,
+                    0, a_policy);
+      int issued = early;
       for (; issued < nkb; ++issued) {
         if (aborted(ctl)) break;
         const int s = issued % kStages;

@@ -284,9 +284,11 @@ def select_rows(wl: Workload, rows) -> Workload:
 # q_b, [hidden, local_heads * kv_lora_rank] for the absorbed o) with 64 heads
 # (the decode configurations), kv_lora_rank 512 (the latent), q_lora_rank
 # 1536 and hidden 4096 (the notes on weights_proj: a read of cfg.hidden
-# elements of the 1536-wide q_resid ran 5120 bytes past its end).  Each entry
-# is (name, output width N, input width K): the weight is [N, K].
-PROJECTIONS = (("q_a", 1536, 4096), ("q_absorb", 64 * 512, 1536), ("kv_a", 512, 4096),
+# elements of the 1536-wide q_resid ran 5120 bytes past its end).  q_a and
+# kv_a both project the layer input, so they run as one projection with the
+# two weights stacked (rows 0..1535 q_a, 1536..2047 kv_a).  Each entry is
+# (name, output width N, input width K): the weight is [N, K].
+PROJECTIONS = (("qkv_a", 1536 + 512, 4096), ("q_absorb", 64 * 512, 1536),
                ("o_absorb", 4096, 64 * 512))
 
 
