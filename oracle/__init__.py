@@ -17,7 +17,9 @@ follows on the pages:
 * "Struct Glm5NextDsaLayer" rustdoc page -- ``kv_scale`` (write takes 1/scale).
 * "glm5next_dsa/layer.rs" -- the ``gemm`` helper (C[M, N] = A[M, K] @ B[N, K]^T)
   and the ``decode_k`` notes on the batched projections of the K-token verify
-  (``dense_mm``).
+  (``dense_mm``); the module header trap 2 and ``indexer_forward`` (the
+  indexer's k_norm LayerNorm with a bias and the store at the token's
+  position: ``layer_norm_row``, ``indexer_write_rows``).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, brute force, exhaustive code tables, library routines) and by
@@ -84,6 +86,8 @@ def _load():
             lib.dsa_oracle_bt_entries_needed.restype = i64
             lib.dsa_oracle_dense_mm_row.argtypes = [i32, i32, P, P, P, P]
             lib.dsa_oracle_dense_mm_row.restype = None
+            lib.dsa_oracle_layer_norm_row.argtypes = [i32, P, P, P, f32, P, P]
+            lib.dsa_oracle_layer_norm_row.restype = None
             _lib = lib
     return _lib
 
@@ -243,6 +247,31 @@ def dense_mm(a: np.ndarray, b: np.ndarray):
         c[m] = cm
         mag[m] = gm
     return c, mag
+
+
+def layer_norm_row(x: np.ndarray, w: np.ndarray, b: np.ndarray, eps: float):
+    """Indexer k_norm of one row (nn.LayerNorm with a bias; x, w, b: [dim]
+    bf16 bits) -> (y, mag) in float64.  ("glm5next_dsa/layer.rs", module
+    header trap 2, indexer_forward.)"""
+    x, w, b = _c(x, np.uint16), _c(w, np.uint16), _c(b, np.uint16)
+    dim = x.shape[0]
+    y = np.zeros(dim, np.float64)
+    mag = np.zeros(dim, np.float64)
+    _load().dsa_oracle_layer_norm_row(dim, _ptr(x), _ptr(w), _ptr(b), float(eps), _ptr(y), _ptr(mag))
+    return y, mag
+
+
+def indexer_write_rows(k_raw: np.ndarray, ln_w: np.ndarray, ln_b: np.ndarray, eps: float,
+                       idx_base: np.ndarray, positions: np.ndarray):
+    """Indexer write side for each row r: the arena row t = idx_base[r] +
+    positions[r] that receives LayerNorm(k_raw[r]).  Returns [(t, y, mag)].
+    ("glm5next_dsa/layer.rs", indexer_forward: the row lands at the token's
+    position, placed from a device-side position by dsa_indexer_store.)"""
+    out = []
+    for r in range(k_raw.shape[0]):
+        y, mag = layer_norm_row(k_raw[r], ln_w, ln_b, eps)
+        out.append((int(idx_base[r]) + int(positions[r]), y, mag))
+    return out
 
 
 def run_path_rows(wl, rows=None, threads: int = 1, sel_from=None):

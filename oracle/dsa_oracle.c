@@ -360,3 +360,32 @@ void dsa_oracle_dense_mm_row(int n, int k, const uint16_t *a_row, const uint16_t
             mag[j] = m;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Indexer write side: k_norm                                                */
+/* ------------------------------------------------------------------------ */
+
+/* "glm5next_dsa/layer.rs", module header trap 2 and indexer_forward: the
+ * indexer's k_norm is an nn.LayerNorm with a bias (mean subtraction, the
+ * biased variance, weight and bias), applied to the wk projection of the
+ * token before it is stored in the key cache. */
+void dsa_oracle_layer_norm_row(int dim, const uint16_t *x, const uint16_t *w, const uint16_t *b,
+                               float eps, double *y, double *mag)
+{
+    double mu = 0.0, var = 0.0;
+    for (int d = 0; d < dim; ++d)
+        mu += dsa_oracle_bf16_value(x[d]);
+    mu /= dim;
+    for (int d = 0; d < dim; ++d) {
+        double c = dsa_oracle_bf16_value(x[d]) - mu;
+        var += c * c;
+    }
+    var /= dim;
+    double inv = 1.0 / sqrt(var + (double)eps);
+    for (int d = 0; d < dim; ++d) {
+        double t = (dsa_oracle_bf16_value(x[d]) - mu) * inv * dsa_oracle_bf16_value(w[d]);
+        y[d] = t + dsa_oracle_bf16_value(b[d]);
+        if (mag)
+            mag[d] = fabs(t) + fabs(dsa_oracle_bf16_value(b[d]));
+    }
+}

@@ -115,6 +115,14 @@ int64_t dsa_oracle_bt_entries_needed(int64_t seq_len, int64_t k, int64_t block_s
 void dsa_oracle_dense_mm_row(int n, int k, const uint16_t *a_row, const uint16_t *b,
                              double *c, double *mag);
 
+/* Indexer k_norm (nn.LayerNorm with a bias) of one row:
+ *   mu = sum_d x_d / dim,  var = sum_d (x_d - mu)^2 / dim
+ *   y_d = (x_d - mu) / sqrt(var + eps) * w_d + b_d
+ * x, w, b: [dim] bf16 bits; y: [dim]; mag (optional): [dim]
+ * |(x_d - mu) / sqrt(var + eps) * w_d| + |b_d| (scale for tolerances). */
+void dsa_oracle_layer_norm_row(int dim, const uint16_t *x, const uint16_t *w, const uint16_t *b,
+                               float eps, double *y, double *mag);
+
 #ifdef __cplusplus
 }
 #endif

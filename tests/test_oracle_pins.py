@@ -427,3 +427,77 @@ def test_planted_dense_mm_mistakes_are_caught(oracle):
     cs, _ = oracle.dense_mm(a, sq)
     cst, _ = oracle.dense_mm(a, np.ascontiguousarray(sq.T))
     assert not np.array_equal(cs, cst)
+
+
+# ----------------------------------------------------------------------------- indexer k_norm
+def test_layer_norm_matches_torch_layer_norm_fp64(oracle):
+    # The pages name it an nn.LayerNorm with a bias: torch's own layer_norm in
+    # float64 on the same values is that definition.
+    rng = np.random.default_rng(9)
+    for dim, eps in ((128, 1e-6), (64, 1e-5)):
+        x = _bf16(rng.standard_normal(dim) * 3 + 1)
+        w = _bf16(rng.standard_normal(dim))
+        b = _bf16(rng.standard_normal(dim))
+        y, _ = oracle.layer_norm_row(x, w, b, eps)
+        xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double()
+        wv = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).double()
+        bv = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).double()
+        ref = torch.nn.functional.layer_norm(xv, (dim,), wv, bv, float(np.float32(eps))).numpy()
+        assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_norm_closed_forms(oracle):
+    dim = 128
+    rng = np.random.default_rng(10)
+    w = _bf16(rng.standard_normal(dim))
+    b = _bf16(rng.standard_normal(dim))
+    bval = np.array([oracle.bf16_value(int(v)) for v in b])
+    # A constant row has no deviation from its mean: the output is the bias.
+    y, _ = oracle.layer_norm_row(np.full(dim, _bf16([2.5])[0], np.uint16), w, b, 1e-6)
+    assert np.array_equal(y, bval)
+    # With w = 1, b = 0 the output has mean 0 and mean square var / (var + eps).
+    x = _bf16(rng.standard_normal(dim))
+    xv = np.array([oracle.bf16_value(int(v)) for v in x])
+    ones = np.full(dim, 0x3F80, np.uint16)
+    eps = 0.25
+    y, _ = oracle.layer_norm_row(x, ones, np.zeros(dim, np.uint16), eps)
+    var = np.mean((xv - xv.mean()) ** 2)
+    assert abs(y.mean()) < 1e-12
+    assert abs(np.mean(y ** 2) - var / (var + eps)) < 1e-12
+    # Shifting the input by a constant leaves the output unchanged (mean
+    # subtraction); an RMSNorm would not.  Quarter-integers in [-8, 8) and
+    # their shift by 8 are exact in bf16, and so are the sums and the mean in
+    # double, so the two outputs agree bit for bit.
+    q = rng.integers(-32, 32, size=dim) / 4.0
+    y1, _ = oracle.layer_norm_row(_bf16(q), w, b, 1e-6)
+    y2, _ = oracle.layer_norm_row(_bf16(q + 8.0), w, b, 1e-6)
+    assert np.array_equal(y1, y2)
+
+
+def test_indexer_write_rows_place_each_row_at_its_position(oracle):
+    rng = np.random.default_rng(11)
+    D = 64
+    k_raw = _bf16(rng.standard_normal((3, D)))
+    w = _bf16(rng.standard_normal(D))
+    b = _bf16(rng.standard_normal(D))
+    out = oracle.indexer_write_rows(k_raw, w, b, 1e-6, np.array([0, 0, 1000]), np.array([5, 6, 0]))
+    assert [t for t, _, _ in out] == [5, 6, 1000]
+    for r, (_, y, _) in enumerate(out):
+        assert np.array_equal(y, oracle.layer_norm_row(k_raw[r], w, b, 1e-6)[0])
+
+
+def test_planted_layer_norm_mistakes_are_caught(oracle):
+    # An RMSNorm in its place (no mean subtraction) or a dropped bias breaks
+    # the constant-row pin.
+    dim = 64
+    rng = np.random.default_rng(12)
+    w = _bf16(rng.standard_normal(dim))
+    b = _bf16(rng.standard_normal(dim))
+    bval = np.array([oracle.bf16_value(int(v)) for v in b])
+    wval = np.array([oracle.bf16_value(int(v)) for v in w])
+    xc = np.full(dim, 2.5)
+    rms_form = xc / np.sqrt(np.mean(xc ** 2) + 1e-6) * wval + bval
+    no_bias = (xc - xc.mean()) / np.sqrt(np.var(xc) + 1e-6) * wval
+    y, _ = oracle.layer_norm_row(np.full(dim, _bf16([2.5])[0], np.uint16), w, b, 1e-6)
+    assert np.array_equal(y, bval)
+    assert not np.allclose(rms_form, bval) and not np.allclose(no_bias, bval)
