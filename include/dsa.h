@@ -217,6 +217,32 @@ size_t dsa_noalloc_scratch_bytes(int32_t rows, int32_t heads, int32_t topk);
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 
 /*
+ * Indexer write side for each row's new token ("glm5next_dsa/layer.rs",
+ * module header trap 2: indexer.k_norm is an nn.LayerNorm with a bias;
+ * indexer_forward: the wk projection of the token lands in the key cache row,
+ * normalised in place, the row placed from a DEVICE-side position so that a
+ * captured graph replays at the next position).  For each row r, at arena
+ * row t = idx_base[r] + positions[r]:
+ *   mu = mean_d k_raw[r][d],   var = mean_d (k_raw[r][d] - mu)^2
+ *   idx_k[t][d] = bf16_rne((k_raw[r][d] - mu) / sqrt(var + eps) * ln_w[d] + ln_b[d])
+ *   idx_gate[t] = gate[r]                                (when gate != NULL)
+ *   k_raw [rows][index_dim] bf16 (the wk projection, e.g. from
+ *         dsa_dense_mm_bf16), 8-byte aligned
+ *   ln_w, ln_b [index_dim] bf16     gate [rows] bf16 or NULL
+ *   idx_k [idx_tokens][index_dim] bf16, 8-byte aligned; idx_gate [idx_tokens]
+ * rows->positions is required (the new token of row r is position
+ * seq_lens[r]-1).  index_dim 64 or 128 (DSA_ERR_UNSUPPORTED otherwise).
+ * Numerics: mean, variance and the affine map in double, one rounding to
+ * bf16 (nearest, ties to even).  A row whose position is not seq_lens[r]-1
+ * (DSA_DEVERR_POSITION) or whose arena row lies outside [0, idx_tokens)
+ * (DSA_DEVERR_ARENA) is skipped and recorded.
+ */
+dsa_status dsa_indexer_write(const dsa_rows *rows, const uint16_t *k_raw, const uint16_t *ln_w,
+                             const uint16_t *ln_b, float eps, const uint16_t *gate,
+                             const int64_t *idx_base, uint16_t *idx_k, uint16_t *idx_gate,
+                             int64_t idx_tokens, int32_t index_dim, void *stream);
+
+/*
  * Batched projection for the K-token verify: the K rows of one sequence sweep
  * a BF16 weight once ("glm5next_dsa/layer.rs": the gemm helper,
  * C[M, N] = A[M, K] @ B[N, K]^T, and the decode_k notes on

@@ -62,6 +62,7 @@ def load() -> ctypes.CDLL:
         "dsa_mla_decode_fp8_noalloc": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P],
         "dsa_get_error": [P, P, P, i32],
         "dsa_dense_mm_bf16": [P, P, P, i32, i32, i32, i32, P, sz, P],
+        "dsa_indexer_write": [RP, P, P, P, f32, P, P, P, P, i64, i32, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -198,6 +199,23 @@ def dsa_mla_decode_fp8_noalloc(rows: Rows, q: torch.Tensor, pool: torch.Tensor, 
                                         _ptr(out, torch.uint16, "out"), _ptr(lse, torch.float32, "lse"),
                                         _stream(stream))
     _check("dsa_mla_decode_fp8_noalloc", st)
+
+
+def dsa_indexer_write(rows: Rows, k_raw: torch.Tensor, ln_w: torch.Tensor, ln_b: torch.Tensor,
+                      eps: float, idx_base: torch.Tensor, idx_k: torch.Tensor,
+                      idx_gate: torch.Tensor | None = None, gate: torch.Tensor | None = None,
+                      stream=None) -> None:
+    """LayerNorm (with bias) of each row's k_raw [R, D] bf16, stored into the
+    key arena idx_k [T, D] at row idx_base[r] + positions[r] (and gate[r] into
+    idx_gate there when given)."""
+    lib = load()
+    st = lib.dsa_indexer_write(ctypes.byref(rows), _ptr(k_raw, torch.uint16, "k_raw"),
+                               _ptr(ln_w, torch.uint16, "ln_w"), _ptr(ln_b, torch.uint16, "ln_b"),
+                               float(eps), _ptr(gate, torch.uint16, "gate"),
+                               _ptr(idx_base, torch.int64, "idx_base"), _ptr(idx_k, torch.uint16, "idx_k"),
+                               _ptr(idx_gate, torch.uint16, "idx_gate"), idx_k.shape[0], idx_k.shape[1],
+                               _stream(stream))
+    _check("dsa_indexer_write", st)
 
 
 def dsa_dense_mm_bf16(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor,

@@ -256,6 +256,39 @@ size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
   return mla_decode_tc_workspace_bytes(rows, heads, topk);
 }
 
+dsa_status dsa_indexer_write(const dsa_rows* rows, const uint16_t* k_raw, const uint16_t* ln_w,
+                             const uint16_t* ln_b, float eps, const uint16_t* gate,
+                             const int64_t* idx_base, uint16_t* idx_k, uint16_t* idx_gate,
+                             int64_t idx_tokens, int32_t index_dim, void* stream) {
+  dsa_status st = check_rows(rows, false);
+  if (st != DSA_OK) return st;
+  if (rows->positions == nullptr || k_raw == nullptr || ln_w == nullptr || ln_b == nullptr ||
+      idx_base == nullptr || idx_k == nullptr || idx_tokens < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (gate != nullptr && idx_gate == nullptr) return DSA_ERR_INVALID_ARG;
+  if (index_dim != 64 && index_dim != 128) return DSA_ERR_UNSUPPORTED;
+  if (!(eps >= 0.0f)) return DSA_ERR_INVALID_ARG;
+  if (!aligned(k_raw, 8) || !aligned(idx_k, 8)) return DSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = device_info();
+  if (dev == nullptr) return DSA_ERR_CUDA;
+  IndexerWriteParams p{};
+  p.positions = rows->positions;
+  p.seq_lens = rows->seq_lens;
+  p.idx_base = idx_base;
+  p.k_raw = k_raw;
+  p.ln_w = ln_w;
+  p.ln_b = ln_b;
+  p.gate = gate;
+  p.idx_k = idx_k;
+  p.idx_gate = idx_gate;
+  p.idx_tokens = idx_tokens;
+  p.rows = rows->rows;
+  p.dim = index_dim;
+  p.eps = eps;
+  p.err = dev->err;
+  return launched(launch_indexer_write(p, static_cast<cudaStream_t>(stream)));
+}
+
 size_t dsa_dense_mm_workspace_bytes(int32_t n_out, int32_t k) {
   if (n_out < 1 || k < 8 || k % 8 != 0) return 0;
   const DeviceInfo* dev = device_info();

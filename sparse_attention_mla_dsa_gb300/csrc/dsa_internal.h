@@ -81,6 +81,24 @@ int topk_cluster_size(int32_t max_len);
 size_t topk_smem_bytes(int32_t max_len, int cluster);
 cudaError_t launch_select_topk(const TopkParams& p, cudaStream_t stream);
 
+struct IndexerWriteParams {
+  const uint32_t* positions;
+  const int32_t* seq_lens;
+  const int64_t* idx_base;
+  const uint16_t* k_raw;   // [rows][dim] bf16
+  const uint16_t* ln_w;    // [dim] bf16
+  const uint16_t* ln_b;    // [dim] bf16
+  const uint16_t* gate;    // [rows] bf16 or nullptr
+  uint16_t* idx_k;         // [idx_tokens][dim] bf16
+  uint16_t* idx_gate;      // [idx_tokens] bf16
+  int64_t idx_tokens;
+  int32_t rows;
+  int32_t dim;
+  float eps;
+  int* err;
+};
+cudaError_t launch_indexer_write(const IndexerWriteParams& p, cudaStream_t stream);
+
 struct DenseMmParams {
   const uint16_t* a;      // [m][k] bf16 activations
   const uint16_t* b;      // [n][k] bf16 weight

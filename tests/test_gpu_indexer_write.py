@@ -1,0 +1,157 @@
+"""Indexer write side on the GPU: the wk projection of each row's new token
+(dsa_dense_mm_bf16), the k_norm LayerNorm with a bias and the store into the
+key arena at the row's device-side position (dsa_indexer_write), against the
+FP64 oracle ("glm5next_dsa/layer.rs", module header trap 2, indexer_forward).
+
+The norm runs in double on both sides and is rounded once to bf16, so the
+stored bytes must equal the oracle's value rounded to nearest-even, except
+where that value lies within 1e-12 (relative) of a rounding midpoint (the two
+sides sum in different orders); such elements are counted (expected none).
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = np.int16(0x7FC0)  # bf16 NaN in rows nothing may write
+
+
+@pytest.fixture(scope="module")
+def api():
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_attention_mla_dsa_gb300 import api
+    api.load()
+    api.dsa_get_error(reset=True)
+    return api
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+
+
+def _bf16_rne(v):
+    """Round float64 values to bf16 bit patterns, nearest-even, and flag the
+    ones within 1e-12 relative of a midpoint."""
+    v = np.asarray(v, np.float64)
+    f = v.astype(np.float32).view(np.uint32).astype(np.int64)
+    base = f & 0xFFFF0000
+    cands = np.stack([base - 0x10000, base, base + 0x10000])
+    ok = (cands >= 0) & ((cands >> 31) == (base >> 31))
+    vals = np.where(ok, cands, 0).astype(np.uint32).view(np.float32).astype(np.float64)
+    dist = np.where(ok, np.abs(vals - v[None]), np.inf)
+    order = np.argsort(dist, axis=0, kind="stable")
+    best = np.take_along_axis(dist, order[:1], 0)[0]
+    second = np.take_along_axis(dist, order[1:2], 0)[0]
+    pick = np.take_along_axis(cands, order[:1], 0)[0]
+    alt = np.take_along_axis(cands, order[1:2], 0)[0]
+    tie = np.abs(best - second) <= 1e-12 * np.abs(v)
+    even = np.where(((pick >> 16) & 1) == 0, pick, alt)
+    out = np.where(best == second, even, pick)
+    return (out >> 16).astype(np.uint16), tie
+
+
+def _rows(api, seq_lens, positions):
+    sl = torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
+    pos = torch.tensor(positions, dtype=torch.int32, device="cuda")
+    return api.make_rows(sl, positions=pos), (sl, pos)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_projection_norm_and_store_match_oracle(api, oracle, D):
+    rng = np.random.default_rng(21 + D)
+    R, H, T = 6, 4096, 4000
+    hidden = _bf16(rng.standard_normal((R, H)))
+    wk = _bf16(rng.standard_normal((D, H)) / np.sqrt(H))
+    ln_w = _bf16(1.0 + 0.1 * rng.standard_normal(D))
+    ln_b = _bf16(0.1 * rng.standard_normal(D))
+    gate = _bf16(1.0 / (1.0 + np.exp(-rng.standard_normal(R))))
+    seq_lens = [1, 17, 900, 901, 2000, 64]
+    positions = [L - 1 for L in seq_lens]
+    idx_base = np.array([0, 0, 1000, 1000, 1950, 3900], np.int64)
+    eps = 1e-6
+
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    k_raw = torch.empty((R, D), dtype=torch.int16, device="cuda")
+    ws = torch.empty(max(256, api.dsa_dense_mm_workspace_bytes(D, H)), dtype=torch.uint8, device="cuda")
+    api.dsa_dense_mm_bf16(dev(hidden), dev(wk), k_raw, ws)
+    idx_k = torch.full((T, D), SENTINEL, dtype=torch.int16, device="cuda")
+    idx_gate = torch.full((T,), SENTINEL, dtype=torch.int16, device="cuda")
+    rows, keep = _rows(api, seq_lens, positions)
+    base_d = torch.from_numpy(idx_base).cuda()
+    api.dsa_indexer_write(rows, k_raw, dev(ln_w), dev(ln_b), eps, base_d, idx_k, idx_gate, dev(gate))
+    torch.cuda.synchronize()
+    assert api.dsa_get_error(reset=True)[0] == 0
+
+    kr = k_raw.cpu().numpy().view(np.uint16)
+    arena = idx_k.cpu().numpy().view(np.uint16)
+    gates = idx_gate.cpu().numpy().view(np.uint16)
+    # The projection itself is the batched projection (tested on its own);
+    # here its bf16 output must be close to the oracle's product.
+    ref_k, mag = oracle.dense_mm(hidden, wk)
+    kv = torch.from_numpy(kr.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.all(np.abs(kv - ref_k) <= 1e-3 * mag + 2.0 ** -8 * np.abs(ref_k))
+    written = set()
+    ties = 0
+    for t, y, _ in oracle.indexer_write_rows(kr, ln_w, ln_b, eps, idx_base, np.array(positions)):
+        want, tie = _bf16_rne(y)
+        ties += int(tie.sum())
+        assert np.array_equal(arena[t][~tie], want[~tie]), f"arena row {t}"
+        written.add(t)
+    for r in range(R):
+        assert gates[idx_base[r] + positions[r]] == gate[r]
+    untouched = np.array([t for t in range(T) if t not in written])
+    assert np.all(arena[untouched] == np.uint16(SENTINEL))
+    assert np.all(gates[untouched] == np.uint16(SENTINEL))
+    assert ties == 0
+
+
+def test_bad_rows_are_skipped_and_recorded(api):
+    D, T = 128, 256
+    rng = np.random.default_rng(3)
+    k_raw = torch.from_numpy(_bf16(rng.standard_normal((3, D))).view(np.int16)).cuda()
+    ln_w = torch.from_numpy(_bf16(np.ones(D)).view(np.int16)).cuda()
+    ln_b = torch.zeros(D, dtype=torch.int16, device="cuda")
+    idx_k = torch.full((T, D), SENTINEL, dtype=torch.int16, device="cuda")
+    base = torch.tensor([0, 0, 250], dtype=torch.int64, device="cuda")
+    # row 0 fine (t = 9); row 1 position != seq_len - 1; row 2 runs past the arena
+    rows, keep = _rows(api, [10, 20, 10], [9, 5, 9])
+    api.dsa_indexer_write(rows, k_raw, ln_w, ln_b, 1e-6, base, idx_k)
+    torch.cuda.synchronize()
+    code, row, count = api.dsa_get_error(reset=True)
+    names = {v: k for k, v in api.DEVERR.items()}
+    assert code in (names["position"], names["arena"]) and count == 2
+    arena = idx_k.cpu().numpy().view(np.uint16)
+    assert not np.all(arena[9] == np.uint16(SENTINEL))
+    assert np.all(np.delete(arena, 9, axis=0) == np.uint16(SENTINEL))
+
+
+def test_graph_replay_writes_the_next_position(api):
+    # The placement comes from device memory: one captured write, replayed
+    # after the row's position advances, lands one row further.
+    D, T = 128, 64
+    rng = np.random.default_rng(4)
+    k_raw = torch.from_numpy(_bf16(rng.standard_normal((1, D))).view(np.int16)).cuda()
+    ln_w = torch.from_numpy(_bf16(np.ones(D)).view(np.int16)).cuda()
+    ln_b = torch.zeros(D, dtype=torch.int16, device="cuda")
+    idx_k = torch.full((T, D), SENTINEL, dtype=torch.int16, device="cuda")
+    base = torch.tensor([10], dtype=torch.int64, device="cuda")
+    rows, (sl, pos) = _rows(api, [5], [4])
+    api.dsa_indexer_write(rows, k_raw, ln_w, ln_b, 1e-6, base, idx_k)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        api.dsa_indexer_write(rows, k_raw, ln_w, ln_b, 1e-6, base, idx_k)
+    for step in range(2):
+        sl += 1
+        pos += 1
+        g.replay()
+    torch.cuda.synchronize()
+    assert api.dsa_get_error(reset=True)[0] == 0
+    arena = idx_k.cpu().numpy().view(np.uint16)
+    first = arena[14].copy()
+    assert not np.all(first == np.uint16(SENTINEL))
+    assert np.array_equal(arena[15], first) and np.array_equal(arena[16], first)
+    assert np.all(np.delete(arena, [14, 15, 16], axis=0) == np.uint16(SENTINEL))
