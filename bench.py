@@ -44,9 +44,13 @@ DESCRIPTIONS = {
               "index 32x128, topk 2048",
     "long": "long-context batch: 64 seqs x 1 row, len log-U[4096,131072], 128 heads, index 64x128, "
             "topk 2048, latent write of the new row",
+    "index_write": "indexer write side: 4 rows x (wk 128x4096 bf16 out, weights_proj 32x4096 fp32 out, "
+                   "LayerNorm with bias + store into a 131072-token key arena), L2 flushed between steps",
     "proj_verify": "K-token verify projections: 4 rows x (q_a and kv_a stacked 2048x4096, absorbed q_b "
                    "32768x1536, absorbed o 4096x32768) bf16, one weight sweep per step",
 }
+IW_METRIC = ("indexer write rows/s (wk and weights_proj projections, k_norm LayerNorm with bias, "
+             "store at the device-side position); % HBM roofline")
 PROJ_METRIC = ("K-token verify projection rows/s (q_a, absorbed q_b, kv_a, absorbed o of one layer, "
                "64 heads; one bf16 weight sweep per step); % HBM roofline")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -591,6 +595,192 @@ def run_projections_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- indexer write side
+IW_ROWS, IW_HIDDEN, IW_DIM, IW_HEADS, IW_TOKENS = 4, 4096, 128, 32, 131072
+
+
+def _iw_inputs(seed=6):
+    """Synthetic inputs of the indexer write step (weights_proj carries the
+    index_heads^-0.5 scale, folded in as the pages fold it at load)."""
+    import numpy as np
+    from sparse_attention_mla_dsa_gb300 import workloads
+    rng = np.random.default_rng(seed)
+    f32 = np.float32
+    hidden = workloads._bf16_bits(rng.standard_normal((IW_ROWS, IW_HIDDEN), dtype=f32))
+    wk = workloads._bf16_bits(rng.standard_normal((IW_DIM, IW_HIDDEN), dtype=f32) / f32(IW_HIDDEN ** 0.5))
+    wp = workloads._bf16_bits(rng.standard_normal((IW_HEADS, IW_HIDDEN), dtype=f32)
+                              / f32(IW_HIDDEN ** 0.5) * f32(IW_HEADS ** -0.5))
+    ln_w = workloads._bf16_bits(1.0 + 0.1 * rng.standard_normal(IW_DIM, dtype=f32))
+    ln_b = workloads._bf16_bits(0.1 * rng.standard_normal(IW_DIM, dtype=f32))
+    lens = rng.integers(IW_TOKENS // 8, IW_TOKENS // IW_ROWS, size=IW_ROWS)
+    base = np.arange(IW_ROWS, dtype=np.int64) * (IW_TOKENS // IW_ROWS)
+    return hidden, wk, wp, ln_w, ln_b, lens.astype(np.int32), base
+
+
+def _iw_bytes():
+    w = (IW_DIM + IW_HEADS) * IW_HIDDEN * 2
+    return w + IW_ROWS * (IW_HIDDEN * 2 + IW_DIM * 2 * 2 + IW_DIM * 2 + IW_HEADS * 4)
+
+
+def run_indexer_write(args):
+    """One step = the indexer write side of 4 rows: the wk projection (bf16
+    out) and the weights_proj projection (FP32 out, the head weights S1 reads)
+    by dsa_dense_mm_bf16, then dsa_indexer_write.  The step's data is small
+    and L2-resident, so L2 is flushed (a 2 x L2 buffer written) before every
+    timed step and each step is timed on its own events."""
+    import numpy as np
+    import torch
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import __graft_entry__
+    from sparse_attention_mla_dsa_gb300 import build as _b
+    if rank == 0 and _b.is_stale():
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from sparse_attention_mla_dsa_gb300 import api, shard
+    api.load()
+    hidden, wk, wp, ln_w, ln_b, lens, base = _iw_inputs()
+    d16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+    t_hidden, t_wk, t_wp, t_lw, t_lb = d16(hidden), d16(wk), d16(wp), d16(ln_w), d16(ln_b)
+    k_raw = torch.empty((IW_ROWS, IW_DIM), dtype=torch.int16, device=dev)
+    head_w = torch.empty((IW_ROWS, IW_HEADS), dtype=torch.float32, device=dev)
+    arena = torch.zeros((IW_TOKENS, IW_DIM), dtype=torch.int16, device=dev)
+    ws1 = torch.empty(max(256, api.dsa_dense_mm_workspace_bytes(IW_DIM, IW_HIDDEN)), dtype=torch.uint8, device=dev)
+    ws2 = torch.empty(max(256, api.dsa_dense_mm_workspace_bytes(IW_HEADS, IW_HIDDEN)), dtype=torch.uint8, device=dev)
+    seq_lens = torch.from_numpy(lens).to(dev)
+    positions = (seq_lens - 1).to(torch.int32)
+    idx_base = torch.from_numpy(base).to(dev)
+    rows = api.make_rows(seq_lens, positions=positions)
+
+    def step():
+        api.dsa_dense_mm_bf16(t_hidden, t_wk, k_raw, ws1)
+        api.dsa_dense_mm_bf16(t_hidden, t_wp, head_w, ws2)
+        api.dsa_indexer_write(rows, k_raw, t_lw, t_lb, 1e-6, idx_base, arena)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if api.dsa_get_error(reset=True)[0] != 0:
+        raise RuntimeError("device error during warm-up")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            g.replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    step_ms = shard.max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / K)
+    if api.dsa_get_error(reset=True)[0] != 0:
+        raise RuntimeError("device error during the timed steps")
+    value = IW_ROWS * world / (step_ms / 1e3)
+    peak, peak_kind = _peaks()
+    alg = _iw_bytes()
+    ach = alg / (step_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "index_write step", "achieved": round(ach, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind, "traffic": None,
+                "algorithmic_bytes": alg}
+    e2e = None
+    if not args.no_e2e:
+        h_in = torch.from_numpy(hidden.view(np.int16)).pin_memory()
+        h_out = torch.empty((IW_ROWS, IW_HEADS), dtype=torch.float32).pin_memory()
+
+        def host_step():
+            t_hidden.copy_(h_in, non_blocking=True)
+            step()
+            h_out.copy_(head_w, non_blocking=True)
+
+        host_step()
+        torch.cuda.synchronize()
+        hg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(hg):
+            host_step()
+        hevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            hevs[i][0].record(stream)
+            hg.replay()
+            hevs[i][1].record(stream)
+        torch.cuda.synchronize()
+        ems = shard.max_over_ranks(sum(a.elapsed_time(b) for a, b in hevs) / K)
+        e2e = {"value": round(IW_ROWS * world / (ems / 1e3), 2), "unit": UNIT,
+               "h2d_bytes_per_step": h_in.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 4}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, cores = _iw_oracle_rows_per_s(1)
+        cpu = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{IW_ROWS} rows: both projections and the norm, one task per row"}
+    launches = 3 + sum(1 for n in (IW_DIM, IW_HEADS) if api.dsa_dense_mm_workspace_bytes(n, IW_HIDDEN) > 0)
+    line = {
+        "metric": IW_METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": IW_ROWS,
+                   "algorithmic_bytes_per_step": alg,
+                   "l2": f"flushed before every step (a {2 * l2 / 1e6:.0f} MB buffer written)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU", "launch": "cuda-graph"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K * launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _iw_oracle_rows_per_s(reps):
+    import numpy as np
+    import oracle
+    oracle.build()
+    hidden, wk, wp, ln_w, ln_b, lens, base = _iw_inputs()
+    cores = os.cpu_count() or 1
+
+    def one(r):
+        row = np.ascontiguousarray(hidden[r:r + 1])
+        c, _ = oracle.dense_mm(row, wk)
+        oracle.dense_mm(row, wp)
+        from sparse_attention_mla_dsa_gb300 import workloads
+        oracle.layer_norm_row(workloads._bf16_bits(c[0]), ln_w, ln_b, 1e-6)
+
+    rows = [r % IW_ROWS for r in range(reps * IW_ROWS)]
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(one, rows))
+    return len(rows) / (time.perf_counter() - t0), cores
+
+
+def run_indexer_write_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    v, cores = _iw_oracle_rows_per_s(max(1, args.steps))
+    line = {"impl": "reference", "metric": IW_METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(IW_ROWS / v * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": IW_ROWS},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} steps x {IW_ROWS} rows over {cores} threads"},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------------------- oracle (CPU)
 def _oracle_rows_per_s(wl, rows, threads):
     import oracle
@@ -654,10 +844,14 @@ def main():
             args.steps = 20     # the oracle is slow; keep the run within minutes
         if args.workload == "proj_verify":
             run_projections_reference(args)
+        elif args.workload == "index_write":
+            run_indexer_write_reference(args)
         else:
             run_reference(args)
     elif args.workload == "proj_verify":
         run_projections(args)
+    elif args.workload == "index_write":
+        run_indexer_write(args)
     else:
         run_ours(args)
 
