@@ -66,6 +66,7 @@ def assert_out(gpu, ref, tag=""):
 def assert_lse(gpu, ref, tag=""):
     gpu = gpu.astype(np.float64)
     both_inf = np.isneginf(gpu) & np.isneginf(ref)
-    err = np.where(both_inf, 0.0, np.abs(gpu - ref))
+    with np.errstate(invalid="ignore"):          # -inf - -inf where both are empty
+        err = np.where(both_inf, 0.0, np.abs(gpu - ref))
     assert (err <= 1e-4 * np.maximum(1.0, np.abs(np.where(both_inf, 0, ref)))).all(), \
         f"{tag}: lse max err {err.max()}"

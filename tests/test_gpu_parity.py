@@ -111,6 +111,29 @@ def test_ragged_and_short_rows(dsa, oracle):
     check_path(oracle, api, path, wl)
 
 
+def test_empty_row_large_topk_and_odd_index_heads(dsa, oracle):
+    """A row with seq_len 0 (nothing visible: every entry -1, out 0, lse -inf),
+    rows far below topk, topk 4096 (sixteen 256-entry splits per row at 64
+    heads) and 24 index heads (not a multiple of 16: one row per launch group)."""
+    api, path = dsa
+    wl = workloads.make_workload("edge", 41, seqs=4, rows_per_seq=1, len_kind="list", len_lo=0,
+                                 len_hi=0, lens=[0, 1, 2, 5000], heads=64, index_heads=24,
+                                 index_dim=128, topk=4096, with_write=False)
+    dw = check_path(oracle, api, path, wl)
+    assert np.all(dw.sel.cpu().numpy()[0] == -1)
+    assert np.all(dw.out_f32()[0] == 0) and np.all(np.isneginf(dw.lse.cpu().numpy()[0]))
+
+
+def test_many_head_groups_with_write(dsa, oracle):
+    """256 heads (four 64-head groups, 2048-entry splits), 64 index heads,
+    topk 4096 (two splits per head group), with the latent write first."""
+    api, path = dsa
+    wl = workloads.make_workload("wide", 42, seqs=2, rows_per_seq=1, len_kind="list", len_lo=0,
+                                 len_hi=0, lens=[3000, 7000], heads=256, index_heads=64,
+                                 index_dim=128, topk=4096, with_write=True)
+    check_path(oracle, api, path, wl)
+
+
 def test_k_row_verify_bit_identical_to_serial(dsa, oracle):
     """decode_k: a K-row verify launch equals K single-row launches bit for bit."""
     api, path = dsa
