@@ -6,9 +6,9 @@ in stream order -- S0 latent write (when the workload writes new rows), S1
 index scores, S2 top-k, S3 gather-attend -- without any host synchronisation.
 
 ``DsaDecoder`` is the host-facing form: per step it copies that step's inputs
-(queries, head weights, the new latent rows, row metadata) from pinned host
-memory to the device, runs the same four calls and reads the attention output
-back into pinned host memory.
+(queries, head weights, the new latent rows, row metadata) from one pinned
+host staging buffer to the device in one copy, runs the same four calls and
+reads the attention output back into pinned host memory.
 """
 from __future__ import annotations
 
@@ -117,13 +117,19 @@ class DsaDecoder:
     """Host-facing decode: resident caches, per-step host inputs and outputs.
 
     The caches (key arena, gate, FP8 latent pool) live on the device; each
-    ``decode`` call copies the step's inputs from pinned host buffers to the
-    device, runs S0-S3 and copies the attention output back.  With
-    ``graphs=True`` (the default) that whole sequence -- the host-to-device
-    copies, the four calls and the device-to-host copy -- is captured once per
-    cache replica as a CUDA graph and replayed, so a step costs one launch; the
-    pinned buffers and device tensors keep their addresses, so each replay
-    moves the current contents of the pinned inputs."""
+    ``decode`` call copies the step's inputs from pinned host memory to the
+    device, runs S0-S3 and copies the attention output back.  The per-step
+    inputs (queries, head weights, the new latent rows, row metadata) sit in
+    one pinned staging buffer mirrored by one device buffer per cache replica,
+    whose views the kernels read, so a step moves its inputs in one copy.
+    With ``graphs=True`` (the default) the whole sequence -- the host-to-device
+    copy, the four calls and the device-to-host copy -- is captured once per
+    cache replica as a CUDA graph and replayed, so a step costs one launch;
+    the buffers keep their addresses, so each replay moves the current
+    contents of the pinned inputs."""
+
+    _INPUTS = ("q_idx", "head_w", "Q", "seq_lens", "positions", "slots", "block_table",
+               "idx_base")
 
     def __init__(self, wl, device: str | torch.device = "cuda", replicas: int = 1,
                  graphs: bool = True):
@@ -131,17 +137,31 @@ class DsaDecoder:
         self.replicas = [first] + [first.clone() for _ in range(replicas - 1)]
         self._next = 0
         self._graphs = [None] * len(self.replicas) if graphs else None
-        dw = first
-        self._host_in = {}
-        for name in ("q_idx", "head_w", "Q", "seq_lens", "positions", "slots", "block_table",
-                     "idx_base") + (("kv_a",) if dw.kv_a is not None else ()):
-            t = getattr(dw, name)
-            self._host_in[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        self.host_out = torch.empty(dw.out.shape, dtype=dw.out.dtype, pin_memory=True)
+        names = self._INPUTS + (("kv_a",) if first.kv_a is not None else ())
+        layout, off = [], 0
+        for name in names:
+            t = getattr(first, name)
+            nbytes = t.numel() * t.element_size()
+            layout.append((name, off, nbytes, t.dtype, tuple(t.shape)))
+            off = (off + nbytes + 255) // 256 * 256
+        self._stage_bytes = off
+        self._host = torch.empty(off, dtype=torch.uint8, pin_memory=True)
+        self._host_in = {name: self._host[o:o + n].view(dt).view(shape)
+                         for name, o, n, dt, shape in layout}
+        for dw in self.replicas:
+            buf = torch.empty(off, dtype=torch.uint8, device=first.device)
+            for name, o, n, dt, shape in layout:
+                view = buf[o:o + n].view(dt).view(shape)
+                view.copy_(getattr(dw, name))
+                setattr(dw, name, view)
+            dw.stage_buf = buf
+            dw.rows = api.make_rows(dw.seq_lens, dw.block_table, wl.block_size, dw.slots,
+                                    dw.positions, shared_table=(wl.bt_stride == 0))
+        self.host_out = torch.empty(first.out.shape, dtype=first.out.dtype, pin_memory=True)
 
     @property
     def h2d_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in self._host_in.values())
+        return self._stage_bytes
 
     @property
     def d2h_bytes(self) -> int:
@@ -159,8 +179,7 @@ class DsaDecoder:
             t.copy_(torch.from_numpy(np.ascontiguousarray(src[k])))
 
     def _run(self, dw, stream=None) -> None:
-        for k, t in self._host_in.items():
-            getattr(dw, k).copy_(t, non_blocking=True)
+        dw.stage_buf.copy_(self._host, non_blocking=True)
         dw.step(stream)
         self.host_out.copy_(dw.out, non_blocking=True)
 
