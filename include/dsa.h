@@ -8,7 +8,13 @@
  *   S1 dsa_index_scores    lightning-indexer score of every visible token
  *   S2 dsa_select_topk     per-row top-k of those scores
  *   S3 dsa_mla_decode_fp8  absorbed NoPE MLA gather-attend over the selection
- * issued in that order on one stream.  Sources (spark_model documentation):
+ * issued in that order on one stream.  Around the path, for the K-token
+ * verify and the indexer's write side:
+ *      dsa_dense_mm_bf16   batched projection: up to 16 rows per sweep of a
+ *                          bf16 weight, each row bit-identical to a one-row call
+ *      dsa_indexer_write   the indexer key's LayerNorm (with bias) and its store
+ *                          at the row's device-side arena position
+ * Sources (spark_model documentation):
  * the "glm5next_dsa/layer.rs" source page (module header: decode data flow
  * and its traps; decode_k: latent write, per-row metadata, one attend for all
  * rows; attend_rows; the selection notes on a total order) and the "Struct
