@@ -168,6 +168,9 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  * A row with nothing selected gets out = 0 and lse = -inf.
  *   q   [rows][heads][latent_dim] bf16       pool [nslots][latent_dim] FP8
  *   sel [rows][topk] int32                   out  [rows][heads][latent_dim] bf16
+ * out may also be page-locked host memory mapped into the device's address
+ * space (cudaHostAlloc memory under unified addressing): the kernels store the
+ * result there directly, with no separate device-to-host copy.
  * latent_dim must be 512; heads a multiple of 16; nslots below 2^31
  * (DSA_ERR_UNSUPPORTED otherwise).  Numerics: the logits are the exact
  * products of the bf16 q and the E4M3 latent accumulated in FP32 on the

@@ -92,12 +92,14 @@ def _check(fn: str, status: int):
 _BITS16 = (torch.uint16, torch.int16, torch.bfloat16)
 
 
-def _ptr(t: torch.Tensor | None, dtype=None, name: str = "") -> int | None:
+def _ptr(t: torch.Tensor | None, dtype=None, name: str = "", host_ok: bool = False) -> int | None:
     """Device pointer of a contiguous CUDA tensor.  bf16 arguments (bit
-    patterns) may be passed as uint16, int16 or bfloat16 tensors."""
+    patterns) may be passed as uint16, int16 or bfloat16 tensors.  With
+    ``host_ok`` a pinned host tensor is accepted too (pinned memory is mapped
+    into the device's address space, so kernels write it directly)."""
     if t is None:
         return None
-    if not t.is_cuda:
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
         raise ValueError(f"{name}: expected a CUDA tensor")
     allowed = _BITS16 if dtype is torch.uint16 else (dtype,)
     if dtype is not None and t.dtype not in allowed:
@@ -171,12 +173,14 @@ def dsa_mla_decode_fp8(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: tor
                        kv_scale: float, sm_scale: float, out: torch.Tensor,
                        lse: torch.Tensor | None, workspace: torch.Tensor | None = None,
                        stream=None) -> None:
+    """``out`` may be a CUDA tensor or a pinned host tensor (written directly)."""
     lib = load()
     heads = q.shape[-2]
     st = lib.dsa_mla_decode_fp8(ctypes.byref(rows), _ptr(q, torch.uint16, "q"),
                                 _ptr(pool, torch.uint8, "pool"), pool.shape[0],
                                 _ptr(sel, torch.int32, "sel"), int(topk), heads, q.shape[-1],
-                                float(kv_scale), float(sm_scale), _ptr(out, torch.uint16, "out"),
+                                float(kv_scale), float(sm_scale),
+                                _ptr(out, torch.uint16, "out", host_ok=True),
                                 _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
                                 0 if workspace is None else workspace.numel() * workspace.element_size(),
                                 _stream(stream))

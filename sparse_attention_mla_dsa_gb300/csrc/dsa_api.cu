@@ -213,6 +213,18 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   if (heads < 16 || heads % 16 != 0 || heads > 4096) return DSA_ERR_UNSUPPORTED;
   if (topk < 1 || topk > 65536) return DSA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(out, 8)) return DSA_ERR_INVALID_ARG;
+  {
+    // out: device memory, or page-locked host memory the device reaches at
+    // the same address; anything else is refused before a kernel could touch it.
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, out) != cudaSuccess) {
+      cudaGetLastError();  // not sticky: clear it for the caller
+      return DSA_ERR_INVALID_ARG;
+    }
+    const bool on_device = a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+    const bool mapped_host = a.type == cudaMemoryTypeHost && a.devicePointer == out;
+    if (!on_device && !mapped_host) return DSA_ERR_INVALID_ARG;
+  }
   const DeviceInfo* dev = device_info();
   if (dev == nullptr) return DSA_ERR_CUDA;
   DecodeParams p{};

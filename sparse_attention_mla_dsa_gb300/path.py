@@ -7,8 +7,8 @@ index scores, S2 top-k, S3 gather-attend -- without any host synchronisation.
 
 ``DsaDecoder`` is the host-facing form: per step it copies that step's inputs
 (queries, head weights, the new latent rows, row metadata) from one pinned
-host staging buffer to the device in one copy, runs the same four calls and
-reads the attention output back into pinned host memory.
+host staging buffer to the device in one copy, runs the same four calls, and
+the gather-attend writes the attention output straight into pinned host memory.
 """
 from __future__ import annotations
 
@@ -58,6 +58,7 @@ class DeviceWorkload:
         self.lse = torch.empty((R, H), dtype=torch.float32, device=d)
         nbytes = api.dsa_workspace_bytes(R, H, wl.topk)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=d)
+        self.out_target = None      # where S3 writes; None = self.out
         self.rows = api.make_rows(self.seq_lens, self.block_table, wl.block_size, self.slots,
                                   self.positions, shared_table=(wl.bt_stride == 0))
 
@@ -69,6 +70,7 @@ class DeviceWorkload:
             t = getattr(src, name)
             setattr(self, name, None if t is None else t.clone())
         self.max_len = src.max_len
+        self.out_target = None
         wl = self.wl
         self.rows = api.make_rows(self.seq_lens, self.block_table, wl.block_size, self.slots,
                                   self.positions, shared_table=(wl.bt_stride == 0))
@@ -97,8 +99,9 @@ class DeviceWorkload:
 
     def mla_decode(self, stream=None):
         wl = self.wl
+        out = self.out if self.out_target is None else self.out_target
         api.dsa_mla_decode_fp8(self.rows, self.Q, self.pool, self.sel, wl.topk, wl.kv_scale,
-                               wl.sm_scale, self.out, self.lse, self.workspace, stream)
+                               wl.sm_scale, out, self.lse, self.workspace, stream)
 
     def step(self, stream=None):
         """One pass of the whole hot path (S0 when the workload writes, S1-S3)."""
@@ -118,12 +121,13 @@ class DsaDecoder:
 
     The caches (key arena, gate, FP8 latent pool) live on the device; each
     ``decode`` call copies the step's inputs from pinned host memory to the
-    device, runs S0-S3 and copies the attention output back.  The per-step
+    device, runs S0-S3, and the gather-attend writes the attention output into
+    pinned host memory.  The per-step
     inputs (queries, head weights, the new latent rows, row metadata) sit in
     one pinned staging buffer mirrored by one device buffer per cache replica,
     whose views the kernels read, so a step moves its inputs in one copy.
     With ``graphs=True`` (the default) the whole sequence -- the host-to-device
-    copy, the four calls and the device-to-host copy -- is captured once per
+    copy and the four calls -- is captured once per
     cache replica as a CUDA graph and replayed, so a step costs one launch;
     the buffers keep their addresses, so each replay moves the current
     contents of the pinned inputs."""
@@ -157,7 +161,12 @@ class DsaDecoder:
             dw.stage_buf = buf
             dw.rows = api.make_rows(dw.seq_lens, dw.block_table, wl.block_size, dw.slots,
                                     dw.positions, shared_table=(wl.bt_stride == 0))
+        # Pinned host memory is mapped into the device's address space: the
+        # gather-attend (or its merge) stores the output there directly, so no
+        # device-to-host copy follows the step.
         self.host_out = torch.empty(first.out.shape, dtype=first.out.dtype, pin_memory=True)
+        for dw in self.replicas:
+            dw.out_target = self.host_out
 
     @property
     def h2d_bytes(self) -> int:
@@ -180,8 +189,7 @@ class DsaDecoder:
 
     def _run(self, dw, stream=None) -> None:
         dw.stage_buf.copy_(self._host, non_blocking=True)
-        dw.step(stream)
-        self.host_out.copy_(dw.out, non_blocking=True)
+        dw.step(stream)                       # S3 writes straight into host_out
 
     def decode(self, stream=None) -> torch.Tensor:
         """Copy staged inputs in, run the path, copy the output out (async on

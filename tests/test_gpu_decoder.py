@@ -44,3 +44,28 @@ def test_graph_decoder_moves_current_inputs(dsa):
         torch.cuda.synchronize()
         assert torch.equal(got, ref.out.cpu()), f"step {step}"
     assert api.dsa_get_error(reset=True)[0] == 0
+
+
+def test_attend_refuses_an_unmapped_host_output(dsa):
+    # Pinned host memory is accepted as the output (the decoder writes there);
+    # ordinary pageable host memory is refused before any launch.
+    api, path = dsa
+    import ctypes
+    wl = workloads.scaled("tiny", len_div=4)
+    dw = path.DeviceWorkload(wl)
+    dw.step()
+    torch.cuda.synchronize()
+    pinned = torch.empty(dw.out.shape, dtype=dw.out.dtype, pin_memory=True)
+    api.dsa_mla_decode_fp8(dw.rows, dw.Q, dw.pool, dw.sel, wl.topk, wl.kv_scale, wl.sm_scale,
+                           pinned, dw.lse, dw.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(pinned, dw.out.cpu())
+    pageable = np.zeros(dw.out.numel() + 8, np.int16)
+    addr = (pageable.ctypes.data + 15) // 16 * 16
+    lib = api.load()
+    st = lib.dsa_mla_decode_fp8(ctypes.byref(dw.rows), dw.Q.data_ptr(), dw.pool.data_ptr(),
+                                dw.pool.shape[0], dw.sel.data_ptr(), wl.topk, wl.heads, 512,
+                                wl.kv_scale, wl.sm_scale, addr, None, dw.workspace.data_ptr(),
+                                dw.workspace.numel(), None)
+    assert st == 1
+    assert api.dsa_get_error(reset=True)[0] == 0
