@@ -277,6 +277,12 @@ dsa_status dsa_dense_mm_bf16(const uint16_t *a, const uint16_t *b, void *c, int3
                              int32_t n_out, int32_t k, int32_t c_fp32, void *workspace,
                              size_t workspace_bytes, void *stream);
 
+/* The number of k ranges dsa_dense_mm_bf16 splits an n_out x k weight into on
+ * a device with num_sms SMs (host arithmetic only; 0 on bad arguments).  One
+ * range when the 128-row weight tiles alone reach num_sms, else enough ranges
+ * to, each at least four 64-element blocks of k long. */
+int32_t dsa_dense_mm_splits(int32_t n_out, int32_t k, int32_t num_sms);
+
 /* Workspace bytes dsa_dense_mm_bf16 needs on the current device for a weight
  * of n_out x k (0 when it needs none or on bad arguments). */
 size_t dsa_dense_mm_workspace_bytes(int32_t n_out, int32_t k);

@@ -301,6 +301,15 @@ dsa_status dsa_indexer_write(const dsa_rows* rows, const uint16_t* k_raw, const 
   return launched(launch_indexer_write(p, static_cast<cudaStream_t>(stream)));
 }
 
+int32_t dsa_dense_mm_splits(int32_t n_out, int32_t k, int32_t num_sms) {
+  if (n_out < 1 || k < 8 || k % 8 != 0 || num_sms < 1) return 0;
+  DenseMmParams p{};
+  p.n = n_out;
+  p.k = k;
+  plan_dense_mm(p, num_sms);
+  return p.splits;
+}
+
 size_t dsa_dense_mm_workspace_bytes(int32_t n_out, int32_t k) {
   if (n_out < 1 || k < 8 || k % 8 != 0) return 0;
   const DeviceInfo* dev = device_info();

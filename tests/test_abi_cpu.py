@@ -83,3 +83,26 @@ def test_dense_mm_host_checks_without_gpu():
     assert f(None, x, x, 4, 64, 64, 0, None, 0, None) == 1        # null activations
     assert f(x, x, x, 4, 64, 64, 2, None, 0, None) == 1           # output type flag
     assert f(x + 8, x, x, 4, 64, 64, 0, None, 0, None) == 1       # misaligned activations
+
+
+def test_dense_mm_split_plan_host_arithmetic():
+    # The K split of the batched projection is fixed by (N, K, SM count) only
+    # (so a row's arithmetic never depends on how many rows share the sweep).
+    from sparse_attention_mla_dsa_gb300 import build
+    lib = ctypes.CDLL(build.build())
+    f = lib.dsa_dense_mm_splits
+    f.argtypes = [ctypes.c_int32] * 3
+    f.restype = ctypes.c_int32
+    sms = 152
+    assert f(32768, 1536, sms) == 1            # 256 weight tiles fill the SMs
+    assert f(4096, 32768, sms) == 5            # 32 tiles: ceil(152/32) ranges of 103 blocks
+    assert f(2048, 4096, sms) == 10            # 16 tiles
+    assert f(128, 4096, sms) == 16             # one tile: capped at 64 blocks / 4
+    assert f(1000, 200, sms) == 1              # 4 blocks of k: no split
+    assert f(0, 64, sms) == 0 and f(64, 12, sms) == 0 and f(64, 64, 0) == 0
+    for n, k in ((128, 4096), (300, 1536), (4096, 32768), (640, 32768), (7, 8)):
+        s = f(n, k, sms)
+        kblocks = (k + 63) // 64
+        per = (kblocks + s - 1) // s
+        assert s >= 1 and (s - 1) * per < kblocks          # no empty range
+        assert s == 1 or per >= 4                           # at least four blocks each
