@@ -207,8 +207,16 @@ __global__ void __launch_bounds__(256) dense_mm_reduce_kernel(const DenseMmParam
   const int64_t total = static_cast<int64_t>(p.m) * p.n;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= total) return;
-  float s = p.part[i];
-  for (int r = 1; r < p.splits; ++r) s += p.part[r * total + i];
+  // Eight partials in flight per round trip, added in range order.
+  float s = 0.0f;
+  for (int r0 = 0; r0 < p.splits; r0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = r0 + u < p.splits ? p.part[(r0 + u) * total + i] : 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (r0 + u < p.splits) s = (r0 + u == 0) ? v[u] : s + v[u];
+  }
   if (p.c_fp32)
     static_cast<float*>(p.c)[i] = s;
   else
