@@ -155,3 +155,56 @@ def test_graph_replay_writes_the_next_position(api):
     assert not np.all(first == np.uint16(SENTINEL))
     assert np.array_equal(arena[15], first) and np.array_equal(arena[16], first)
     assert np.all(np.delete(arena, [14, 15, 16], axis=0) == np.uint16(SENTINEL))
+
+
+def test_rewind_after_a_rejected_verify(api, oracle):
+    # "glm5next_dsa/layer.rs", the lockstep notes: after a speculative-verify
+    # reject the rows past the accepted prefix are unreachable (the selector
+    # reads [0, len)) and the next write at seq_len - 1 overwrites them.  Here:
+    # four draft keys written by one K-row call, one accepted, the next token
+    # written at the first rejected position, then the indexer over the
+    # rolled-back length must equal the oracle on the arena as it stands.
+    from tests import parity
+    rng = np.random.default_rng(31)
+    D, H, T, L = 128, 32, 2048, 1000
+    arena_np = np.full((T, D), SENTINEL, np.int16)
+    gates_np = np.full(T, SENTINEL, np.int16)
+    arena_np[:L] = _bf16(rng.standard_normal((L, D))).view(np.int16)
+    gates_np[:L] = _bf16(1.0 / (1.0 + np.exp(-rng.standard_normal(L)))).view(np.int16)
+    idx_k = torch.from_numpy(arena_np).cuda()
+    idx_gate = torch.from_numpy(gates_np).cuda()
+    ln_w = torch.from_numpy(_bf16(1.0 + 0.1 * rng.standard_normal(D)).view(np.int16)).cuda()
+    ln_b = torch.from_numpy(_bf16(0.1 * rng.standard_normal(D)).view(np.int16)).cuda()
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+    # Verify: four draft rows at positions L .. L+3 (seq_lens L+1 .. L+4).
+    drafts = _bf16(rng.standard_normal((4, D)))
+    rows4, keep4 = _rows(api, [L + 1, L + 2, L + 3, L + 4], [L, L + 1, L + 2, L + 3])
+    base4 = torch.zeros(4, dtype=torch.int64, device="cuda")
+    api.dsa_indexer_write(rows4, dev16(drafts), ln_w, ln_b, 1e-6, base4, idx_k, idx_gate,
+                          dev16(_bf16(np.full(4, 0.75))))
+    torch.cuda.synchronize()
+    after_verify = idx_k.cpu().numpy().copy()
+    # One draft accepted: the next token is position L+1, seq_len L+2.
+    nxt = _bf16(rng.standard_normal((1, D)))
+    rows1, keep1 = _rows(api, [L + 2], [L + 1])
+    base1 = torch.zeros(1, dtype=torch.int64, device="cuda")
+    api.dsa_indexer_write(rows1, dev16(nxt), ln_w, ln_b, 1e-6, base1, idx_k, idx_gate,
+                          dev16(_bf16([0.5])))
+    torch.cuda.synchronize()
+    arena = idx_k.cpu().numpy()
+    assert np.array_equal(arena[L], after_verify[L])                 # the accepted draft stays
+    assert not np.array_equal(arena[L + 1], after_verify[L + 1])     # the rejected one is replaced
+    assert np.array_equal(arena[L + 2:L + 4], after_verify[L + 2:L + 4])  # stale, past the length
+
+    # The selector over [0, L+2) on the rolled-back state.
+    q = rng.standard_normal((1, H, D)).astype(np.float32)
+    w = (rng.standard_normal((1, H)) * H ** -0.5).astype(np.float32)
+    scores = torch.full((1, L + 2), float("nan"), dtype=torch.float32, device="cuda")
+    api.dsa_index_scores(rows1, torch.from_numpy(q).cuda(), torch.from_numpy(w).cuda(), idx_k,
+                         idx_gate, base1, 1, L + 2, scores)
+    torch.cuda.synchronize()
+    assert api.dsa_get_error(reset=True)[0] == 0
+    s, A, M = oracle.index_scores_row(q[0], w[0], arena.view(np.uint16),
+                                      idx_gate.cpu().numpy().view(np.uint16), L + 2)
+    parity.assert_scores(scores.cpu().numpy()[0], s, A, M, "rewound row")
