@@ -55,6 +55,9 @@ PROJ_METRIC = ("K-token verify projection rows/s (q_a, absorbed q_b, kv_a, absor
                "64 heads; one bf16 weight sweep per step); % HBM roofline")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+TRAFFIC_NOTE = ("DRAM read+write bytes per launch of the stage's kernels from one ncu capture "
+                "with --cache-control none (the merge's reads of the split partials are L2 hits, "
+                "as in the chained step); null when the kernel source changed since the capture")
 
 
 def _args():
@@ -66,6 +69,8 @@ def _args():
     ap.add_argument("--workload", default="single", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the batched / verify / long lines of the default run")
     ap.add_argument("--eager", action="store_true", help="launch every step eagerly (no CUDA graph)")
     return ap.parse_args()
 
@@ -191,6 +196,117 @@ def stage_bytes(wl):
 
 
 # --------------------------------------------------------------------------- our arm
+SECONDARY = ("batched", "verify", "long")
+
+
+def config_of(name, wl):
+    """The workload's description; both arms print exactly this."""
+    return {"workload": DESCRIPTIONS[name], "rows_per_step": wl.rows,
+            "algorithmic_bytes_per_step": wl.algorithmic_bytes()}
+
+
+def time_path(wl, dev, K, warmup, eager, world, api, path, shard):
+    """Time K steps of the whole path on resident inputs.
+
+    Steps rotate over enough input replicas (distinct device addresses) that
+    one rotation touches more than 2x the L2.  The K timed steps are one CUDA
+    graph of K consecutive steps (step s on replica s % n), the form a model
+    gives a decode step that runs the path once per layer: the kernels of
+    consecutive steps are chained by programmatic dependent launch like the
+    stages inside a step.  A second pass replays one graph per step with
+    timing events between the stages, for the per-stage breakdown (the event
+    nodes serialise the chain, so the stages add up to more than a step)."""
+    import torch
+    sb, _ = stage_bytes(wl)
+    alg_bytes = wl.algorithmic_bytes()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    first = path.DeviceWorkload(wl, dev)
+    n_rep = max(2, min(64, math.ceil(2.0 * l2 / max(alg_bytes, 1)) + 1))
+    reps = [first] + [first.clone() for _ in range(n_rep - 1)]
+    stages = (["latent_write"] if wl.has_write else []) + ["index_scores", "select_topk", "mla_decode"]
+
+    def one_step(dw, evs=None):
+        s = torch.cuda.current_stream()
+        calls = ([dw.latent_write] if wl.has_write else []) + [dw.index_scores, dw.select_topk,
+                                                               dw.mla_decode]
+        if evs is not None:
+            evs[0].record(s)
+        for j, call in enumerate(calls):
+            call()
+            if evs is not None:
+                evs[j + 1].record(s)
+
+    for i in range(max(3, warmup)):
+        one_step(reps[i % n_rep])
+    torch.cuda.synchronize()
+    code, row, _ = api.dsa_get_error(reset=True)
+    if code != 0:
+        raise RuntimeError(f"device error during warm-up: {api.DEVERR.get(code)} row {row}")
+
+    run_graph, staged, mode = None, [], "eager"
+    if not eager:
+        try:
+            for dw in reps[:min(K, n_rep)]:
+                evs = [torch.cuda.Event(enable_timing=True, external=True)
+                       for _ in range(len(stages) + 1)]
+                gs = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gs):
+                    one_step(dw, evs)
+                staged.append((gs, evs))
+            run_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(run_graph):
+                for i in range(K):
+                    one_step(reps[i % n_rep])
+            run_graph.replay()                     # untimed warm-up of the timed graph
+            torch.cuda.synchronize()
+            mode = f"one CUDA graph of the {K} timed steps"
+        except (TypeError, RuntimeError) as ex:
+            run_graph, staged = None, []
+            torch.cuda.synchronize()
+            print(f"cuda graph capture unavailable ({ex}); timing eager launches", file=sys.stderr)
+
+    stream = torch.cuda.current_stream()
+    eager_evs = None if run_graph is not None else [
+        [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        start.record(stream)
+        if run_graph is not None:
+            run_graph.replay()
+        else:
+            for i in range(K):
+                one_step(reps[i % n_rep], eager_evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        if staged:  # second pass: per-stage events (same rotation, same replicas)
+            for i in range(K):
+                staged[i % len(staged)][0].replay()
+            torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = shard.max_over_ranks(start.elapsed_time(end))
+    ev_sets = [evs for _, evs in staged] if staged else eager_evs
+    stage_ms = {st: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev_sets)
+                for j, st in enumerate(stages)}
+    code, row, _ = api.dsa_get_error(reset=True)
+    if code != 0:
+        raise RuntimeError(f"device error during the timed steps: {api.DEVERR.get(code)} row {row}")
+    peak, peak_kind = _peaks()
+    dominant = max(stages, key=lambda st: stage_ms[st])
+    ach = sb[dominant] / (stage_ms[dominant] / 1e3) / 1e9
+    # The gather-attend is one kernel, plus a combine kernel when a row's
+    # selection is cut into more than one split.
+    launches = len(stages) + (1 if api.decode_splits(wl.heads, wl.topk) > 1 else 0)
+    del run_graph, staged, reps
+    return {"elapsed_ms": elapsed_ms, "stage_ms": stage_ms, "dominant": dominant,
+            "achieved": ach, "peak": peak, "peak_kind": peak_kind, "stage_bytes": sb,
+            "alg_bytes": alg_bytes, "n_rep": n_rep, "l2": l2, "mode": mode,
+            "launches_per_step": launches, "clocks": clk.summary()}
+
+
 def run_ours(args):
     import torch
     rank, world, local = _dist()
@@ -210,129 +326,31 @@ def run_ours(args):
         torch.distributed.barrier()
     from sparse_attention_mla_dsa_gb300 import api, path, shard, workloads
 
-    wl = workloads.named(args.workload)
-    sb, key_tokens = stage_bytes(wl)
-    alg_bytes = wl.algorithmic_bytes()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    first = path.DeviceWorkload(wl, dev)
-    # Enough replicas that one rotation moves more than 2x L2 of inputs.
-    touched = max(alg_bytes, 1)
-    n_rep = max(2, min(64, math.ceil(2.0 * l2 / touched) + 1))
-    reps = [first] + [first.clone() for _ in range(n_rep - 1)]
-    stages = (["latent_write"] if wl.has_write else []) + ["index_scores", "select_topk", "mla_decode"]
-
-    def one_step(dw, evs=None):
-        s = torch.cuda.current_stream()
-        if evs is not None:
-            evs[0].record(s)
-        k = 1
-        if wl.has_write:
-            dw.latent_write()
-            if evs is not None:
-                evs[k].record(s)
-                k += 1
-        dw.index_scores()
-        if evs is not None:
-            evs[k].record(s)
-            k += 1
-        dw.select_topk()
-        if evs is not None:
-            evs[k].record(s)
-            k += 1
-        dw.mla_decode()
-        if evs is not None:
-            evs[k].record(s)
-
-    for i in range(max(3, args.warmup)):
-        one_step(reps[i % n_rep])
-    torch.cuda.synchronize()
-    code, row, _ = api.dsa_get_error(reset=True)
-    if code != 0:
-        raise RuntimeError(f"device error during warm-up: {api.DEVERR.get(code)} row {row}")
-
-    # Per input replica two CUDA graphs of one whole step: a plain one for the
-    # timed steps (kernels chained by programmatic dependent launch) and one
-    # with timing events between the stages, replayed in a second timed pass
-    # for the per-kernel breakdown (event nodes serialise the chain).
-    graphs, staged, mode = [], [], "eager"
-    if not args.eager:
-        try:
-            for dw in reps:
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    one_step(dw)
-                graphs.append(g)
-                evs = [torch.cuda.Event(enable_timing=True, external=True)
-                       for _ in range(len(stages) + 1)]
-                gs = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gs):
-                    one_step(dw, evs)
-                staged.append((gs, evs))
-            for g in graphs:
-                g.replay()
-            torch.cuda.synchronize()
-            mode = "cuda-graph"
-        except (TypeError, RuntimeError) as ex:
-            graphs, staged = [], []
-            torch.cuda.synchronize()
-            print(f"cuda graph capture unavailable ({ex}); timing eager launches", file=sys.stderr)
-
     K = args.steps
-    stream = torch.cuda.current_stream()
-    eager_evs = None if graphs else [[torch.cuda.Event(enable_timing=True)
-                                      for _ in range(len(stages) + 1)] for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        start.record(stream)
-        for i in range(K):
-            if graphs:
-                graphs[i % n_rep].replay()
-            else:
-                one_step(reps[i % n_rep], eager_evs[i])
-        end.record(stream)
-        torch.cuda.synchronize()
-        if staged:  # second pass: per-stage events (same rotation, same replicas)
-            for i in range(K):
-                staged[i % n_rep][0].replay()
-            torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    elapsed_ms = start.elapsed_time(end)
-    # only the replicas the K steps replayed hold recorded events
-    ev_sets = [evs for _, evs in staged[:min(K, n_rep)]] if staged else eager_evs
-    stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev_sets)
-                for j, s in enumerate(stages)}
-    elapsed_ms = shard.max_over_ranks(elapsed_ms)
-    code, row, _ = api.dsa_get_error(reset=True)
-    if code != 0:
-        raise RuntimeError(f"device error during the timed steps: {api.DEVERR.get(code)} row {row}")
-
+    wl = workloads.named(args.workload)
+    t = time_path(wl, dev, K, args.warmup, args.eager, world, api, path, shard)
+    elapsed_ms, stage_ms, dominant = t["elapsed_ms"], t["stage_ms"], t["dominant"]
     value = K * wl.rows * world / (elapsed_ms / 1e3)
-    peak, peak_kind = _peaks()
-    dominant = max(stages, key=lambda s: stage_ms[s])
-    ach = sb[dominant] / (stage_ms[dominant] / 1e3) / 1e9
-    traffic = _traffic(args.workload, dominant)
-    roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
-                "traffic": traffic, "algorithmic_bytes": sb[dominant],
+    peak = t["peak"]
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(t["achieved"], 1),
+                "peak": peak, "unit": "GB/s", "frac": round(t["achieved"] / peak, 4),
+                "peak_source": t["peak_kind"], "traffic": _traffic(args.workload, dominant),
+                "traffic_note": TRAFFIC_NOTE, "algorithmic_bytes": t["stage_bytes"][dominant],
                 "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
-                "path_frac": round(alg_bytes / (elapsed_ms / K / 1e3) / 1e9 / peak, 4)}
+                "path_frac": round(t["alg_bytes"] / (elapsed_ms / K / 1e3) / 1e9 / peak, 4)}
 
     e2e = None
     if not args.no_e2e:
-        del graphs, staged, reps
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-        dec = path.DsaDecoder(wl, dev, replicas=n_rep)
+        dec = path.DsaDecoder(wl, dev, replicas=t["n_rep"])
         dec.stage(wl)
         # Every replica's step graph is captured on its first use: warm up over
         # all of them so that no capture falls inside the timed steps.
-        for i in range(max(3, args.warmup, n_rep)):
+        for i in range(max(3, args.warmup, t["n_rep"])):
             dec.decode()
         torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             torch.distributed.barrier()
@@ -342,31 +360,50 @@ def run_ours(args):
             dec.decode()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        ems = shard.max_over_ranks(ems)
+        ems = shard.max_over_ranks(e0.elapsed_time(e1))
         e2e = {"value": round(K * wl.rows * world / (ems / 1e3), 2), "unit": UNIT,
-               "h2d_bytes_per_step": dec.h2d_bytes, "d2h_bytes_per_step": dec.d2h_bytes}
+               "h2d_bytes_per_step": dec.h2d_bytes, "d2h_bytes_per_step": dec.d2h_bytes,
+               "launch": "one CUDA graph per step: pinned H2D copy of the step's inputs, "
+                         "the path, the output stored into pinned host memory"}
+        del dec
+        torch.cuda.empty_cache()
+
+    secondary = None
+    launches = K * t["launches_per_step"]
+    if args.workload == "single" and not args.no_secondary:
+        secondary = {}
+        for name in SECONDARY:
+            w2 = workloads.named(name)
+            t2 = time_path(w2, dev, K, args.warmup, args.eager, world, api, path, shard)
+            ms = t2["elapsed_ms"] / K
+            secondary[name] = {
+                "config": config_of(name, w2),
+                "value": round(K * w2.rows * world / (t2["elapsed_ms"] / 1e3), 2), "unit": UNIT,
+                "ms_per_step": round(ms, 5),
+                "path_frac": round(t2["alg_bytes"] / (ms / 1e3) / 1e9 / t2["peak"], 4),
+                "stage_ms": {k: round(v, 5) for k, v in t2["stage_ms"].items()},
+                "dominant": t2["dominant"], "dominant_frac": round(t2["achieved"] / t2["peak"], 4),
+                "traffic": _traffic(name, t2["dominant"]), "clocks": t2["clocks"]}
+            launches += K * t2["launches_per_step"]
+            del w2
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, rows_target=None)
 
-    # The gather-attend is one kernel, plus a combine kernel when a row's
-    # selection is cut into more than one split.
-    launches_per_step = len(stages) + (1 if api.decode_splits(wl.heads, wl.topk) > 1 else 0)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": wl.rows,
-                   "algorithmic_bytes_per_step": alg_bytes,
-                   "l2": f"rotating {n_rep} input replicas at distinct addresses "
-                         f"({n_rep * alg_bytes / 1e6:.0f} MB of touched inputs per rotation, "
-                         f"L2 {l2 / 1e6:.0f} MB)",
+        "config": config_of(args.workload, wl),
+        "timing": {"l2": f"rotating {t['n_rep']} input replicas at distinct addresses "
+                         f"({t['n_rep'] * t['alg_bytes'] / 1e6:.0f} MB of touched inputs per "
+                         f"rotation, L2 {t['l2'] / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                   "launch": mode},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": K * launches_per_step, "clocks": clk.summary(),
+                   "launch": t["mode"]},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "secondary": secondary,
+        "gpu_launches": launches, "clocks": t["clocks"],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -553,11 +590,11 @@ def run_projections(args):
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": pw.rows,
-                   "algorithmic_bytes_per_step": alg,
-                   "l2": f"rotating {n_rep} weight replicas ({n_rep * wbytes / 1e6:.0f} MB per "
+                   "algorithmic_bytes_per_step": alg},
+        "timing": {"l2": f"rotating {n_rep} weight replicas ({n_rep * wbytes / 1e6:.0f} MB per "
                          f"rotation, L2 {l2 / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                   "launch": "cuda-graph"},
+                   "launch": "one CUDA graph per step"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": K * launches, "clocks": clk.summary(),
     }
@@ -587,7 +624,8 @@ def run_projections_reference(args):
             "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": round(el / K * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": pw.rows},
+            "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": pw.rows,
+                       "algorithmic_bytes_per_step": pw.algorithmic_bytes()},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -733,9 +771,10 @@ def run_indexer_write(args):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": IW_ROWS,
-                   "algorithmic_bytes_per_step": alg,
-                   "l2": f"flushed before every step (a {2 * l2 / 1e6:.0f} MB buffer written)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU", "launch": "cuda-graph"},
+                   "algorithmic_bytes_per_step": alg},
+        "timing": {"l2": f"flushed before every step (a {2 * l2 / 1e6:.0f} MB buffer written)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "launch": "one CUDA graph per step"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K * launches,
         "clocks": clk.summary(),
     }
@@ -774,7 +813,8 @@ def run_indexer_write_reference(args):
     line = {"impl": "reference", "metric": IW_METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(IW_ROWS / v * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": IW_ROWS},
+            "data": "synthetic", "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": IW_ROWS,
+                                            "algorithmic_bytes_per_step": _iw_bytes()},
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} steps x {IW_ROWS} rows over {cores} threads"},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -824,12 +864,14 @@ def run_reference(args):
     o.run_path_rows(wl, rows=rows, threads=cores)
     el = time.perf_counter() - t0
     value = len(rows) / el
-    sample = (f"{K} steps x {rows_per_step} rows of the workload, rows over {cores} threads")
+    sample = (f"{K} steps, each a bounded sample of {rows_per_step} of the workload's {wl.rows} "
+              f"rows (index over the full context, full-sort top-k, gather-attend), rows over "
+              f"{cores} threads")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": round(el / K * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": rows_per_step},
+            "config": config_of(args.workload, wl),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 #define DSA_LATENT_DIM 512
 
 typedef enum dsa_status {
@@ -135,7 +135,8 @@ dsa_status dsa_latent_write(const dsa_rows *rows, const uint16_t *kv_a, const ui
 dsa_status dsa_index_scores(const dsa_rows *rows, const float *q_idx, const float *head_w,
                             const uint16_t *idx_k, const uint16_t *idx_gate, int64_t idx_tokens,
                             const int64_t *idx_base, int32_t index_heads, int32_t index_dim,
-                            int32_t rows_per_seq, int32_t max_len, float *scores, void *stream);
+                            int32_t rows_per_seq, int32_t max_len, float *scores,
+                            void *stream);
 
 /*
  * S2 -- per-row top-k ("glm5next_dsa/layer.rs", notes on batch_select_enabled
@@ -147,12 +148,10 @@ dsa_status dsa_index_scores(const dsa_rows *rows, const float *q_idx, const floa
  *   scores [rows][max_len] fp32 (as written by dsa_index_scores)
  *   sel    [rows][topk] int32 (output)
  * topk in [1, 65536]; max_len up to about 390k tokens (a row is held in
- * shared memory by a cluster of up to 8 CTAs).  No workspace is used at
- * present; pass the same workspace as to dsa_mla_decode_fp8 (or NULL / 0).
+ * shared memory by a cluster of up to 8 CTAs).  No workspace.
  */
 dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t max_len,
-                           int32_t topk, int32_t *sel, void *workspace, size_t workspace_bytes,
-                           void *stream);
+                           int32_t topk, int32_t *sel, void *stream);
 
 /*
  * S3 -- absorbed NoPE MLA gather-attend over the selection
@@ -191,23 +190,29 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uin
                               void *stream);
 
 /*
- * S3 for callers that cannot allocate device memory where they run the
- * attend (inside CUDA-graph stream capture, under another allocator they may
- * not call, or on a serving path that must not take cudaMalloc's device
- * synchronisation).  No counterpart on the pages: it is dsa_mla_decode_fp8
- * with the split partials kept in a device array inside the library instead
- * of a caller workspace.  It allocates nothing and calls no allocating routine.
+ * S3 for callers that cannot allocate device memory at the point where they
+ * run the attend: code that must not take cudaMalloc's implicit device
+ * synchronisation on a latency-bound decode path, and code whose device
+ * memory belongs to an allocator it may not call (an embedding runtime or a
+ * host framework that owns every allocation).  No counterpart on the pages:
+ * it is dsa_mla_decode_fp8 with the split partials kept in a device array
+ * inside the library instead of a caller workspace.  It allocates nothing and
+ * calls no allocating routine.
  *   - Limit: dsa_noalloc_scratch_bytes(rows, heads, topk) must not exceed
  *     DSA_NOALLOC_SCRATCH_BYTES (32 MiB), else DSA_ERR_UNSUPPORTED and
  *     nothing is launched.  Every GPU that loads the library holds that
  *     array until the process exits.
- *   - The first call on a device looks the array's device address up
- *     (once per device, that device current); make that first call before
- *     any stream capture.
+ *   - Set-up: the first call on a device looks the array's device address up
+ *     (once per device, with that device current) and keeps it for the life
+ *     of the process; make that first call before any stream capture.  The
+ *     address belongs to the device's primary context: after
+ *     cudaDeviceReset, or under another context on the same device, it is
+ *     stale and this entry point must not be used.
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero).  Calls whose work overlaps on
  *     the GPU (other streams, other threads) race on it: serialise them.
- * Other arguments, results and errors are those of dsa_mla_decode_fp8.
+ * Other arguments, results and errors are those of dsa_mla_decode_fp8, and
+ * the results are bit-identical to that entry point's.
  */
 #define DSA_NOALLOC_SCRATCH_BYTES (32u << 20)
 dsa_status dsa_mla_decode_fp8_noalloc(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,

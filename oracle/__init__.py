@@ -77,7 +77,7 @@ def _load():
             lib.dsa_oracle_select_topk_row.argtypes = [i64, i32, P, P]
             lib.dsa_oracle_select_topk_row.restype = i32
             lib.dsa_oracle_mla_decode_row.argtypes = [i32, i32, P, P, i64, P, i32, i32, i64,
-                                                      P, i32, f32, f32, P, P]
+                                                      P, i32, f32, f32, P, P, P]
             lib.dsa_oracle_mla_decode_row.restype = i32
             lib.dsa_oracle_dense_mla_row.argtypes = [i32, i32, P, P, i64, P, i32, i32, i64,
                                                      f32, f32, P, P]
@@ -184,9 +184,12 @@ def select_topk_row(scores: np.ndarray, length: int, topk: int) -> np.ndarray:
 
 # --------------------------------------------------------------------------- S3
 def mla_decode_row(Q: np.ndarray, pool: np.ndarray, bt_row: np.ndarray, block_size: int,
-                   seq_len: int, sel_row: np.ndarray, kv_scale: float, sm_scale: float):
+                   seq_len: int, sel_row: np.ndarray, kv_scale: float, sm_scale: float,
+                   with_zmag: bool = False):
     """Gather-attend of one row.  Q [H, 512] bf16 bits, pool [nslots, 512] u8,
-    bt_row [max_blocks] i32, sel_row [K] i32.  Returns (out f64[H,512], lse f64[H])."""
+    bt_row [max_blocks] i32, sel_row [K] i32.  Returns (out f64[H,512], lse f64[H]),
+    plus zmag f64[H] (max over the selection of |sm_scale| sum_c |Q_c Khat_c|,
+    the logits' conditioning scale) when ``with_zmag``."""
     Q = _c(Q, np.uint16)
     pool = _c(pool, np.uint8)
     bt_row = _c(bt_row, np.int32)
@@ -194,13 +197,15 @@ def mla_decode_row(Q: np.ndarray, pool: np.ndarray, bt_row: np.ndarray, block_si
     heads, dim = Q.shape
     out = np.zeros((heads, dim), np.float64)
     lse = np.zeros(heads, np.float64)
+    zmag = np.zeros(heads, np.float64) if with_zmag else None
     rc = _load().dsa_oracle_mla_decode_row(heads, dim, _ptr(Q), _ptr(pool), pool.shape[0],
                                            _ptr(bt_row), bt_row.shape[0], int(block_size),
                                            int(seq_len), _ptr(sel_row), sel_row.shape[0],
-                                           float(kv_scale), float(sm_scale), _ptr(out), _ptr(lse))
+                                           float(kv_scale), float(sm_scale), _ptr(out), _ptr(lse),
+                                           _ptr(zmag))
     if rc != 0:
         raise ValueError("oracle: a selected index is outside the row's visible range or table")
-    return out, lse
+    return (out, lse, zmag) if with_zmag else (out, lse)
 
 
 def dense_mla_row(Q: np.ndarray, pool: np.ndarray, bt_row: np.ndarray, block_size: int,

@@ -229,7 +229,7 @@ int dsa_oracle_mla_decode_row(int heads, int dim, const uint16_t *Q,
                               const int32_t *bt, int max_blocks, int block_size,
                               int64_t seq_len, const int32_t *sel, int topk,
                               float kv_scale, float sm_scale,
-                              double *out, double *lse)
+                              double *out, double *lse, double *zmag)
 {
     /* the selected, dequantised latent rows */
     int n = 0;
@@ -255,17 +255,27 @@ int dsa_oracle_mla_decode_row(int heads, int dim, const uint16_t *Q,
             o[c] = 0.0;
         if (n == 0) {
             lse[h] = -INFINITY;
+            if (zmag)
+                zmag[h] = 0.0;
             continue;
         }
         double m = -INFINITY;
+        double mag_max = 0.0;
         for (int j = 0; j < n; ++j) {
-            double dot = 0.0;
-            for (int c = 0; c < dim; ++c)
-                dot += dsa_oracle_bf16_value(Q[(size_t)h * dim + c]) * khat[(size_t)j * dim + c];
+            double dot = 0.0, mag = 0.0;
+            for (int c = 0; c < dim; ++c) {
+                const double term = dsa_oracle_bf16_value(Q[(size_t)h * dim + c]) * khat[(size_t)j * dim + c];
+                dot += term;
+                mag += fabs(term);
+            }
             z[j] = (double)sm_scale * dot;
             if (z[j] > m)
                 m = z[j];
+            if (fabs((double)sm_scale) * mag > mag_max)
+                mag_max = fabs((double)sm_scale) * mag;
         }
+        if (zmag)
+            zmag[h] = mag_max;
         double denom = 0.0;
         for (int j = 0; j < n; ++j)
             denom += exp(z[j] - m);

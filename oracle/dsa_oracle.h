@@ -83,14 +83,17 @@ int dsa_oracle_select_topk_row(int64_t len, int topk, const double *scores, int3
  *   p_hj    = softmax_j(z_hj) over the selected j only
  *   out[h]  = sum_j p_hj * Khat_j ;  lse[h] = log sum_j exp(z_hj)
  * Entries of sel equal to -1 are padding and are skipped.  With nothing
- * selected, out = 0 and lse = -inf.  Returns 0, or -1 if an entry is outside
- * [0, seq_len), or maps outside the table or the pool. */
+ * selected, out = 0 and lse = -inf.  zmag (optional): [heads], the largest
+ * over the selected j of |sm_scale| * sum_c |Q[h][c] * Khat_j[c]|, the size of
+ * the terms a logit sums (the conditioning scale of z and lse; 0 when nothing
+ * is selected).  Returns 0, or -1 if an entry is outside [0, seq_len), or
+ * maps outside the table or the pool. */
 int dsa_oracle_mla_decode_row(int heads, int dim, const uint16_t *Q,
                               const uint8_t *pool, int64_t nslots,
                               const int32_t *bt, int max_blocks, int block_size,
                               int64_t seq_len, const int32_t *sel, int topk,
                               float kv_scale, float sm_scale,
-                              double *out, double *lse);
+                              double *out, double *lse, double *zmag);
 
 /* Dense MLA attention of one row over every token 0..seq_len-1, written
  * independently of the gather path (a full logits matrix, then a two-pass

@@ -57,7 +57,7 @@ def load() -> ctypes.CDLL:
     sig = {
         "dsa_latent_write": [RP, P, P, P, i64, i32, f32, f32, P],
         "dsa_index_scores": [RP, P, P, P, P, i64, P, i32, i32, i32, i32, P, P],
-        "dsa_select_topk": [RP, P, i32, i32, P, P, sz, P],
+        "dsa_select_topk": [RP, P, i32, i32, P, P],
         "dsa_mla_decode_fp8": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, sz, P],
         "dsa_mla_decode_fp8_noalloc": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P],
         "dsa_get_error": [P, P, P, i32],
@@ -159,13 +159,10 @@ def dsa_index_scores(rows: Rows, q_idx: torch.Tensor, head_w: torch.Tensor, idx_
 
 
 def dsa_select_topk(rows: Rows, scores: torch.Tensor, max_len: int, topk: int, sel: torch.Tensor,
-                    workspace: torch.Tensor | None = None, stream=None) -> None:
+                    stream=None) -> None:
     lib = load()
-    ws = _ptr(workspace, None, "workspace")
     st = lib.dsa_select_topk(ctypes.byref(rows), _ptr(scores, torch.float32, "scores"), int(max_len),
-                             int(topk), _ptr(sel, torch.int32, "sel"), ws,
-                             0 if workspace is None else workspace.numel() * workspace.element_size(),
-                             _stream(stream))
+                             int(topk), _ptr(sel, torch.int32, "sel"), _stream(stream))
     _check("dsa_select_topk", st)
 
 
@@ -191,9 +188,11 @@ def dsa_mla_decode_fp8_noalloc(rows: Rows, q: torch.Tensor, pool: torch.Tensor, 
                                topk: int, kv_scale: float, sm_scale: float, out: torch.Tensor,
                                lse: torch.Tensor | None, stream=None) -> None:
     """dsa_mla_decode_fp8 for callers that cannot allocate device memory where
-    they run the attend: the split partials live in the library's own device
-    array (see include/dsa.h for its size limit, the first-call set-up and the
-    no-overlap rule)."""
+    they run the attend (a decode loop that must not take cudaMalloc's device
+    synchronisation, or memory owned by an allocator the caller may not call):
+    the split partials live in the library's own device array (see
+    include/dsa.h for its size limit, the first-call set-up and the rule that
+    overlapping calls race)."""
     lib = load()
     heads = q.shape[-2]
     st = lib.dsa_mla_decode_fp8_noalloc(ctypes.byref(rows), _ptr(q, torch.uint16, "q"),

@@ -114,7 +114,8 @@ dsa_status dsa_latent_write(const dsa_rows* rows, const uint16_t* kv_a, const ui
 dsa_status dsa_index_scores(const dsa_rows* rows, const float* q_idx, const float* head_w,
                             const uint16_t* idx_k, const uint16_t* idx_gate, int64_t idx_tokens,
                             const int64_t* idx_base, int32_t index_heads, int32_t index_dim,
-                            int32_t rows_per_seq, int32_t max_len, float* scores, void* stream) {
+                            int32_t rows_per_seq, int32_t max_len, float* scores,
+                            void* stream) {
   dsa_status st = check_rows(rows, false);
   if (st != DSA_OK) return st;
   if (q_idx == nullptr || head_w == nullptr || idx_k == nullptr || idx_gate == nullptr ||
@@ -177,10 +178,7 @@ dsa_status dsa_index_scores(const dsa_rows* rows, const float* q_idx, const floa
 }
 
 dsa_status dsa_select_topk(const dsa_rows* rows, const float* scores, int32_t max_len,
-                           int32_t topk, int32_t* sel, void* workspace, size_t workspace_bytes,
-                           void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
+                           int32_t topk, int32_t* sel, void* stream) {
   dsa_status st = check_rows(rows, false);
   if (st != DSA_OK) return st;
   if (scores == nullptr || sel == nullptr || max_len < 0) return DSA_ERR_INVALID_ARG;

@@ -22,6 +22,13 @@ __device__ __forceinline__ void record_error(int* err, int code, int row) {
   atomicAdd(&err[2], 1);
 }
 
+// Order-preserving key of a float score: a larger score gives a larger
+// unsigned key; -0.0 is folded onto +0.0 first.  Scores must not be NaN.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // ------------------------------------------------------------------ timers / waits
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -106,6 +113,14 @@ __device__ __forceinline__ float4 ld_dep_f4(const float4* p) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint4 ld_dep_u4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void grid_dep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -119,6 +134,21 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// L2 prefetches.  They move no data into the SM and complete on nothing, so
+// they may be issued before grid_dep_wait(): L2 is where every write of the
+// device lands, so a later load after the wait still sees the newest value.
+// One box of a tiled tensor (same coordinates as a load):
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+// The 128-byte line holding `p`:
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
 // 2-D tiled load of one box into shared memory, completing on `bar`.

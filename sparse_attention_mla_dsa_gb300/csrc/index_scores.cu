@@ -92,17 +92,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r0 = seq_row0 + sub * p.sub_rows;
   const int nrows = min(p.sub_rows, seq_row0 + p.rows_per_seq - r0);
   const int nreal = nrows * p.heads;
+  const int t_begin = blockIdx.y * p.chunk_tiles;
+  const int stages = p.stages;
+  const float* qsrc = p.q_idx + static_cast<int64_t>(r0) * p.heads * D;
+
+  // ---------------------------------------------------------------- before the wait
+  // Every input here may be the output of the kernel before (the key arena
+  // and gates of an indexer write, q and the head weights of a projection,
+  // row metadata written on the device), so nothing is loaded before
+  // grid_dep_wait().  What overlaps the kernel before: barrier set-up, the
+  // tensor map, and L2 prefetches of this CTA's first key tiles and of its q
+  // rows (a prefetch only warms L2, where the device's writes land, so it
+  // cannot make a later load return a stale value; the arena base used for
+  // the prefetch address may be stale, which only wastes the prefetch).
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&ctl->tfull[a], 1);
+      mbar_init(&ctl->tempty[a], 4);
+    }
+    mbar_init(&ctl->drain, 1);
+    fence_mbar_init();
+    tma_prefetch_map(&kmap);
+    const int64_t base_hint = *reinterpret_cast<const volatile int64_t*>(p.idx_base + seq_row0);
+    for (int i = 0; i < min(stages, p.chunk_tiles); ++i) {
+      const int64_t y = base_hint + static_cast<int64_t>(t_begin + i) * kTileM;
+      if (y >= 0 && y < p.idx_tokens)
+#pragma unroll
+        for (int sb = 0; sb < kSub; ++sb) tma_prefetch_l2_2d(&kmap, sb * 64, static_cast<int32_t>(y));
+    }
+  }
+  for (int off = threadIdx.x * 32; off < nreal * D; off += kThreads * 32)
+    prefetch_l2(qsrc + off);  // 128-byte lines
+  grid_dep_wait();
 
   // Row lengths and arena bases: one load per row, all rows in parallel.
   if (threadIdx.x < 32) {
     const bool report = blockIdx.y == 0;
     const int j = threadIdx.x;
-    const int64_t base = __ldg(p.idx_base + seq_row0);
+    const int64_t base = p.idx_base[seq_row0];
     int len = 0;
     if (j < nrows) {
       const int r = r0 + j;
-      len = __ldg(p.seq_lens + r);
-      const int64_t rb = __ldg(p.idx_base + r);
+      len = p.seq_lens[r];
+      const int64_t rb = p.idx_base[r];
       if (len < 0 || len > p.max_len) {
         if (report) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
         len = 0;
@@ -123,28 +159,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   const int tiles = (ctl->max_len_group + kTileM - 1) / kTileM;
-  const int t_begin = blockIdx.y * p.chunk_tiles;
   const int t_end = min(t_begin + p.chunk_tiles, tiles);
-  if (t_begin >= t_end) return;  // uniform across the CTA, before any barrier or TMEM use
+  if (t_begin >= t_end) return;  // uniform across the CTA, before any TMA, MMA or TMEM use
   const int ntiles = t_end - t_begin;
   const int64_t base = ctl->base;
-  const int stages = p.stages;
 
   // ---------------------------------------------------------------- setup
   uint64_t policy = 0;
   int issued = 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&ctl->tfull[a], 1);
-      mbar_init(&ctl->tempty[a], 4);
-    }
-    mbar_init(&ctl->drain, 1);
-    fence_mbar_init();
-    tma_prefetch_map(&kmap);
     policy = l2_policy_evict_first();
     // The first `stages` tiles need no empty-slot wait.
     for (; issued < min(stages, ntiles); ++issued) {
@@ -165,7 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // K-major layout the MMA descriptor expects (row n at n*128 B inside a
   // 64-element sub-tile, 16-byte chunk c stored at chunk c ^ (n % 8)).
   {
-    const float* qsrc = p.q_idx + static_cast<int64_t>(r0) * p.heads * D;
     const int vec_per_row = D / 8;
     const int nvec = npad * vec_per_row;
     // Up to eight 8-float vectors per thread are loaded before any is used,
@@ -179,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = v / vec_per_row, c8 = v % vec_per_row;
         if (v < nvec && n < nreal) {
           const float4* src = reinterpret_cast<const float4*>(qsrc + static_cast<int64_t>(n) * D + c8 * 8);
-          u[k][0] = __ldg(src);
-          u[k][1] = __ldg(src + 1);
+          u[k][0] = ld_dep_f4(src);
+          u[k][1] = ld_dep_f4(src + 1);
         } else {
           u[k][0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           u[k][1] = u[k][0];
@@ -210,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     for (int n = threadIdx.x; n < npad; n += kThreads)
-      w_s[n] = n < nreal ? __ldg(p.head_w + static_cast<int64_t>(r0) * p.heads + n) : 0.0f;
+      w_s[n] = n < nreal ? p.head_w[static_cast<int64_t>(r0) * p.heads + n] : 0.0f;
     fence_proxy_async_smem();  // generic-proxy smem writes -> visible to the MMA
   }
   tc_fence_before();
@@ -283,16 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const int heads = p.heads;
     const int cols_per_row = (heads % 16 == 0) ? heads : npad;  // heads%16 != 0 -> one row
-    // Each tile's gate is loaded one tile ahead (the first before the
-    // dependency wait: gates are inputs, not a predecessor's output), so the
-    // load's DRAM latency hides behind the TMA and the MMAs.
+    // Each tile's gate is loaded one tile ahead, so the load's DRAM latency
+    // hides behind the TMA and the MMAs (plain loads: the gates may come from
+    // the kernel before, which the wait at the top has ordered).
     const int max_len_group = ctl->max_len_group;
     auto load_gate = [&](int i) {
       const int t = (t_begin + i) * kTileM + lane_tok;
-      return (i < ntiles && t < max_len_group) ? __ldg(p.gate + base + t) : static_cast<uint16_t>(0);
+      return (i < ntiles && t < max_len_group) ? p.gate[base + t] : static_cast<uint16_t>(0);
     };
     uint16_t g_next = load_gate(0);
-    grid_dep_wait();  // the previous top-k may still read the scores buffer
     for (int i = 0; i < ntiles; ++i) {
       if (__shfl_sync(0xFFFFFFFFu, aborted(ctl) ? 1 : 0, 0)) break;
       const int a = i & 1;

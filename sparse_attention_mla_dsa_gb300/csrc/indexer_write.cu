@@ -38,14 +38,16 @@ __global__ void __launch_bounds__(kWarps * 32) indexer_write_kernel(const Indexe
   grid_dep_launch();
   if (r >= p.rows) return;  // whole warps only
 
-  // Inputs no kernel of the chain writes: the norm's weight and bias and the
-  // row metadata.
+  // The norm's weight and bias are weights (no kernel of a chain writes
+  // them) and are read before the wait; the row metadata, k_raw and the gate
+  // may come from kernels before, and the arena may still be read by one.
   double w[kPer], b[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     w[i] = static_cast<double>(__uint_as_float(static_cast<uint32_t>(p.ln_w[lane * kPer + i]) << 16));
     b[i] = static_cast<double>(__uint_as_float(static_cast<uint32_t>(p.ln_b[lane * kPer + i]) << 16));
   }
+  grid_dep_wait();
   const int64_t pos = p.positions[r];
   const int64_t len = p.seq_lens[r];
   const int64_t base = p.idx_base[r];
@@ -59,7 +61,6 @@ __global__ void __launch_bounds__(kWarps * 32) indexer_write_kernel(const Indexe
     ok = false;
   }
 
-  grid_dep_wait();  // k_raw comes from the kernel before; the arena may still be read by one
   if (!ok) return;
   double x[kPer];
 #pragma unroll

@@ -44,6 +44,11 @@ __global__ void __launch_bounds__(kThreads) latent_write_kernel(LatentWriteParam
   __shared__ double warp_sum[kThreads / 32];
   __shared__ int skip;
   grid_dep_launch();
+  // Every input may be the output of the kernel before (kv_a from a
+  // projection, metadata written on the device), and the previous
+  // gather-attend may still read the pool: nothing is read or written before
+  // the wait.
+  grid_dep_wait();
 
   if (tid == 0) {
     int bad = 0;
@@ -58,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) latent_write_kernel(LatentWriteParam
       const int64_t len = p.rows.seq_lens[r];
       const int64_t blk = pos / p.rows.block_size;
       const int32_t* bt = p.rows.block_table + static_cast<int64_t>(r) * p.rows.bt_stride;
-      if (pos + 1 != len || blk >= p.rows.max_blocks_per_seq ||
+      if (pos < 0 || pos + 1 != len || blk >= p.rows.max_blocks_per_seq ||
           static_cast<int64_t>(bt[blk]) * p.rows.block_size + pos % p.rows.block_size != slot) {
         record_error(p.err, DSA_DEVERR_POSITION, r);
         bad = 1;
@@ -95,7 +100,6 @@ __global__ void __launch_bounds__(kThreads) latent_write_kernel(LatentWriteParam
     packed |= static_cast<uint32_t>(encode_e4m3_rne(y * inv)) << (8 * i);
   }
   const int64_t slot = p.rows.slots[r];
-  grid_dep_wait();  // the previous gather-attend may still read the pool
   reinterpret_cast<uint32_t*>(p.pool + slot * 512)[tid] = packed;
 }
 

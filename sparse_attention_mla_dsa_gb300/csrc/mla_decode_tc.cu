@@ -272,13 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nheads = min(kHeads, p.heads - head0);
 
   grid_dep_launch();
-  int len = __ldg(p.rows.seq_lens + r);
-  if (len < 0) {
-    if (report && split == 0 && tid == 0) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
-    len = 0;
-  }
 
-  // ---- set-up: barriers, TMEM
+  // ---- set-up: barriers, TMEM (nothing here reads an input)
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl->full[s], 1);
@@ -298,10 +293,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (tid < kHeads) ctl->mrun[tid] = -INFINITY;
-  // ---- Q: warp w converts heads w, w+12, ...; lane l dims 16l..16l+15.  Q
-  // does not depend on the kernels before, so its loads and conversion run
-  // before the dependency wait (overlapping the top-k under dependent launch).
+  // Q may be the output of the kernel before (a projection), so it is only
+  // prefetched into L2 here (a prefetch cannot make a later load stale) and
+  // loaded after the dependency wait.  Warp w converts heads w, w+12, ...;
+  // lane l dims 16l..16l+15 (32 bytes: lanes 4i..4i+3 share a 128-byte line).
   constexpr int kQPer = (kHeads + kThreads / 32 - 1) / (kThreads / 32);
+#pragma unroll
+  for (int j = 0; j < kQPer; ++j) {
+    const int h = warp + j * (kThreads / 32);
+    if (h < nheads && (lane & 3) == 0)
+      prefetch_l2(p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + lane * 16);
+  }
+  grid_dep_wait();  // the selection (and possibly Q, seq_lens) come from kernels before
+
+  int len = p.rows.seq_lens[r];
+  if (len < 0) {
+    if (report && split == 0 && tid == 0) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
+    len = 0;
+  }
   uint4 qa[kQPer], qb[kQPer];
 #pragma unroll
   for (int j = 0; j < kQPer; ++j) {
@@ -309,12 +318,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (h < nheads) {
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + lane * 16);
-      qa[j] = __ldg(src);
-      qb[j] = __ldg(src + 1);
+      qa[j] = ld_dep_u4(src);
+      qb[j] = ld_dep_u4(src + 1);
     } else {
       qa[j] = make_uint4(0, 0, 0, 0);
       qb[j] = make_uint4(0, 0, 0, 0);
     }
+  }
+  // The split's selection entries, issued before the Q conversion so both
+  // round trips overlap.
+  constexpr int kPer = (kMaxTiles * kTok + kThreads - 1) / kThreads;
+  int idx[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid + i * kThreads;
+    idx[i] = e < nj ? p.sel[static_cast<int64_t>(r) * p.topk + j0 + e] : -1;  // plain load
   }
   // ---- Q operand: q*2^s = hi + lo (E4M3 each), s a power of two per head
   // putting the head's largest |q| in [128, 256).  Row h holds hi, row 64+h lo.
@@ -360,17 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     *reinterpret_cast<uint4*>(blk + h * 128 + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     *reinterpret_cast<uint4*>(blk + (h + kHeads) * 128 + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
-  grid_dep_wait();  // the selection comes from the kernel before
 
-  // ---- slots of every entry of this split (two dependent loads each)
+  // ---- slots of every entry of this split (a table lookup each)
   {
-    constexpr int kPer = (kMaxTiles * kTok + kThreads - 1) / kThreads;
-    int idx[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = tid + i * kThreads;
-      idx[i] = e < nj ? p.sel[static_cast<int64_t>(r) * p.topk + j0 + e] : -1;  // plain load
-    }
     const int32_t* bt = p.rows.block_table + static_cast<int64_t>(r) * p.rows.bt_stride;
     const int bs = p.rows.block_size;
     // All table lookups in flight before any is used (one round trip).
@@ -379,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kPer; ++i) {
       const int t = idx[i];
       const int blk = t >= 0 && t < len ? t / bs : -1;
-      phys[i] = (blk >= 0 && blk < p.rows.max_blocks_per_seq) ? __ldg(bt + blk) : -1;
+      phys[i] = (blk >= 0 && blk < p.rows.max_blocks_per_seq) ? bt[blk] : -1;  // plain load
     }
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
@@ -876,15 +886,13 @@ cudaError_t launch_mla_decode_tc(const DecodeParams& p, const CUtensorMap& pmap,
 // Allocation-free gather-attend.
 //
 // Some callers cannot allocate device memory at the point where they run the
-// attend: code that runs while a stream is being captured into a CUDA graph
-// (an allocation there would either fail or be baked into the graph), code
-// whose device memory is owned by another allocator that it may not call, and
-// serving loops that must not pay cudaMalloc's implicit device synchronisation
-// on the decode path.  This entry point runs the same kernel as
-// dsa_mla_decode_fp8 with the split partials in this file-scope device array
-// instead of a caller-provided workspace.  The array is
-// DSA_NOALLOC_SCRATCH_BYTES long and every GPU that loads the library keeps it
-// until the process exits.
+// attend: a decode loop that must not pay cudaMalloc's implicit device
+// synchronisation, and code whose device memory belongs to an allocator it may
+// not call.  This entry point runs the same kernel as dsa_mla_decode_fp8 with
+// the split partials in this file-scope device array instead of a
+// caller-provided workspace.  The array is DSA_NOALLOC_SCRATCH_BYTES long and
+// every GPU that loads the library keeps it until the process exits.  Every
+// call shares it: calls that overlap on the GPU race on it.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
 
 namespace {

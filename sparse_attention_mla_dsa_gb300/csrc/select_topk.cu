@@ -30,11 +30,6 @@ constexpr int kBins = 256;             // 8-bit digits
 constexpr int kItems = 8;              // consecutive tokens per thread in the output pass
 constexpr int kKeysPerCta = 4096;      // target keys per CTA when choosing the cluster size
 
-// Larger float -> larger unsigned key; -0.0 is folded onto +0.0 first.
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;

@@ -94,8 +94,7 @@ class DeviceWorkload:
                              self.idx_base, self.wl.group_rows, self.max_len, self.scores, stream)
 
     def select_topk(self, stream=None):
-        api.dsa_select_topk(self.rows, self.scores, self.max_len, self.wl.topk, self.sel,
-                            self.workspace, stream)
+        api.dsa_select_topk(self.rows, self.scores, self.max_len, self.wl.topk, self.sel, stream)
 
     def mla_decode(self, stream=None):
         wl = self.wl

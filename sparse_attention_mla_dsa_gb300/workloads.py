@@ -320,3 +320,68 @@ def make_projections(seed: int = 5, rows: int = 4, shapes=PROJECTIONS) -> Projec
         del w
         acts.append(_bf16_bits(rng.standard_normal((rows, k), dtype=np.float32)))
     return ProjectionWorkload(f"proj_k{rows}", rows, tuple(shapes), weights, acts)
+
+
+# --------------------------------------------------------------------------- peaked attention rows
+# The named workloads draw Q ~ 0.05 N(0,1), which with sm_scale 1/16 and a
+# latent ~ N(0,1) gives logits of standard deviation ~0.07: a nearly flat
+# softmax.  Real attention rows are peaked.  These cases keep the geometry (one
+# row, a 512-wide FP8 latent behind a shuffled block table) but lay out the
+# drawn numbers so that the gather-attend meets peaked rows.  Every row sees
+# `length` tokens and selects up to `topk`; with length <= topk the selection
+# is [0, length) in ascending order, so the e-th selected entry is token e.
+#
+#   sharp       Q ~ 5 N(0,1): logit standard deviation ~7.
+#   dominant    per head h a random token j_h; Q[h] = 0.5 x_{j_h} + 0.02 N(0,1),
+#               where x_j is token j's latent draw (before FP8 storage): that
+#               token's logit is ~16 above the others (standard deviation ~0.7).
+#   rising      the latent of token t is x_t = N(0,1) + 0.2 (t/128) v for one
+#               drawn direction v; Q[h] = a_h v + 0.05 N(0,1), a_h ~ U[0.3, 0.6]:
+#               each head's logits climb by ~2-4 per 128-token tile, so the
+#               running maximum moves in every tile (kv_scale 0.05 keeps the
+#               stored latent below the E4M3 maximum).
+#   mixed_heads Q[h] ~ s_h N(0,1) with s_h log-spaced over [0.01, 8] in a
+#               shuffled head order: flat and very peaked heads side by side.
+#   split_underflow  dominant tokens (Q[h] = 0.6 x_{j_h}) all among the first
+#               256 selected entries: every later stretch of the selection
+#               carries weights far below the first one's.
+ATTEND_KINDS = ("sharp", "dominant", "rising", "mixed_heads", "split_underflow")
+
+
+def attend_case(kind: str, heads: int = 64, length: int = 2048, topk: int = 2048,
+                seed: int = 60) -> Workload:
+    """One decode row whose attention is peaked as described above.  The
+    indexer inputs (8 index heads x 64) are the base generator's; only Q and
+    the latent rows of tokens [0, length) are laid out per ``kind``."""
+    if kind not in ATTEND_KINDS:
+        raise ValueError(kind)
+    kv_scale = 0.05 if kind == "rising" else 0.02
+    wl = make_workload(f"attend/{kind}/h{heads}/len{length}", seed, seqs=1, rows_per_seq=1,
+                       len_kind="fixed", len_lo=length, len_hi=length, heads=heads,
+                       index_heads=8, index_dim=64, topk=topk, kv_scale=kv_scale)
+    rng = np.random.default_rng(seed + 1000)
+    f32 = np.float32
+    x = rng.standard_normal((length, LATENT_DIM), dtype=f32)
+    if kind == "sharp":
+        q = f32(5.0) * rng.standard_normal((heads, LATENT_DIM), dtype=f32)
+    elif kind in ("dominant", "split_underflow"):
+        hi = length if kind == "dominant" else min(length, 256)
+        j = rng.integers(0, hi, size=heads)
+        a = f32(0.5 if kind == "dominant" else 0.6)
+        q = a * x[j] + f32(0.02) * rng.standard_normal((heads, LATENT_DIM), dtype=f32)
+    elif kind == "rising":
+        v = rng.standard_normal(LATENT_DIM, dtype=f32)
+        ramp = (np.arange(length, dtype=f32) / f32(128.0)) * f32(0.2)
+        x = x + ramp[:, None] * v[None, :]
+        a = rng.uniform(0.3, 0.6, size=heads).astype(f32)
+        q = a[:, None] * v[None, :] + f32(0.05) * rng.standard_normal((heads, LATENT_DIM), dtype=f32)
+    else:  # mixed_heads
+        s = np.exp(np.linspace(np.log(0.01), np.log(8.0), heads)).astype(f32)
+        rng.shuffle(s)
+        q = s[:, None] * rng.standard_normal((heads, LATENT_DIM), dtype=f32)
+    pool = wl.pool.copy()
+    bt = wl.block_table[0]
+    t = np.arange(length)
+    slots = bt[t // wl.block_size].astype(np.int64) * wl.block_size + t % wl.block_size
+    pool[slots] = _fp8_codes(x / f32(kv_scale))
+    return dataclasses.replace(wl, pool=pool, Q=_bf16_bits(q)[None])

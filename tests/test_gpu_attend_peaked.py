@@ -1,0 +1,91 @@
+"""GPU parity of the gather-attend on peaked attention rows.
+
+The named workloads give nearly flat softmax rows (logit standard deviation
+~0.07), where a logit-scale error of 10 % moves the output by under 1 % and
+the kernel's lazily moving maximum never rescales after the first tile.  These
+cases (``workloads.attend_case``) make the rows peaked: logits of standard
+deviation ~7, one dominant token per head, logits that climb tile after tile
+(the running maximum moves in every tile, forcing the in-TMEM rescale of O),
+flat and peaked heads side by side in one CTA, and a selection whose later
+splits all weigh far below the first split (the merge).  Each runs at 16, 64
+(eight 256-entry splits per row) and 128 heads (one 2048-entry split per
+64-head group), through the whole path (index, top-k, attend) on the GPU, and
+the attend is compared with the oracle on the GPU's own selection under the
+numerics-derived bounds of ``tests/parity.py``.
+
+The bounds are themselves checked: the same GPU output compared with an
+oracle whose softmax scale is off by 10 % must fail them, on a peaked row and
+on a flat one.
+"""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_mla_dsa_gb300 import workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_attention_mla_dsa_gb300 import api, path
+    api.load()
+    api.dsa_get_error(reset=True)
+    return api, path
+
+
+CASES = ([(k, h, 2048) for k in workloads.ATTEND_KINDS for h in (64, 128)]
+         + [("sharp", 64, 2000),        # 48 padding entries in the last tile
+            ("dominant", 16, 2048),
+            ("rising", 16, 2048),
+            ("sharp", 64, 8192)])       # a real top-k of 2048 out of 8192
+
+
+def _run(api, path, wl):
+    dw = path.DeviceWorkload(wl)
+    dw.step()
+    torch.cuda.synchronize()
+    code, row, count = api.dsa_get_error(reset=True)
+    assert code == 0, f"device error {api.DEVERR.get(code)} row {row} count {count}"
+    return dw
+
+
+@pytest.mark.parametrize("kind,heads,length", CASES)
+def test_attend_peaked_rows(dsa, oracle, kind, heads, length):
+    api, path = dsa
+    wl = workloads.attend_case(kind, heads=heads, length=length)
+    dw = _run(api, path, wl)
+    L = int(wl.seq_lens[0])
+    scores = dw.scores.cpu().numpy()[0, :L]
+    sel = dw.sel.cpu().numpy()[0]
+    assert np.array_equal(oracle.select_topk_row(scores.astype(np.float64), L, wl.topk), sel)
+    o_ref, lse_ref, zmag = oracle.mla_decode_row(wl.Q[0], wl.pool, wl.block_table[0], wl.block_size,
+                                                 L, sel, wl.kv_scale, wl.sm_scale, with_zmag=True)
+    st = parity.assert_out(dw.out_f32()[0], o_ref, wl.name)
+    st.update(parity.assert_lse(dw.lse.cpu().numpy()[0], lse_ref, zmag, wl.name))
+    print(f"{wl.name}: max_abs {st['max_abs']:.3e} rel_l2 {st['rel_l2']:.3e} "
+          f"elem/bound {st['elem_ratio']:.3f} lse_err {st['lse_max_abs']:.3e} "
+          f"lse err/tol {st['lse_ratio']:.3f}")
+
+
+@pytest.mark.parametrize("case", ["sharp", "flat"])
+def test_bounds_reject_a_ten_percent_scale_error(dsa, oracle, case):
+    """A planted mistake in the oracle (softmax scale x 1.1) must fail the
+    output bounds that the correct oracle passes."""
+    api, path = dsa
+    wl = (workloads.attend_case("sharp") if case == "sharp"
+          else workloads.scaled("single", len_div=8))
+    dw = _run(api, path, wl)
+    L = int(wl.seq_lens[0])
+    sel = dw.sel.cpu().numpy()[0]
+    out = dw.out_f32()[0]
+    good, _ = oracle.mla_decode_row(wl.Q[0], wl.pool, wl.block_table[0], wl.block_size, L, sel,
+                                    wl.kv_scale, wl.sm_scale)
+    parity.assert_out(out, good, "correct oracle")
+    bad, _ = oracle.mla_decode_row(wl.Q[0], wl.pool, wl.block_table[0], wl.block_size, L, sel,
+                                   wl.kv_scale, wl.sm_scale * 1.1)
+    with pytest.raises(AssertionError):
+        parity.assert_out(out, bad, "oracle with sm_scale x 1.1")

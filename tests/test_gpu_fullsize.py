@@ -41,10 +41,10 @@ def _check_rows(oracle, wl, dw, rows, pool_after):
         if parity.topk_gap_ok(s, A, M, min(wl.topk, L)):
             assert np.array_equal(oracle.select_topk_row(s, L, wl.topk), sel[r])
         bt = wl.block_table[r] if wl.bt_stride else wl.block_table[0]
-        o_ref, lse_ref = oracle.mla_decode_row(wl.Q[r], pool_after, bt, wl.block_size, L, sel[r],
-                                               wl.kv_scale, wl.sm_scale)
+        o_ref, lse_ref, zmag = oracle.mla_decode_row(wl.Q[r], pool_after, bt, wl.block_size, L,
+                                                     sel[r], wl.kv_scale, wl.sm_scale, with_zmag=True)
         parity.assert_out(out[r], o_ref, f"{wl.name} row {r} out")
-        parity.assert_lse(lse[r], lse_ref, f"{wl.name} row {r} lse")
+        parity.assert_lse(lse[r], lse_ref, zmag, f"{wl.name} row {r} lse")
 
 
 @pytest.mark.parametrize("name", ["tiny", "single", "batched", "verify", "long"])

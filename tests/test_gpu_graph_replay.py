@@ -117,8 +117,8 @@ def test_one_graph_serves_a_growing_context(dsa, oracle):
         assert np.array_equal(oracle.select_topk_row(scores.astype(np.float64), L, state.topk), sel)
         diff = dw.pool.cpu().numpy()[state.slots] != pool_ref[state.slots]
         assert not (diff & (near == 0)).any(), f"step {step}: latent bytes"
-        o_ref, lse_ref = oracle.mla_decode_row(state.Q[0], pool_ref, state.block_table[0],
-                                               state.block_size, L, sel, state.kv_scale,
-                                               state.sm_scale)
+        o_ref, lse_ref, zmag = oracle.mla_decode_row(state.Q[0], pool_ref, state.block_table[0],
+                                                     state.block_size, L, sel, state.kv_scale,
+                                                     state.sm_scale, with_zmag=True)
         parity.assert_out(dw.out_f32()[0], o_ref, f"replay step {step} out")
-        parity.assert_lse(dw.lse.cpu().numpy()[0], lse_ref, f"replay step {step} lse")
+        parity.assert_lse(dw.lse.cpu().numpy()[0], lse_ref, zmag, f"replay step {step} lse")

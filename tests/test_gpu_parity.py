@@ -80,10 +80,10 @@ def check_path(oracle, api, path, wl, rows=None):
             ref_sel = oracle.select_topk_row(s, L, wl.topk)
             assert np.array_equal(ref_sel, sel[r]), f"{wl.name} row {r}: top-k set differs"
         bt = wl.block_table[r] if wl.bt_stride else wl.block_table[0]
-        o_ref, lse_ref = oracle.mla_decode_row(wl.Q[r], pool_after, bt, wl.block_size, L, sel[r],
-                                               wl.kv_scale, wl.sm_scale)
+        o_ref, lse_ref, zmag = oracle.mla_decode_row(wl.Q[r], pool_after, bt, wl.block_size, L,
+                                                     sel[r], wl.kv_scale, wl.sm_scale, with_zmag=True)
         parity.assert_out(out[r], o_ref, f"{wl.name} row {r} out")
-        parity.assert_lse(lse[r], lse_ref, f"{wl.name} row {r} lse")
+        parity.assert_lse(lse[r], lse_ref, zmag, f"{wl.name} row {r} lse")
     return dw
 
 

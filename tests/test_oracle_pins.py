@@ -299,6 +299,35 @@ def test_decode_empty_selection(oracle):
     assert (out == 0).all() and np.isneginf(lse).all()
 
 
+def test_decode_logit_magnitude_bounds_and_closed_form(oracle):
+    """zmag[h] (the logits' conditioning scale) is never below a selected
+    logit's magnitude, and equals the largest logit when every term of every
+    dot product is non-negative (each term then adds its own magnitude)."""
+    rng = np.random.default_rng(16)
+    pool, bt, Q = _decode_case(rng)
+    sel = np.array([0, 5, 9, 17, 23, 39, -1], np.int32)
+    out, lse, zmag = oracle.mla_decode_row(Q, pool, bt, 8, 40, sel, 0.02, 0.0625, with_zmag=True)
+    slots = [int(bt[j // 8]) * 8 + j % 8 for j in sel if j >= 0]
+    kv = torch.from_numpy(pool[slots]).view(torch.float8_e4m3fn).double() * float(np.float32(0.02))
+    q = torch.from_numpy(Q.view(np.int16)).view(torch.bfloat16).double()
+    z = ((q @ kv.T) * 0.0625).numpy()
+    assert (zmag >= np.abs(z).max(1) * (1 - 1e-15)).all()
+    # all-positive operands: codes 0x00..0x3F are the non-negative finite E4M3 values
+    pos_pool = (rng.integers(0, 0x40, pool.shape)).astype(np.uint8)
+    pos_q = _bf16(np.abs(rng.standard_normal(Q.shape)) * 0.05)
+    _, lse2, zmag2 = oracle.mla_decode_row(pos_q, pos_pool, bt, 8, 40, sel, 0.02, 0.0625,
+                                          with_zmag=True)
+    kv2 = torch.from_numpy(pos_pool[slots]).view(torch.float8_e4m3fn).double() * float(np.float32(0.02))
+    q2 = torch.from_numpy(pos_q.view(np.int16)).view(torch.bfloat16).double()
+    z2 = ((q2 @ kv2.T) * 0.0625).numpy()
+    assert np.allclose(zmag2, z2.max(1), rtol=1e-13)
+    assert (lse2 >= z2.max(1)).all()
+    # and with nothing selected it is 0
+    _, _, zmag0 = oracle.mla_decode_row(Q, pool, bt, 8, 0, np.full(3, -1, np.int32), 0.02, 0.0625,
+                                        with_zmag=True)
+    assert (zmag0 == 0).all()
+
+
 # ----------------------------------------------------------------------------- planted mistakes
 def test_planted_wrong_operand_fails_decode_pin(oracle):
     """Transposed / wrong-slot reads: a decode that reads slot j instead of

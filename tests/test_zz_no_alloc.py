@@ -1,20 +1,19 @@
 """The allocation-free gather-attend entry point (collected last on purpose).
 
 dsa_mla_decode_fp8_noalloc serves callers that cannot allocate device memory
-where they run the attend (stream capture, foreign allocators, allocator-free
-serving loops): it keeps the split partials in the library's own device array
-instead of a caller workspace.  Through the C ABI, two calls in a row -- on
-two different workloads, so the second cannot pass on the first's leftovers
-in the shared device array -- must match the workspace entry point within the
-parity tolerances used everywhere else; a shape whose partials exceed the
-array must be refused without a launch.
+where they run the attend (a decode loop that must not take cudaMalloc's
+device synchronisation, or memory owned by an allocator the caller may not
+call): it keeps the split partials in the library's own device array instead
+of a caller workspace.  Through the C ABI, two calls in a row -- on two
+different workloads, so the second cannot pass on the first's leftovers in the
+shared device array -- must equal the workspace entry point bit for bit: both
+run the same kernels on the same inputs with the same split plan.  A shape
+whose partials exceed the array must be refused without a launch.
 """
-import numpy as np
 import pytest
 import torch
 
 from sparse_attention_mla_dsa_gb300 import workloads
-from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -40,18 +39,16 @@ def _compare(api, path, wl):
                                    wl.sm_scale, dw.out, dw.lse)
     torch.cuda.synchronize()
     assert api.dsa_get_error(reset=True)[0] == 0
-    a = out_ws.view(torch.bfloat16).double().cpu().numpy()
-    b = dw.out.view(torch.bfloat16).double().cpu().numpy()
-    for r in range(wl.rows):
-        parity.assert_out(b[r], a[r], f"{wl.name} row {r} no-alloc vs workspace")
-        parity.assert_lse(dw.lse[r].double().cpu().numpy(), lse_ws[r].double().cpu().numpy(),
-                          f"{wl.name} row {r} lse")
+    assert torch.equal(dw.out, out_ws), f"{wl.name}: no-alloc output differs from the workspace call"
+    assert torch.equal(dw.lse.view(torch.int32), lse_ws.view(torch.int32)), f"{wl.name}: lse differs"
 
 
 def test_noalloc_matches_workspace_entry_point_twice(dsa):
     api, path = dsa
+    # Both shapes have 64 heads (eight 256-entry splits per row), so both
+    # calls pass their partials through the shared array.
     _compare(api, path, workloads.scaled("batched", seqs=3, len_div=16))
-    _compare(api, path, workloads.scaled("long", seqs=2, len_div=16))
+    _compare(api, path, workloads.scaled("verify", seqs=2, len_div=32))
 
 
 def test_noalloc_refuses_oversized_call(dsa):
