@@ -20,6 +20,10 @@ follows on the pages:
   (``dense_mm``); the module header trap 2 and ``indexer_forward`` (the
   indexer's k_norm LayerNorm with a bias and the store at the token's
   position: ``layer_norm_row``, ``indexer_write_rows``).
+* "glm5next_dsa/layer.rs" -- the notes above ``batch_select_enabled`` and on
+  ``select_rows_batched`` (pool candidacy, the total order over pools, the
+  per-row ``row_select_k`` and the visible tail): ``select_pools_row``,
+  ``expand_selection_row``.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, brute force, exhaustive code tables, library routines) and by
@@ -79,6 +83,10 @@ def _load():
             lib.dsa_oracle_mla_decode_row.argtypes = [i32, i32, P, P, i64, P, i32, i32, i64,
                                                       P, i32, f32, f32, P, P, P]
             lib.dsa_oracle_mla_decode_row.restype = i32
+            lib.dsa_oracle_select_pools_row.argtypes = [i64, P, P, i64, i32, i32, P]
+            lib.dsa_oracle_select_pools_row.restype = i32
+            lib.dsa_oracle_expand_selection_row.argtypes = [i32, i32, P, i64, i32, P]
+            lib.dsa_oracle_expand_selection_row.restype = None
             lib.dsa_oracle_dense_mla_row.argtypes = [i32, i32, P, P, i64, P, i32, i32, i64,
                                                      f32, f32, P, P]
             lib.dsa_oracle_dense_mla_row.restype = i32
@@ -224,6 +232,33 @@ def dense_mla_row(Q: np.ndarray, pool: np.ndarray, bt_row: np.ndarray, block_siz
     if rc != 0:
         raise ValueError("oracle: block table does not cover the context")
     return out, lse
+
+
+# --------------------------------------------------------------------------- pool selection
+def select_pools_row(scores: np.ndarray, valid: np.ndarray, q_pos: int, kp: int,
+                     select_k: int) -> np.ndarray:
+    """Pool selection of one row ("glm5next_dsa/layer.rs", notes on
+    batch_select_enabled / select_rows_batched): candidates are the valid
+    pools whose last token is <= q_pos; the first min(select_k, (q_pos+1)//kp)
+    of them under (score DESC, pool ASC), in that order, -1 padded to
+    select_k.  scores float32 [P], valid uint8 [P]."""
+    scores = _c(scores, np.float32)
+    valid = _c(valid, np.uint8)
+    sel = np.zeros(select_k, np.int32)
+    _load().dsa_oracle_select_pools_row(scores.shape[0], _ptr(scores), _ptr(valid), int(q_pos),
+                                        int(kp), int(select_k), _ptr(sel))
+    return sel
+
+
+def expand_selection_row(pools: np.ndarray, q_pos: int, kp: int, out_width: int) -> np.ndarray:
+    """Pools to tokens: pool i's kp tokens at [i*kp, (i+1)*kp) for i <
+    min(select_k, (q_pos+1)//kp), then the visible tail (the tokens after the
+    last complete pool, up to q_pos); -1 elsewhere."""
+    pools = _c(pools, np.int32)
+    out = np.zeros(out_width, np.int32)
+    _load().dsa_oracle_expand_selection_row(pools.shape[0], int(kp), _ptr(pools), int(q_pos),
+                                            int(out_width), _ptr(out))
+    return out
 
 
 def bt_entries_needed(seq_len: int, k: int, block_size: int) -> int:

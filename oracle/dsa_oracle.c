@@ -399,3 +399,68 @@ void dsa_oracle_layer_norm_row(int dim, const uint16_t *x, const uint16_t *w, co
             mag[d] = fabs(t) + fabs(dsa_oracle_bf16_value(b[d]));
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Pool-compressed selection, the half the pages specify.                   */
+/* "glm5next_dsa/layer.rs", the notes above batch_select_enabled and on      */
+/* select_rows_batched: a pool is a candidate for row r only when it is      */
+/* complete (pool_valid) and its last token is visible to the row            */
+/* (end <= q_pos[r]); non-candidates score -FLT_MAX and are left out; the    */
+/* pools are taken under the total order (score DESC, then pool index ASC);  */
+/* the per-row count row_select_k = min(select_k, (q_pos[r] + 1) / KP) sets  */
+/* both the number of pools taken and the base of the visible tail, which   */
+/* dsa_expand_selection writes after the pools' tokens.  How the pool scores */
+/* are computed (the gate and ape compression) is not on the pages; the      */
+/* caller supplies them.                                                     */
+/* ------------------------------------------------------------------------ */
+static int64_t row_select_k(int select_k, int kp, int64_t q_pos)
+{
+    int64_t visible = q_pos + 1 >= 0 ? (q_pos + 1) / (kp > 0 ? kp : 1) : 0;
+    return visible < (int64_t)select_k ? visible : (int64_t)select_k;
+}
+
+int dsa_oracle_select_pools_row(int64_t npools, const float *scores, const uint8_t *valid,
+                                int64_t q_pos, int kp, int select_k, int32_t *sel)
+{
+    int64_t want = row_select_k(select_k, kp, q_pos);
+    /* candidates of this row, then the total order over them */
+    scored_token *cand = (scored_token *)malloc((size_t)(npools > 0 ? npools : 1) * sizeof *cand);
+    int64_t nc = 0;
+    for (int64_t p = 0; p < npools; ++p) {
+        int64_t end = (p + 1) * (int64_t)kp - 1;
+        if (valid[p] && end <= q_pos) {
+            cand[nc].score = (double)scores[p];
+            cand[nc].index = p;
+            ++nc;
+        }
+    }
+    qsort(cand, (size_t)nc, sizeof *cand, by_score_desc_index_asc);
+    int64_t n = nc < want ? nc : want;
+    for (int64_t i = 0; i < n; ++i)
+        sel[i] = (int32_t)cand[i].index;
+    for (int64_t i = n; i < select_k; ++i)
+        sel[i] = -1;
+    free(cand);
+    return (int)n;
+}
+
+void dsa_oracle_expand_selection_row(int select_k, int kp, const int32_t *pools, int64_t q_pos,
+                                     int out_width, int32_t *tokens)
+{
+    int64_t k = row_select_k(select_k, kp, q_pos);
+    for (int i = 0; i < out_width; ++i)
+        tokens[i] = -1;
+    /* the selected pools' tokens, pool i at [i*KP, (i+1)*KP) */
+    for (int64_t i = 0; i < k; ++i)
+        if (pools[i] >= 0)
+            for (int j = 0; j < kp; ++j)
+                if (i * kp + j < out_width)
+                    tokens[i * kp + j] = (int32_t)((int64_t)pools[i] * kp + j);
+    /* the visible tail: the tokens after the last complete pool, up to q_pos */
+    int64_t tail_start = q_pos + 1 >= 0 ? ((q_pos + 1) / kp) * kp : 0;
+    for (int64_t t = tail_start; t <= q_pos; ++t) {
+        int64_t at = k * kp + (t - tail_start);
+        if (at < out_width)
+            tokens[at] = (int32_t)t;
+    }
+}

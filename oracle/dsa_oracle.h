@@ -126,6 +126,23 @@ void dsa_oracle_dense_mm_row(int n, int k, const uint16_t *a_row, const uint16_t
 void dsa_oracle_layer_norm_row(int dim, const uint16_t *x, const uint16_t *w, const uint16_t *b,
                                float eps, double *y, double *mag);
 
+/* Pool-compressed selection of one row (the part the pages specify; the pool
+ * scores themselves are the caller's).  Pool p covers tokens [p*kp, (p+1)*kp)
+ * and is a candidate iff valid[p] != 0 and (p+1)*kp - 1 <= q_pos.  With
+ * row_select_k = min(select_k, (q_pos+1) / kp), the first min(row_select_k,
+ * #candidates) candidates under (score DESC, pool index ASC) are written to
+ * sel[0..) in that order; the rest of sel[0..select_k) is -1.  Returns the
+ * number written.  scores, valid: [npools]. */
+int dsa_oracle_select_pools_row(int64_t npools, const float *scores, const uint8_t *valid,
+                                int64_t q_pos, int kp, int select_k, int32_t *sel);
+
+/* Expansion of one row's pool selection to tokens: for i < row_select_k,
+ * tokens[i*kp + j] = pools[i]*kp + j (j < kp; -1 where pools[i] is -1), then
+ * the visible tail -- tokens floor((q_pos+1)/kp)*kp .. q_pos -- from index
+ * row_select_k*kp on; every other entry of tokens[0..out_width) is -1. */
+void dsa_oracle_expand_selection_row(int select_k, int kp, const int32_t *pools, int64_t q_pos,
+                                     int out_width, int32_t *tokens);
+
 #ifdef __cplusplus
 }
 #endif

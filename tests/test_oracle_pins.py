@@ -530,3 +530,112 @@ def test_planted_layer_norm_mistakes_are_caught(oracle):
     y, _ = oracle.layer_norm_row(np.full(dim, _bf16([2.5])[0], np.uint16), w, b, 1e-6)
     assert np.array_equal(y, bval)
     assert not np.allclose(rms_form, bval) and not np.allclose(no_bias, bval)
+
+
+# ----------------------------------------------------------------------------- pool selection
+def _brute_pools(scores, valid, q_pos, kp, select_k):
+    """The pages' definition, written out: valid pools ending at or before
+    q_pos, sorted by (score DESC, pool ASC), the first min(select_k,
+    (q_pos+1)//kp) of them."""
+    k = min(select_k, (q_pos + 1) // kp)
+    cand = [p for p in range(len(scores)) if valid[p] and (p + 1) * kp - 1 <= q_pos]
+    cand.sort(key=lambda p: (-float(scores[p]), p))
+    out = cand[:k]
+    return out + [-1] * (select_k - len(out))
+
+
+def test_select_pools_brute_force_with_ties_and_validity(oracle):
+    rng = np.random.default_rng(40)
+    for trial in range(200):
+        P = int(rng.integers(1, 60))
+        kp = int(rng.choice([1, 2, 4, 8, 64]))
+        select_k = int(rng.integers(1, 20))
+        q_pos = int(rng.integers(0, P * kp + kp))
+        scores = (rng.integers(-4, 5, P) if trial % 2 else rng.standard_normal(P)).astype(np.float32)
+        valid = (rng.random(P) < 0.8).astype(np.uint8)
+        got = oracle.select_pools_row(scores, valid, q_pos, kp, select_k)
+        assert list(got) == _brute_pools(scores, valid, q_pos, kp, select_k), trial
+
+
+def test_select_pools_widened_walk_is_unchanged(oracle):
+    """The pages' exactness argument for the batched selection: walking more
+    pools than the row's own (every extra one incomplete or ending past
+    q_pos) selects the same pools in the same order."""
+    rng = np.random.default_rng(41)
+    for _ in range(100):
+        kp = int(rng.choice([1, 4, 16]))
+        own = int(rng.integers(1, 40))
+        q_pos = own * kp - 1 + int(rng.integers(0, kp))        # the row's own pools are complete
+        scores = rng.standard_normal(own).astype(np.float32)
+        valid = (rng.random(own) < 0.9).astype(np.uint8)
+        select_k = int(rng.integers(1, own + 5))
+        base = oracle.select_pools_row(scores, valid, q_pos, kp, select_k)
+        extra = int(rng.integers(1, 30))
+        wide_s = np.concatenate([scores, 10 + rng.standard_normal(extra).astype(np.float32)])
+        wide_v = np.concatenate([valid, np.ones(extra, np.uint8)])     # complete, but past q_pos
+        assert np.array_equal(oracle.select_pools_row(wide_s, wide_v, q_pos, kp, select_k), base)
+
+
+def test_select_pools_kp1_is_the_token_topk(oracle):
+    """With one token per pool and every pool valid, the selected set is the
+    token top-k of the row's visible scores (only the order differs: rank
+    order here, token order there)."""
+    rng = np.random.default_rng(42)
+    for _ in range(50):
+        L = int(rng.integers(1, 300))
+        s = rng.integers(-20, 20, L).astype(np.float32)
+        k = int(rng.integers(1, 64))
+        pools = oracle.select_pools_row(s, np.ones(L, np.uint8), L - 1, 1, k)
+        toks = oracle.select_topk_row(s.astype(np.float64), L, k)
+        assert sorted(pools[pools >= 0].tolist()) == toks[toks >= 0].tolist()
+
+
+def test_expand_selection_tail_at_row_select_k(oracle):
+    """Equal membership is not equal placement (layer.rs, select_rows_batched
+    notes): the visible tail starts at row_select_k * KP, where row_select_k
+    = min(select_k, (q_pos+1)/KP), not at select_k * KP."""
+    kp, select_k = 4, 6
+    q_pos = 13                                   # 3 complete pools, tail 12..13
+    pools = np.array([2, 0, 1, -1, -1, -1], np.int32)
+    out = oracle.expand_selection_row(pools, q_pos, kp, select_k * kp + kp - 1)
+    assert out[:12].tolist() == [8, 9, 10, 11, 0, 1, 2, 3, 4, 5, 6, 7]
+    assert out[12:14].tolist() == [12, 13] and (out[14:] == -1).all()
+    # q_pos before the first complete pool: nothing but the tail
+    out = oracle.expand_selection_row(pools, 2, kp, 27)
+    assert out[:3].tolist() == [0, 1, 2] and (out[3:] == -1).all()
+    # a missing pool (-1) leaves its KP entries -1 and does not move the tail
+    out = oracle.expand_selection_row(np.array([5, -1, 3], np.int32), 27, kp, 3 * kp + kp - 1)
+    assert out[:4].tolist() == [20, 21, 22, 23] and (out[4:8] == -1).all()
+    assert out[8:12].tolist() == [12, 13, 14, 15] and (out[12:] == -1).all()
+
+
+def test_expand_selection_against_closed_form(oracle):
+    rng = np.random.default_rng(43)
+    for _ in range(100):
+        kp = int(rng.choice([1, 2, 4, 8]))
+        select_k = int(rng.integers(1, 12))
+        q_pos = int(rng.integers(0, 100))
+        pools = rng.integers(-1, 30, select_k).astype(np.int32)
+        width = select_k * kp + kp - 1 + int(rng.integers(0, 5))
+        got = oracle.expand_selection_row(pools, q_pos, kp, width)
+        k = min(select_k, (q_pos + 1) // kp)
+        want = [-1] * width
+        for i in range(k):
+            for j in range(kp):
+                want[i * kp + j] = int(pools[i]) * kp + j if pools[i] >= 0 else -1
+        start = ((q_pos + 1) // kp) * kp
+        for t in range(start, q_pos + 1):
+            want[k * kp + t - start] = t
+        assert got.tolist() == want
+
+
+def test_planted_pool_mistakes_fail_the_pins(oracle):
+    """Dropping the validity test or the visibility test changes the
+    selection on inputs where they matter, so the brute-force pin would see
+    either mistake."""
+    scores = np.array([5, 4, 3, 2, 1, 9], np.float32)
+    valid = np.array([1, 0, 1, 1, 1, 1], np.uint8)
+    right = oracle.select_pools_row(scores, valid, 4 * 5 - 1, 4, 3)   # pool 5 ends at 23 > 19
+    assert right.tolist() == [0, 2, 3]
+    assert oracle.select_pools_row(scores, np.ones(6, np.uint8), 19, 4, 3).tolist() != right.tolist()
+    assert oracle.select_pools_row(scores, valid, 23, 4, 3).tolist() != right.tolist()
