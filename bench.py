@@ -44,6 +44,8 @@ DESCRIPTIONS = {
               "index 32x128, topk 2048",
     "long": "long-context batch: 64 seqs x 1 row, len log-U[4096,131072], 128 heads, index 64x128, "
             "topk 2048, latent write of the new row",
+    "prefill": "prefill selection in one pass: 1 seq x 1024 query rows (lens 7977..9000 of a 9000-token "
+               "prompt), 64 heads, index 32x128, topk 2048",
     "index_write": "indexer write side: 4 rows x (wk 128x4096 bf16 out, weights_proj 32x4096 fp32 out, "
                    "LayerNorm with bias + store into a 131072-token key arena), L2 flushed between steps",
     "proj_verify": "K-token verify projections: 4 rows x (q_a and kv_a stacked 2048x4096, absorbed q_b "
@@ -196,7 +198,7 @@ def stage_bytes(wl):
 
 
 # --------------------------------------------------------------------------- our arm
-SECONDARY = ("batched", "verify", "long")
+SECONDARY = ("batched", "verify", "long", "prefill")
 
 
 def config_of(name, wl):

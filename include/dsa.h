@@ -14,6 +14,10 @@
  *                          bf16 weight, each row bit-identical to a one-row call
  *      dsa_indexer_write   the indexer key's LayerNorm (with bias) and its store
  *                          at the row's device-side arena position
+ * and the pool-compressed form of the selection (over caller-supplied pool
+ * scores):
+ *      dsa_select_pools    top pools per row under (score DESC, pool ASC)
+ *      dsa_expand_selection  pools to tokens, plus the visible tail
  * Sources (spark_model documentation):
  * the "glm5next_dsa/layer.rs" source page (module header: decode data flow
  * and its traps; decode_k: latent write, per-row metadata, one attend for all
@@ -71,7 +75,9 @@ enum {
     DSA_DEVERR_BLOCK = 4,     /* block-table entry missing, negative or past the pool   */
     DSA_DEVERR_ARENA = 5,     /* idx_base invalid, or rows of one group differ in base  */
     DSA_DEVERR_POSITION = 6,  /* positions[r] != seq_lens[r]-1, or slot != table slot   */
-    DSA_DEVERR_TIMEOUT = 7    /* a bounded wait inside a kernel gave up                 */
+    DSA_DEVERR_TIMEOUT = 7,   /* a bounded wait inside a kernel gave up                 */
+    DSA_DEVERR_BEHIND = 8     /* a sequence's indexer keys stop short of its length:
+                                 rows were never written (lockstep with the KV cache)  */
 };
 
 /*
@@ -128,6 +134,10 @@ dsa_status dsa_latent_write(const dsa_rows *rows, const uint16_t *kv_a, const ui
  * rows_per_seq: consecutive rows that share one sequence (a K-token verify);
  * they must have equal idx_base (checked on the device) and their keys are
  * read once for all of them.  rows must be a multiple of rows_per_seq.
+ * idx_written (optional, may be NULL): [rows / rows_per_seq] int32, the rows
+ * of each sequence's keys written so far (as kept by dsa_indexer_write); a
+ * row whose seq_len exceeds its sequence's count is skipped (scores not
+ * written) and recorded as DSA_DEVERR_BEHIND.
  * Supported: index_dim in {64, 128}; index_heads in [1, 256]; idx_k 16-byte
  * aligned; idx_tokens < 2^31.  Each row's result does not depend on
  * rows_per_seq or on the other rows (bit for bit).
@@ -136,7 +146,7 @@ dsa_status dsa_index_scores(const dsa_rows *rows, const float *q_idx, const floa
                             const uint16_t *idx_k, const uint16_t *idx_gate, int64_t idx_tokens,
                             const int64_t *idx_base, int32_t index_heads, int32_t index_dim,
                             int32_t rows_per_seq, int32_t max_len, float *scores,
-                            void *stream);
+                            const int32_t *idx_written, void *stream);
 
 /*
  * S2 -- per-row top-k ("glm5next_dsa/layer.rs", notes on batch_select_enabled
@@ -231,6 +241,51 @@ size_t dsa_noalloc_scratch_bytes(int32_t rows, int32_t heads, int32_t topk);
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 
 /*
+ * Pool-compressed selection, the part the pages specify
+ * ("glm5next_dsa/layer.rs", the notes above batch_select_enabled and on
+ * select_rows_batched).  Tokens are grouped into pools of kp; pool p holds
+ * tokens [p*kp, (p+1)*kp).  For each row r, with q_pos = positions[r]:
+ *   - pool p is a candidate iff pool_valid[r*valid_stride + p] != 0 (the pool
+ *     is complete) and (p+1)*kp - 1 <= q_pos (its last token is visible);
+ *   - row_select_k = min(select_k, (q_pos + 1) / kp);
+ *   - sel_pools[r*select_k + i], i < min(row_select_k, #candidates), are the
+ *     candidates in the total order (score DESC, then pool index ASC); every
+ *     other entry is -1 (a non-candidate is never selected).
+ * -0.0 and +0.0 compare equal; scores must not be NaN.  Only pools below
+ * (q_pos+1)/kp are read, so a row's result does not depend on max_pools or
+ * on the other rows.  How the pool scores are made (the pages' gate [D] and
+ * ape [kp][D] compression of the pool's keys) is not on the pages: the caller
+ * supplies them.
+ *   pool_scores [rows][max_pools] fp32          pool_valid [rows or 1][...] u8
+ *   valid_stride: elements between rows of pool_valid, 0 = one shared row
+ *   sel_pools   [rows][select_k] int32 (output)
+ * rows->positions is required.  kp, select_k >= 1; max_pools in
+ * [1, DSA_MAX_POOLS] (DSA_ERR_UNSUPPORTED above).
+ */
+#define DSA_MAX_POOLS 16384
+dsa_status dsa_select_pools(const dsa_rows *rows, const float *pool_scores, int32_t max_pools,
+                            const uint8_t *pool_valid, int32_t valid_stride, int32_t kp,
+                            int32_t select_k, int32_t *sel_pools, void *stream);
+
+/*
+ * Expansion of a pool selection to token indices (same source: the
+ * expansion writes the pools' tokens, then the visible tail at
+ * row_select_k * kp; the per-row row_select_k applies to both).  For each row
+ * r, with q_pos = positions[r] and row_select_k as above:
+ *   sel_tokens[r*out_width + i*kp + j] = sel_pools[r*select_k + i]*kp + j
+ *       for i < row_select_k, j < kp (-1 where the pool entry is -1);
+ *   then the tokens floor((q_pos+1)/kp)*kp .. q_pos (the part of the
+ *   incomplete pool the row sees) from entry row_select_k*kp on;
+ *   every other entry of the row is -1.
+ * The result is a selection row for dsa_mla_decode_fp8 (which skips -1).
+ * out_width >= select_k*kp + kp - 1 (room for the longest tail), else
+ * DSA_ERR_INVALID_ARG.  rows->positions is required.
+ */
+dsa_status dsa_expand_selection(const dsa_rows *rows, const int32_t *sel_pools, int32_t kp,
+                                int32_t select_k, int32_t *sel_tokens, int32_t out_width,
+                                void *stream);
+
+/*
  * Indexer write side for each row's new token ("glm5next_dsa/layer.rs",
  * module header trap 2: indexer.k_norm is an nn.LayerNorm with a bias;
  * indexer_forward: the wk projection of the token lands in the key cache row,
@@ -250,11 +305,22 @@ size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
  * bf16 (nearest, ties to even).  A row whose position is not seq_lens[r]-1
  * (DSA_DEVERR_POSITION) or whose arena row lies outside [0, idx_tokens)
  * (DSA_DEVERR_ARENA) is skipped and recorded.
+ * Lockstep with the KV cache ("glm5next_dsa/layer.rs", decode_k: the indexer
+ * cache must hold exactly the sequence's tokens before the step; more is the
+ * leftover of a rejected verify and is rewound, fewer means rows were never
+ * written and is an error), when idx_written is given ([rows / rows_per_seq]
+ * int32, one count per sequence of rows_per_seq consecutive rows, which must
+ * have the consecutive positions p0, p0+1, ...): a sequence whose count is
+ * below p0 is not written and is recorded as DSA_DEVERR_BEHIND; otherwise
+ * its rows are written and its count becomes p0 + rows_per_seq (a count
+ * above p0 is rewound).  rows_per_seq in [1, 32] and dividing rows when
+ * idx_written is given (ignored otherwise).
  */
 dsa_status dsa_indexer_write(const dsa_rows *rows, const uint16_t *k_raw, const uint16_t *ln_w,
                              const uint16_t *ln_b, float eps, const uint16_t *gate,
                              const int64_t *idx_base, uint16_t *idx_k, uint16_t *idx_gate,
-                             int64_t idx_tokens, int32_t index_dim, void *stream);
+                             int64_t idx_tokens, int32_t index_dim, int32_t *idx_written,
+                             int32_t rows_per_seq, void *stream);
 
 /*
  * Batched projection for the K-token verify: the K rows of one sequence sweep
@@ -306,6 +372,19 @@ dsa_status dsa_get_error(int32_t *code_out, int32_t *row_out, int32_t *count_out
  * seq_len, plus one of slack: (seq_len + k) / block_size + 2, a block size of
  * 0 counted as 1 ("glm5next_dsa/layer.rs", bt_entries_needed). */
 int64_t dsa_bt_entries_needed(int64_t seq_len, int64_t k, int64_t block_size);
+
+/*
+ * Limit, in nanoseconds of wall time, on every pipeline wait inside the
+ * kernels launched after this call (0 restores the default, 500 ms).  A wait
+ * that runs out records DSA_DEVERR_TIMEOUT, the CTA stops its pipeline and
+ * its results are zero; the CTA still waits for its own copies and MMAs in
+ * flight (that drain keeps its own 500 ms limit) before it exits, so a short
+ * limit never leaves work running behind the call.  Meant for tests of the
+ * timeout path and for callers that prefer an early error to a long stall;
+ * process-wide.  No counterpart on the pages.
+ */
+dsa_status dsa_set_wait_limit_ns(uint64_t limit_ns);
+uint64_t dsa_get_wait_limit_ns(void);
 
 /* Static text for a status code. */
 const char *dsa_status_string(dsa_status status);

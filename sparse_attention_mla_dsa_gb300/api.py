@@ -18,7 +18,7 @@ LATENT_DIM = 512
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
            4: "device-side error recorded", 5: "workspace missing or too small"}
 DEVERR = {0: "none", 1: "seq_len", 2: "slot", 3: "select", 4: "block", 5: "arena",
-          6: "position", 7: "timeout"}
+          6: "position", 7: "timeout", 8: "behind"}
 
 
 class DsaError(RuntimeError):
@@ -56,13 +56,15 @@ def load() -> ctypes.CDLL:
     RP = ctypes.POINTER(Rows)
     sig = {
         "dsa_latent_write": [RP, P, P, P, i64, i32, f32, f32, P],
-        "dsa_index_scores": [RP, P, P, P, P, i64, P, i32, i32, i32, i32, P, P],
+        "dsa_index_scores": [RP, P, P, P, P, i64, P, i32, i32, i32, i32, P, P, P],
         "dsa_select_topk": [RP, P, i32, i32, P, P],
         "dsa_mla_decode_fp8": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, sz, P],
         "dsa_mla_decode_fp8_noalloc": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P],
         "dsa_get_error": [P, P, P, i32],
         "dsa_dense_mm_bf16": [P, P, P, i32, i32, i32, i32, P, sz, P],
-        "dsa_indexer_write": [RP, P, P, P, f32, P, P, P, P, i64, i32, P],
+        "dsa_indexer_write": [RP, P, P, P, f32, P, P, P, P, i64, i32, P, i32, P],
+        "dsa_select_pools": [RP, P, i32, P, i32, i32, i32, P, P],
+        "dsa_expand_selection": [RP, P, i32, i32, P, i32, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -78,6 +80,10 @@ def load() -> ctypes.CDLL:
     lib.dsa_bt_entries_needed.restype = i64
     lib.dsa_status_string.argtypes = [ctypes.c_int]
     lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.dsa_set_wait_limit_ns.restype = ctypes.c_int
+    lib.dsa_get_wait_limit_ns.argtypes = []
+    lib.dsa_get_wait_limit_ns.restype = ctypes.c_uint64
     lib.dsa_abi_version.argtypes = []
     lib.dsa_abi_version.restype = i32
     _lib = lib
@@ -147,14 +153,18 @@ def dsa_latent_write(rows: Rows, kv_a: torch.Tensor, norm_w: torch.Tensor, pool:
 
 def dsa_index_scores(rows: Rows, q_idx: torch.Tensor, head_w: torch.Tensor, idx_k: torch.Tensor,
                      idx_gate: torch.Tensor, idx_base: torch.Tensor, rows_per_seq: int,
-                     max_len: int, scores: torch.Tensor, stream=None) -> None:
+                     max_len: int, scores: torch.Tensor, idx_written: torch.Tensor | None = None,
+                     stream=None) -> None:
+    """``idx_written``: optional int32 [R / rows_per_seq] rows written per
+    sequence; a row past its sequence's count is skipped and recorded."""
     lib = load()
     heads, dim = q_idx.shape[-2], q_idx.shape[-1]
     st = lib.dsa_index_scores(ctypes.byref(rows), _ptr(q_idx, torch.float32, "q_idx"),
                               _ptr(head_w, torch.float32, "head_w"), _ptr(idx_k, torch.uint16, "idx_k"),
                               _ptr(idx_gate, torch.uint16, "idx_gate"), idx_k.shape[0],
                               _ptr(idx_base, torch.int64, "idx_base"), heads, dim, int(rows_per_seq),
-                              int(max_len), _ptr(scores, torch.float32, "scores"), _stream(stream))
+                              int(max_len), _ptr(scores, torch.float32, "scores"),
+                              _ptr(idx_written, torch.int32, "idx_written"), _stream(stream))
     _check("dsa_index_scores", st)
 
 
@@ -204,19 +214,47 @@ def dsa_mla_decode_fp8_noalloc(rows: Rows, q: torch.Tensor, pool: torch.Tensor, 
     _check("dsa_mla_decode_fp8_noalloc", st)
 
 
+def dsa_select_pools(rows: Rows, pool_scores: torch.Tensor, pool_valid: torch.Tensor, kp: int,
+                     select_k: int, sel_pools: torch.Tensor, shared_valid: bool = False,
+                     stream=None) -> None:
+    """Top pools per row (score DESC, pool ASC) among the valid pools whose
+    last token is <= positions[r].  pool_scores float32 [R, P]; pool_valid
+    uint8 [R, P] (or [1, P] with shared_valid); sel_pools int32 [R, select_k]."""
+    lib = load()
+    max_pools = pool_scores.shape[-1]
+    st = lib.dsa_select_pools(ctypes.byref(rows), _ptr(pool_scores, torch.float32, "pool_scores"),
+                              max_pools, _ptr(pool_valid, torch.uint8, "pool_valid"),
+                              0 if shared_valid else pool_valid.shape[-1], int(kp), int(select_k),
+                              _ptr(sel_pools, torch.int32, "sel_pools"), _stream(stream))
+    _check("dsa_select_pools", st)
+
+
+def dsa_expand_selection(rows: Rows, sel_pools: torch.Tensor, kp: int, sel_tokens: torch.Tensor,
+                         stream=None) -> None:
+    """Pools to tokens plus the visible tail; sel_tokens int32 [R, out_width]."""
+    lib = load()
+    st = lib.dsa_expand_selection(ctypes.byref(rows), _ptr(sel_pools, torch.int32, "sel_pools"),
+                                  int(kp), sel_pools.shape[-1], _ptr(sel_tokens, torch.int32, "sel_tokens"),
+                                  sel_tokens.shape[-1], _stream(stream))
+    _check("dsa_expand_selection", st)
+
+
 def dsa_indexer_write(rows: Rows, k_raw: torch.Tensor, ln_w: torch.Tensor, ln_b: torch.Tensor,
                       eps: float, idx_base: torch.Tensor, idx_k: torch.Tensor,
                       idx_gate: torch.Tensor | None = None, gate: torch.Tensor | None = None,
+                      idx_written: torch.Tensor | None = None, rows_per_seq: int = 1,
                       stream=None) -> None:
     """LayerNorm (with bias) of each row's k_raw [R, D] bf16, stored into the
     key arena idx_k [T, D] at row idx_base[r] + positions[r] (and gate[r] into
-    idx_gate there when given)."""
+    idx_gate there when given).  With ``idx_written`` (int32 [R /
+    rows_per_seq]) the lockstep with the KV cache is checked and kept."""
     lib = load()
     st = lib.dsa_indexer_write(ctypes.byref(rows), _ptr(k_raw, torch.uint16, "k_raw"),
                                _ptr(ln_w, torch.uint16, "ln_w"), _ptr(ln_b, torch.uint16, "ln_b"),
                                float(eps), _ptr(gate, torch.uint16, "gate"),
                                _ptr(idx_base, torch.int64, "idx_base"), _ptr(idx_k, torch.uint16, "idx_k"),
                                _ptr(idx_gate, torch.uint16, "idx_gate"), idx_k.shape[0], idx_k.shape[1],
+                               _ptr(idx_written, torch.int32, "idx_written"), int(rows_per_seq),
                                _stream(stream))
     _check("dsa_indexer_write", st)
 
@@ -272,6 +310,15 @@ def dsa_get_error(reset: bool = True) -> tuple[int, int, int]:
 
 def dsa_bt_entries_needed(seq_len: int, k: int, block_size: int) -> int:
     return int(load().dsa_bt_entries_needed(int(seq_len), int(k), int(block_size)))
+
+
+def dsa_set_wait_limit_ns(limit_ns: int) -> None:
+    """Limit on the kernels' pipeline waits for later launches (0 = default)."""
+    _check("dsa_set_wait_limit_ns", load().dsa_set_wait_limit_ns(int(limit_ns)))
+
+
+def dsa_get_wait_limit_ns() -> int:
+    return int(load().dsa_get_wait_limit_ns())
 
 
 def dsa_abi_version() -> int:

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Never leave with a copy in flight: wait (bounded) for the last loads.
       for (int i = max(0, issued - kStages); i < issued; ++i)
-        mbar_wait(&ctl->full[i % kStages], (i / kStages) & 1, p.wait_ns);
+        mbar_wait(&ctl->full[i % kStages], (i / kStages) & 1, kDrainWaitNs);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The epilogue always gets its signal; after an abort it writes nothing.
       umma_commit(&ctl->tfull);
       umma_commit(&ctl->drain);
-      mbar_wait(&ctl->drain, 0, p.wait_ns);
+      mbar_wait(&ctl->drain, 0, kDrainWaitNs);
     }
   } else {
     // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. those weight rows.
@@ -170,7 +170,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool write = ok && !__shfl_sync(0xFFFFFFFFu, aborted(ctl) ? 1 : 0, 0);
     tc_fence_after();
     float v[16];
-    tmem_load16(tmem + (static_cast<uint32_t>(quarter * 32) << 16), v);
+    if (ok) {  // (uniform over the warp: tcgen05.ld is warp-collective)
+      tmem_load16(tmem + (static_cast<uint32_t>(quarter * 32) << 16), v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+    }
     grid_dep_wait();  // the kernel before may still read the output
     if (write && n < p.n) {
       if (p.splits > 1) {

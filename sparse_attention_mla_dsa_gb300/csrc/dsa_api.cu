@@ -4,6 +4,7 @@
 // (except dsa_get_error, which says so).
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "dsa_device.cuh"
@@ -26,6 +27,7 @@ DeviceInfo g_devices[kMaxDevices];
 std::mutex g_mutex;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
 
 const DeviceInfo* device_info() {
   int dev = 0;
@@ -80,6 +82,8 @@ int* device_error_word() {
   return d ? d->err : nullptr;
 }
 
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -115,7 +119,7 @@ dsa_status dsa_index_scores(const dsa_rows* rows, const float* q_idx, const floa
                             const uint16_t* idx_k, const uint16_t* idx_gate, int64_t idx_tokens,
                             const int64_t* idx_base, int32_t index_heads, int32_t index_dim,
                             int32_t rows_per_seq, int32_t max_len, float* scores,
-                            void* stream) {
+                            const int32_t* idx_written, void* stream) {
   dsa_status st = check_rows(rows, false);
   if (st != DSA_OK) return st;
   if (q_idx == nullptr || head_w == nullptr || idx_k == nullptr || idx_gate == nullptr ||
@@ -138,6 +142,7 @@ dsa_status dsa_index_scores(const dsa_rows* rows, const float* q_idx, const floa
   p.head_w = head_w;
   p.gate = idx_gate;
   p.idx_base = idx_base;
+  p.idx_written = idx_written;
   p.scores = scores;
   p.err = dev->err;
   p.idx_tokens = idx_tokens;
@@ -159,7 +164,7 @@ dsa_status dsa_index_scores(const dsa_rows* rows, const float* q_idx, const floa
   p.dim = index_dim;
   p.npad = ((sub * index_heads + 15) / 16) * 16;
   p.max_len = max_len;
-  p.wait_ns = kDefaultWaitNs;
+  p.wait_ns = wait_limit_ns();
   plan_index_scores(p, dev->num_sms);
 
   // Key arena [idx_tokens, index_dim] bf16, boxes of 128 tokens x 64 dims
@@ -238,7 +243,9 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   p.err = dev->err;
   p.kv_scale = kv_scale;
   p.sm_scale = sm_scale;
+  p.wait_ns = wait_limit_ns();
   plan_mla_decode_tc(p);
+  plan_mla_decode_speculation(p, dev->num_sms);
   const size_t need = mla_decode_tc_workspace_bytes(rows->rows, heads, topk);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
     return DSA_ERR_WORKSPACE;
@@ -266,10 +273,55 @@ size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
   return mla_decode_tc_workspace_bytes(rows, heads, topk);
 }
 
+dsa_status dsa_select_pools(const dsa_rows* rows, const float* pool_scores, int32_t max_pools,
+                            const uint8_t* pool_valid, int32_t valid_stride, int32_t kp,
+                            int32_t select_k, int32_t* sel_pools, void* stream) {
+  dsa_status st = check_rows(rows, false);
+  if (st != DSA_OK) return st;
+  if (rows->positions == nullptr || pool_scores == nullptr || pool_valid == nullptr ||
+      sel_pools == nullptr || kp < 1 || select_k < 1 || max_pools < 1 || valid_stride < 0 ||
+      (valid_stride != 0 && valid_stride < max_pools))
+    return DSA_ERR_INVALID_ARG;
+  if (max_pools > DSA_MAX_POOLS) return DSA_ERR_UNSUPPORTED;
+  PoolSelectParams p{};
+  p.positions = rows->positions;
+  p.scores = pool_scores;
+  p.valid = pool_valid;
+  p.sel_pools = sel_pools;
+  p.rows = rows->rows;
+  p.max_pools = max_pools;
+  p.valid_stride = valid_stride;
+  p.kp = kp;
+  p.select_k = select_k;
+  return launched(launch_select_pools(p, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_expand_selection(const dsa_rows* rows, const int32_t* sel_pools, int32_t kp,
+                                int32_t select_k, int32_t* sel_tokens, int32_t out_width,
+                                void* stream) {
+  dsa_status st = check_rows(rows, false);
+  if (st != DSA_OK) return st;
+  if (rows->positions == nullptr || sel_pools == nullptr || sel_tokens == nullptr || kp < 1 ||
+      select_k < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(out_width) < static_cast<int64_t>(select_k) * kp + kp - 1)
+    return DSA_ERR_INVALID_ARG;
+  PoolSelectParams p{};
+  p.positions = rows->positions;
+  p.sel_pools = const_cast<int32_t*>(sel_pools);
+  p.sel_tokens = sel_tokens;
+  p.rows = rows->rows;
+  p.kp = kp;
+  p.select_k = select_k;
+  p.out_width = out_width;
+  return launched(launch_expand_selection(p, static_cast<cudaStream_t>(stream)));
+}
+
 dsa_status dsa_indexer_write(const dsa_rows* rows, const uint16_t* k_raw, const uint16_t* ln_w,
                              const uint16_t* ln_b, float eps, const uint16_t* gate,
                              const int64_t* idx_base, uint16_t* idx_k, uint16_t* idx_gate,
-                             int64_t idx_tokens, int32_t index_dim, void* stream) {
+                             int64_t idx_tokens, int32_t index_dim, int32_t* idx_written,
+                             int32_t rows_per_seq, void* stream) {
   dsa_status st = check_rows(rows, false);
   if (st != DSA_OK) return st;
   if (rows->positions == nullptr || k_raw == nullptr || ln_w == nullptr || ln_b == nullptr ||
@@ -279,9 +331,14 @@ dsa_status dsa_indexer_write(const dsa_rows* rows, const uint16_t* k_raw, const 
   if (index_dim != 64 && index_dim != 128) return DSA_ERR_UNSUPPORTED;
   if (!(eps >= 0.0f)) return DSA_ERR_INVALID_ARG;
   if (!aligned(k_raw, 8) || !aligned(idx_k, 8)) return DSA_ERR_INVALID_ARG;
+  if (idx_written != nullptr &&
+      (rows_per_seq < 1 || rows_per_seq > 32 || rows->rows % rows_per_seq != 0))
+    return DSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = device_info();
   if (dev == nullptr) return DSA_ERR_CUDA;
   IndexerWriteParams p{};
+  p.idx_written = idx_written;
+  p.rows_per_seq = idx_written != nullptr ? rows_per_seq : 1;
   p.positions = rows->positions;
   p.seq_lens = rows->seq_lens;
   p.idx_base = idx_base;
@@ -337,7 +394,7 @@ dsa_status dsa_dense_mm_bf16(const uint16_t* a, const uint16_t* b, void* c, int3
   p.n = n_out;
   p.k = k;
   p.c_fp32 = c_fp32;
-  p.wait_ns = kDefaultWaitNs;
+  p.wait_ns = wait_limit_ns();
   plan_dense_mm(p, dev->num_sms);
   if (p.splits > 1) {
     const size_t need = static_cast<size_t>(p.splits) * m_rows * static_cast<size_t>(n_out) * 4;
@@ -401,6 +458,13 @@ const char* dsa_status_string(dsa_status status) {
   }
   return "unknown status";
 }
+
+dsa_status dsa_set_wait_limit_ns(uint64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns != 0 ? limit_ns : kDefaultWaitNs, std::memory_order_relaxed);
+  return DSA_OK;
+}
+
+uint64_t dsa_get_wait_limit_ns(void) { return wait_limit_ns(); }
 
 int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
 

@@ -75,10 +75,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same poll with a bound on how long the hardware may suspend the
+// thread inside it.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are short: every poll is bounded (32 ns suspend) and
+// followed by a look at the clock, so the limit holds to within a poll.
+constexpr uint64_t kShortWaitNs = 1000ull * 1000ull;
+
 // Wait for the phase with the given parity to complete.  Gives up after
-// `limit_ns` of wall time (checked every 256 polls) or 2^30 polls, whichever
-// comes first, and returns false then.
+// `limit_ns` of wall time (checked every 256 polls, every poll for a short
+// limit) or 2^30 polls, whichever comes first, and returns false then.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns < kShortWaitNs) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 30); ++i) {
+      if (mbar_try_wait_hint(bar, parity, 32)) return true;
+      if (global_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {

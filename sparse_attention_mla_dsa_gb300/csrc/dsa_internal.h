@@ -24,8 +24,15 @@ inline cudaLaunchAttribute dependent_launch_attr() {
 // failure); kernels receive it as an argument.
 int* device_error_word();
 
-// Bound on every mbarrier wait in the kernels (wall time).
+// Bound on every pipeline wait in the kernels (wall time); dsa_set_wait_limit_ns
+// changes it for later launches.
 constexpr uint64_t kDefaultWaitNs = 500ull * 1000ull * 1000ull;
+uint64_t wait_limit_ns();
+// Bound on the drain at the end of a CTA -- the waits for its own TMA copies
+// and MMAs still in flight before TMEM is released and the CTA exits.  It is
+// never shortened: a pipeline wait that gave up must not leave a copy or an
+// MMA running behind the CTA.
+constexpr uint64_t kDrainWaitNs = 500ull * 1000ull * 1000ull;
 
 struct LatentWriteParams {
   dsa_rows rows;
@@ -45,6 +52,7 @@ struct IndexParams {
   const float* head_w;
   const uint16_t* gate;
   const int64_t* idx_base;
+  const int32_t* idx_written;  // [sequences] rows written per sequence, or nullptr
   float* scores;
   int* err;
   int64_t idx_tokens;
@@ -60,6 +68,7 @@ struct IndexParams {
   int32_t stages;         // smem pipeline depth
   uint32_t tmem_cols;
   uint32_t smem_bytes;
+  int32_t speculate;      // build the q operand before the dependency wait (one-wave launches)
   uint64_t wait_ns;
 };
 // Fills in chunk_tiles / stages / tmem_cols / smem_bytes from the shape.
@@ -81,6 +90,23 @@ int topk_cluster_size(int32_t max_len);
 size_t topk_smem_bytes(int32_t max_len, int cluster);
 cudaError_t launch_select_topk(const TopkParams& p, cudaStream_t stream);
 
+struct PoolSelectParams {
+  const uint32_t* positions;  // [rows] q_pos
+  const float* scores;        // [rows][max_pools]
+  const uint8_t* valid;       // row r at valid + r*valid_stride, [max_pools]
+  int32_t* sel_pools;         // [rows][select_k]
+  int32_t* sel_tokens;        // [rows][out_width]
+  int32_t rows;
+  int32_t max_pools;
+  int32_t valid_stride;
+  int32_t kp;
+  int32_t select_k;
+  int32_t out_width;
+};
+size_t select_pools_smem_bytes(int32_t max_pools);
+cudaError_t launch_select_pools(const PoolSelectParams& p, cudaStream_t stream);
+cudaError_t launch_expand_selection(const PoolSelectParams& p, cudaStream_t stream);
+
 struct IndexerWriteParams {
   const uint32_t* positions;
   const int32_t* seq_lens;
@@ -91,8 +117,10 @@ struct IndexerWriteParams {
   const uint16_t* gate;    // [rows] bf16 or nullptr
   uint16_t* idx_k;         // [idx_tokens][dim] bf16
   uint16_t* idx_gate;      // [idx_tokens] bf16
+  int32_t* idx_written;    // [sequences] rows written per sequence, or nullptr
   int64_t idx_tokens;
   int32_t rows;
+  int32_t rows_per_seq;    // rows of one sequence (consecutive positions), with idx_written
   int32_t dim;
   float eps;
   int* err;
@@ -134,11 +162,16 @@ struct DecodeParams {
   int32_t heads;
   int32_t splits;
   int32_t split_len;   // selection entries per split (cluster form)
+  int32_t speculate;   // convert Q before the dependency wait (one-wave launches)
+  uint64_t wait_ns;    // pipeline wait limit
   float kv_scale;
   float sm_scale;
 };
 // Split count / length of the gather-attend (a function of topk only).
 void plan_mla_decode_tc(DecodeParams& p);
+// Whether a launch of this shape fits one wave on num_sms SMs (then Q is
+// converted before the dependency wait).
+void plan_mla_decode_speculation(DecodeParams& p, int num_sms);
 size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 void mla_decode_tc_bind_workspace(DecodeParams& p, void* workspace);
 // Split kernel (tcgen05) followed by the merge kernel.  `pmap` describes the

@@ -125,9 +125,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int sb = 0; sb < kSub; ++sb) tma_prefetch_l2_2d(&kmap, sb * 64, static_cast<int32_t>(y));
     }
   }
-  for (int off = threadIdx.x * 32; off < nreal * D; off += kThreads * 32)
-    prefetch_l2(qsrc + off);  // 128-byte lines
+  // B operand: q split into bf16 hi + lo, written in the 128-byte-swizzled
+  // K-major layout the MMA descriptor expects (row n at n*128 B inside a
+  // 64-element sub-tile, 16-byte chunk c stored at chunk c ^ (n % 8)).
+  // Vector v is 8 floats of q row n = v / (D/8); eight vectors per thread are
+  // loaded before any is used (one round trip per eight vectors).
+  const int vec_per_row = D / 8;
+  const int nvec = npad * vec_per_row;
+  constexpr int kBatch = 8;
+  auto load_batch = [&](int v0, float4 (&u)[kBatch][2]) {
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int v = v0 + k * kThreads;
+      const int n = v / vec_per_row, c8 = v % vec_per_row;
+      if (v < nvec && n < nreal) {
+        const float4* src = reinterpret_cast<const float4*>(qsrc + static_cast<int64_t>(n) * D + c8 * 8);
+        u[k][0] = ld_dep_f4(src);
+        u[k][1] = ld_dep_f4(src + 1);
+      } else {
+        u[k][0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        u[k][1] = u[k][0];
+      }
+    }
+  };
+  auto convert_vec = [&](int v, const float4& u0, const float4& u1) {
+    const int n = v / vec_per_row, c8 = v % vec_per_row;
+    const float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(x[2 * i]);
+      const __nv_bfloat16 h1 = __float2bfloat16_rn(x[2 * i + 1]);
+      const float r0f = x[2 * i] - __bfloat162float(h0);
+      const float r1f = x[2 * i + 1] - __bfloat162float(h1);
+      hi[i] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
+      lo[i] = pack_bf16x2(r0f, r1f);
+    }
+    const int sb = (c8 * 8) / 64, chunk = c8 & 7;
+    const uint32_t off = sb * (npad * 128) + n * 128 + ((chunk ^ (n & 7)) * 16);
+    *reinterpret_cast<uint4*>(b_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(b_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  };
+  auto head_weight = [&](int n) {
+    return n < nreal ? *reinterpret_cast<const volatile float*>(p.head_w + static_cast<int64_t>(r0) * p.heads + n)
+                     : 0.0f;
+  };
+  // In a launch that fits one wave (set by the host), when one batch holds
+  // the whole operand (every decode launch group: npad * D / 8 <= 8 * 192),
+  // q and the head weights are loaded and converted speculatively before the
+  // dependency wait, overlapping the kernel before, and read again after it:
+  // a vector or weight that changed in between is converted again, so the
+  // operand always holds the values of after the wait.  Otherwise (larger
+  // operands, or launches whose later CTAs start after the kernel before has
+  // finished, where the second read would only cost) it is built after the
+  // wait.
+  // The raw speculative values are kept in the key-tile stages, which no TMA
+  // fills before the wait.
+  const bool spec = p.speculate != 0 && nvec <= kBatch * kThreads &&
+                    static_cast<uint32_t>(nvec) * 32u <= static_cast<uint32_t>(stages) * kStageBytes;
+  float4* raw = reinterpret_cast<float4*>(stage_base);  // [nvec][2] float4
+  float4 u[kBatch][2];
+  float w_spec = 0.0f;
+  if (spec) {
+    load_batch(threadIdx.x, u);
+    if (threadIdx.x < npad) w_spec = head_weight(threadIdx.x);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int v = threadIdx.x + k * kThreads;
+      if (v < nvec) {
+        convert_vec(v, u[k][0], u[k][1]);
+        raw[2 * v] = u[k][0];
+        raw[2 * v + 1] = u[k][1];
+      }
+    }
+    if (threadIdx.x < npad) w_s[threadIdx.x] = w_spec;
+  } else {
+    for (int off = threadIdx.x * 32; off < nreal * D; off += kThreads * 32)
+      prefetch_l2(qsrc + off);  // 128-byte lines
+  }
+  if (threadIdx.x < nrows) {
+    prefetch_l2(p.seq_lens + r0 + threadIdx.x);
+    prefetch_l2(p.idx_base + r0 + threadIdx.x);
+  }
   grid_dep_wait();
+
+  if (spec) {  // q and head weights again (L2 hits), issued with the metadata loads
+    load_batch(threadIdx.x, u);
+    const float w2 = threadIdx.x < npad ? head_weight(threadIdx.x) : 0.0f;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int v = threadIdx.x + k * kThreads;
+      if (v < nvec) {
+        const float4 a = raw[2 * v], b = raw[2 * v + 1];
+        const bool same = __float_as_uint(u[k][0].x) == __float_as_uint(a.x) &&
+                          __float_as_uint(u[k][0].y) == __float_as_uint(a.y) &&
+                          __float_as_uint(u[k][0].z) == __float_as_uint(a.z) &&
+                          __float_as_uint(u[k][0].w) == __float_as_uint(a.w) &&
+                          __float_as_uint(u[k][1].x) == __float_as_uint(b.x) &&
+                          __float_as_uint(u[k][1].y) == __float_as_uint(b.y) &&
+                          __float_as_uint(u[k][1].z) == __float_as_uint(b.z) &&
+                          __float_as_uint(u[k][1].w) == __float_as_uint(b.w);
+        if (!same) convert_vec(v, u[k][0], u[k][1]);
+      }
+    }
+    if (threadIdx.x < npad && __float_as_uint(w2) != __float_as_uint(w_spec)) w_s[threadIdx.x] = w2;
+  }
 
   // Row lengths and arena bases: one load per row, all rows in parallel.
   if (threadIdx.x < 32) {
@@ -144,6 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         len = 0;
       } else if (rb != base || base < 0 || base + len > p.idx_tokens) {
         if (report) record_error(p.err, DSA_DEVERR_ARENA, r);
+        len = 0;
+      } else if (p.idx_written != nullptr && len > p.idx_written[seq]) {
+        // the sequence's keys stop before this row's range: rows never written
+        if (report) record_error(p.err, DSA_DEVERR_BEHIND, r);
         len = 0;
       }
       ctl->row_len[j] = len;
@@ -169,6 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int issued = 0;
   if (threadIdx.x == 0) {
     policy = l2_policy_evict_first();
+    // The stages held the speculative q (generic-proxy writes) before the
+    // barrier above; order them before the TMA writes into the same bytes.
+    if (spec) fence_proxy_async_smem();
     // The first `stages` tiles need no empty-slot wait.
     for (; issued < min(stages, ntiles); ++issued) {
       uint8_t* dst = stage_base + issued * kStageBytes;
@@ -183,58 +292,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ctl->tmem_base, p.tmem_cols);
     tmem_relinquish();
   }
-
-  // B operand: q split into bf16 hi + lo, written in the 128-byte-swizzled
-  // K-major layout the MMA descriptor expects (row n at n*128 B inside a
-  // 64-element sub-tile, 16-byte chunk c stored at chunk c ^ (n % 8)).
-  {
-    const int vec_per_row = D / 8;
-    const int nvec = npad * vec_per_row;
-    // Up to eight 8-float vectors per thread are loaded before any is used,
-    // so the operand costs one round trip per eight vectors, not per vector.
-    constexpr int kBatch = 8;
+  if (!spec) {
     for (int v0 = threadIdx.x; v0 < nvec; v0 += kBatch * kThreads) {
-      float4 u[kBatch][2];
+      load_batch(v0, u);
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int v = v0 + k * kThreads;
-        const int n = v / vec_per_row, c8 = v % vec_per_row;
-        if (v < nvec && n < nreal) {
-          const float4* src = reinterpret_cast<const float4*>(qsrc + static_cast<int64_t>(n) * D + c8 * 8);
-          u[k][0] = ld_dep_f4(src);
-          u[k][1] = ld_dep_f4(src + 1);
-        } else {
-          u[k][0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          u[k][1] = u[k][0];
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int v = v0 + k * kThreads;
-        if (v >= nvec) break;
-        const int n = v / vec_per_row, c8 = v % vec_per_row;
-        const float x[8] = {u[k][0].x, u[k][0].y, u[k][0].z, u[k][0].w,
-                            u[k][1].x, u[k][1].y, u[k][1].z, u[k][1].w};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(x[2 * i]);
-          const __nv_bfloat16 h1 = __float2bfloat16_rn(x[2 * i + 1]);
-          const float r0f = x[2 * i] - __bfloat162float(h0);
-          const float r1f = x[2 * i + 1] - __bfloat162float(h1);
-          hi[i] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-          lo[i] = pack_bf16x2(r0f, r1f);
-        }
-        const int sb = (c8 * 8) / 64, chunk = c8 & 7;
-        const uint32_t off = sb * (npad * 128) + n * 128 + ((chunk ^ (n & 7)) * 16);
-        *reinterpret_cast<uint4*>(b_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(b_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if (v < nvec) convert_vec(v, u[k][0], u[k][1]);
       }
     }
-    for (int n = threadIdx.x; n < npad; n += kThreads)
-      w_s[n] = n < nreal ? p.head_w[static_cast<int64_t>(r0) * p.heads + n] : 0.0f;
-    fence_proxy_async_smem();  // generic-proxy smem writes -> visible to the MMA
+    for (int n = threadIdx.x; n < npad; n += kThreads) w_s[n] = head_weight(n);
   }
+  fence_proxy_async_smem();  // generic-proxy smem writes -> visible to the MMA
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -260,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Never leave with a copy in flight: wait (bounded) for the last loads.
       for (int i = max(0, issued - stages); i < issued; ++i)
-        mbar_wait(&ctl->full[i % stages], (i / stages) & 1, p.wait_ns);
+        mbar_wait(&ctl->full[i % stages], (i / stages) & 1, kDrainWaitNs);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -296,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every MMA issued by this thread is complete before TMEM is released.
       umma_commit(&ctl->drain);
-      mbar_wait(&ctl->drain, 0, p.wait_ns);
+      mbar_wait(&ctl->drain, 0, kDrainWaitNs);
     }
   } else {
     // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. those tokens.
@@ -389,6 +458,9 @@ void plan_index_scores(IndexParams& p, int num_sms) {
   if (stages < 1) stages = 1;
   p.stages = stages;
   p.smem_bytes = fixed + stages * stage_bytes;
+  // One wave: every CTA resident at once (two per SM).
+  const int64_t ctas = ((tiles_max + chunk - 1) / chunk) * groups;
+  p.speculate = ctas <= 2LL * num_sms ? 1 : 0;
 
   uint32_t cols = 32;
   while (cols < 2u * p.npad) cols <<= 1;

@@ -8,7 +8,17 @@
 // place, placement from a device-side position by dsa_indexer_store so that a
 // captured graph does not freeze a host offset).
 //
-// One warp per row, index_dim / 32 elements per lane.  The statistics and the
+// The lockstep of the indexer cache with the KV cache (decode_k: the
+// indexer's length must equal the sequence length before the step; a longer
+// cache is the leftover of a rejected verify and is rewound, a shorter one
+// means rows were never written and is a hard error): with a per-sequence
+// counter of written rows, the rows of a sequence (consecutive positions
+// p0, p0+1, ... of one call) are written only when the counter is at least
+// p0, and the counter becomes p0 + rows afterwards; a counter below p0 is
+// recorded as DSA_DEVERR_BEHIND and nothing of that sequence is written.
+//
+// One warp per row, index_dim / 32 elements per lane; with the counter, one
+// CTA per sequence (a warp per row of it).  The statistics and the
 // affine map are taken in double (at most 128 elements per row), and the
 // result is rounded to bf16 once: round-to-odd from double to float, then
 // round-to-nearest-even from float to bf16, which equals a direct
@@ -31,37 +41,21 @@ __device__ __forceinline__ uint16_t bf16_rne_from_double(double v) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32) indexer_write_kernel(const IndexerWriteParams p) {
+__device__ __forceinline__ void write_row(const IndexerWriteParams& p, int r, int lane,
+                                          const double (&w)[D / 32], const double (&b)[D / 32]) {
   constexpr int kPer = D / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * kWarps + warp;
-  grid_dep_launch();
-  if (r >= p.rows) return;  // whole warps only
-
-  // The norm's weight and bias are weights (no kernel of a chain writes
-  // them) and are read before the wait; the row metadata, k_raw and the gate
-  // may come from kernels before, and the arena may still be read by one.
-  double w[kPer], b[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    w[i] = static_cast<double>(__uint_as_float(static_cast<uint32_t>(p.ln_w[lane * kPer + i]) << 16));
-    b[i] = static_cast<double>(__uint_as_float(static_cast<uint32_t>(p.ln_b[lane * kPer + i]) << 16));
-  }
-  grid_dep_wait();
   const int64_t pos = p.positions[r];
   const int64_t len = p.seq_lens[r];
   const int64_t base = p.idx_base[r];
   const int64_t t = base + pos;
-  bool ok = true;
   if (pos + 1 != len) {
     if (lane == 0) record_error(p.err, DSA_DEVERR_POSITION, r);
-    ok = false;
-  } else if (base < 0 || t < 0 || t >= p.idx_tokens) {
-    if (lane == 0) record_error(p.err, DSA_DEVERR_ARENA, r);
-    ok = false;
+    return;
   }
-
-  if (!ok) return;
+  if (base < 0 || t < 0 || t >= p.idx_tokens) {
+    if (lane == 0) record_error(p.err, DSA_DEVERR_ARENA, r);
+    return;
+  }
   double x[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i)
@@ -93,16 +87,81 @@ __global__ void __launch_bounds__(kWarps * 32) indexer_write_kernel(const Indexe
   if (p.gate != nullptr && lane == 0) p.idx_gate[t] = p.gate[r];
 }
 
+template <int D>
+__device__ __forceinline__ void load_norm(const IndexerWriteParams& p, int lane, double (&w)[D / 32],
+                                          double (&b)[D / 32]) {
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) {
+    w[i] = static_cast<double>(__uint_as_float(static_cast<uint32_t>(p.ln_w[lane * (D / 32) + i]) << 16));
+    b[i] = static_cast<double>(__uint_as_float(static_cast<uint32_t>(p.ln_b[lane * (D / 32) + i]) << 16));
+  }
+}
+
+// Without the counter: one warp per row, four rows per CTA.
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) indexer_write_kernel(const IndexerWriteParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kWarps + warp;
+  grid_dep_launch();
+  if (r >= p.rows) return;  // whole warps only
+  // The norm's weight and bias are weights (no kernel of a chain writes
+  // them) and are read before the wait; the row metadata, k_raw and the gate
+  // may come from kernels before, and the arena may still be read by one.
+  double w[D / 32], b[D / 32];
+  load_norm<D>(p, lane, w, b);
+  grid_dep_wait();
+  write_row<D>(p, r, lane, w, b);
+}
+
+// With the counter: one CTA per sequence, a warp per row of it.
+template <int D>
+__global__ void __launch_bounds__(32 * 32) indexer_write_lockstep_kernel(const IndexerWriteParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seq = blockIdx.x, r0 = seq * p.rows_per_seq;
+  __shared__ int write_ok;
+  grid_dep_launch();
+  double w[D / 32], b[D / 32];
+  load_norm<D>(p, lane, w, b);
+  grid_dep_wait();
+  if (threadIdx.x == 0) {
+    const int64_t written = p.idx_written[seq];
+    const int64_t p0 = p.positions[r0];
+    // behind: rows [written, p0) of this sequence were never written
+    write_ok = written >= p0 ? 1 : 0;
+    if (!write_ok) record_error(p.err, DSA_DEVERR_BEHIND, r0);
+  }
+  __syncthreads();
+  if (write_ok && warp < p.rows_per_seq) {
+    const int r = r0 + warp;
+    if (static_cast<int64_t>(p.positions[r]) != static_cast<int64_t>(p.positions[r0]) + warp) {
+      if (lane == 0) record_error(p.err, DSA_DEVERR_POSITION, r);
+    } else {
+      write_row<D>(p, r, lane, w, b);
+    }
+  }
+  __syncthreads();
+  // ahead (a rejected verify's rows) or level: the sequence now holds
+  // exactly the rows up to its last new position
+  if (threadIdx.x == 0 && write_ok)
+    p.idx_written[seq] = static_cast<int32_t>(static_cast<int64_t>(p.positions[r0]) + p.rows_per_seq);
+}
+
 }  // namespace
 
 cudaError_t launch_indexer_write(const IndexerWriteParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((p.rows + kWarps - 1) / kWarps), 1, 1);
-  cfg.blockDim = dim3(kWarps * 32, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1] = {dependent_launch_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.idx_written != nullptr) {
+    cfg.gridDim = dim3(static_cast<unsigned>(p.rows / p.rows_per_seq), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * p.rows_per_seq), 1, 1);
+    if (p.dim == 64) return cudaLaunchKernelEx(&cfg, indexer_write_lockstep_kernel<64>, p);
+    return cudaLaunchKernelEx(&cfg, indexer_write_lockstep_kernel<128>, p);
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>((p.rows + kWarps - 1) / kWarps), 1, 1);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
   if (p.dim == 64) return cudaLaunchKernelEx(&cfg, indexer_write_kernel<64>, p);
   return cudaLaunchKernelEx(&cfg, indexer_write_kernel<128>, p);
 }

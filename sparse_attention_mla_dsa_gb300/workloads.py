@@ -19,6 +19,8 @@ verify     8 seqs x 4 rows (lens base..base+3), base ~ U[65536, 131072]
 long       64 seqs x 1 row, len log-uniform [4096, 131072], 128 heads, index
            64x128, pool twice the size needed with free blocks interleaved, and
            the new row's latent written by the latent-write step first
+prefill    1 seq x 1024 rows (a 9,000-token prompt's last 1,024 positions, lens
+           7977..9000), 64 heads, index 32x128, topk 2048
 =========  =====================================================================
 
 Value distributions: latent ~ N(0,1) stored as fp8(x / kv_scale) with
@@ -237,6 +239,12 @@ NAMED = {
     "long": dict(seed=4, seqs=64, rows_per_seq=1, len_kind="loguniform", len_lo=4096,
                  len_hi=131072, heads=128, index_heads=64, index_dim=128, topk=2048,
                  free_fraction=0.5, with_write=True),
+    # Prefill selection in one pass ("glm5next_dsa/layer.rs", select_rows_batched:
+    # the rows of a 9,000-token prefill selected together, each under its own
+    # causal horizon): the last 1,024 tokens of a 9,000-token prompt as query
+    # rows of one sequence, row j seeing tokens [0, 7977 + j).
+    "prefill": dict(seed=7, seqs=1, rows_per_seq=1024, len_kind="fixed", len_lo=7977,
+                    len_hi=7977, heads=64, index_heads=32, index_dim=128, topk=2048),
 }
 
 

@@ -208,3 +208,73 @@ def test_rewind_after_a_rejected_verify(api, oracle):
     s, A, M = oracle.index_scores_row(q[0], w[0], arena.view(np.uint16),
                                       idx_gate.cpu().numpy().view(np.uint16), L + 2)
     parity.assert_scores(scores.cpu().numpy()[0], s, A, M, "rewound row")
+
+
+def test_lockstep_counter_level_ahead_and_behind(api, oracle):
+    """The indexer cache in lockstep with the KV cache ("glm5next_dsa/layer.rs",
+    decode_k): with a per-sequence count of written rows, a write at positions
+    p0.. proceeds when the count is p0 (level) or above it (a rejected
+    verify's leftover rows: rewound), and sets the count to p0 + rows; a count
+    below p0 (rows never written) is refused as DSA_DEVERR_BEHIND and nothing
+    of that sequence is written.  The indexer then refuses a row whose
+    seq_len exceeds its sequence's count, and scores the others at parity."""
+    rng = np.random.default_rng(33)
+    D, G, T = 128, 4, 3000
+    seqs = 3
+    R = seqs * G
+    # sequence 0 level (count 100), 1 ahead (count 330, a rejected verify), 2 behind (count 590)
+    p0 = [100, 300, 600]
+    counts = [100, 330, 590]
+    base = np.array([0, 1000, 2000], np.int64)
+    positions = [p0[s] + j for s in range(seqs) for j in range(G)]
+    seq_lens = [p + 1 for p in positions]
+    rows, keep = _rows(api, seq_lens, positions)
+    k_raw = torch.from_numpy(_bf16(rng.standard_normal((R, D))).view(np.int16)).cuda()
+    ln_w = torch.from_numpy(_bf16(1.0 + 0.1 * rng.standard_normal(D)).view(np.int16)).cuda()
+    ln_b = torch.from_numpy(_bf16(0.1 * rng.standard_normal(D)).view(np.int16)).cuda()
+    arena0 = _bf16(rng.standard_normal((T, D)))
+    idx_k = torch.from_numpy(arena0.view(np.int16).copy()).cuda()
+    idx_base = torch.from_numpy(np.repeat(base, G)).cuda()
+    written = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    api.dsa_indexer_write(rows, k_raw, ln_w, ln_b, 1e-6, idx_base, idx_k, idx_written=written,
+                          rows_per_seq=G)
+    torch.cuda.synchronize()
+    code, row, count = api.dsa_get_error(reset=True)
+    assert api.DEVERR[code] == "behind" and row == 2 * G and count == 1
+    assert written.cpu().tolist() == [p0[0] + G, p0[1] + G, counts[2]]
+    got = idx_k.cpu().numpy().view(np.uint16)
+    for s in range(seqs):
+        for j in range(G):
+            t = int(base[s]) + p0[s] + j
+            if s == 2:
+                assert np.array_equal(got[t], arena0[t]), "a behind sequence must not be written"
+            else:
+                y, _ = oracle.layer_norm_row(k_raw[s * G + j].cpu().numpy().view(np.uint16),
+                                             ln_w.cpu().numpy().view(np.uint16),
+                                             ln_b.cpu().numpy().view(np.uint16), 1e-6)
+                want, tie = _bf16_rne(y)
+                assert not ((got[t] != want) & ~tie).any()
+    # the indexer: rows of sequences 0 and 1 score at parity, sequence 2 is refused
+    Hi = 32
+    q = rng.standard_normal((R, Hi, D)).astype(np.float32)
+    w = (rng.standard_normal((R, Hi)) * Hi ** -0.5).astype(np.float32)
+    gate = torch.from_numpy(_bf16(np.full(T, 0.5)).view(np.int16)).cuda()
+    max_len = max(seq_lens)
+    scores = torch.full((R, max_len), float("nan"), dtype=torch.float32, device="cuda")
+    api.dsa_index_scores(rows, torch.from_numpy(q).cuda(), torch.from_numpy(w).cuda(), idx_k, gate,
+                         idx_base, G, max_len, scores, idx_written=written)
+    torch.cuda.synchronize()
+    code, row, _ = api.dsa_get_error(reset=True)
+    assert api.DEVERR[code] == "behind" and 2 * G <= row < 3 * G
+    sc = scores.cpu().numpy()
+    k_np = idx_k.cpu().numpy().view(np.uint16)
+    g_np = gate.cpu().numpy().view(np.uint16)
+    for r in range(R):
+        L = seq_lens[r]
+        if r >= 2 * G:
+            assert np.isnan(sc[r]).all(), "a refused row is not scored"
+            continue
+        s_, A, M = oracle.index_scores_row(q[r], w[r], k_np[int(idx_base[r]):], g_np[int(idx_base[r]):], L)
+        from tests import parity
+        parity.assert_scores(sc[r, :L], s_, A, M, f"row {r}")
+    del keep
