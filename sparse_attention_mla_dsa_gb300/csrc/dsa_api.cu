@@ -245,7 +245,6 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   p.sm_scale = sm_scale;
   p.wait_ns = wait_limit_ns();
   plan_mla_decode_tc(p);
-  plan_mla_decode_speculation(p, dev->num_sms);
   const size_t need = mla_decode_tc_workspace_bytes(rows->rows, heads, topk);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
     return DSA_ERR_WORKSPACE;

@@ -93,25 +93,30 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
 // followed by a look at the clock, so the limit holds to within a poll.
 constexpr uint64_t kShortWaitNs = 1000ull * 1000ull;
 
-// Wait for the phase with the given parity to complete.  Gives up after
-// `limit_ns` of wall time (checked every 256 polls, every poll for a short
-// limit) or 2^30 polls, whichever comes first, and returns false then.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+// The polling loop of mbar_wait, out of line so that the kernels' wait sites
+// stay small (a wait that gets here is waiting anyway).
+static __device__ __noinline__ bool mbar_wait_polls(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
   if (limit_ns < kShortWaitNs) {
-    const uint64_t t0 = global_ns();
     for (uint32_t i = 0; i < (1u << 30); ++i) {
       if (mbar_try_wait_hint(bar, parity, 32)) return true;
       if (global_ns() - t0 > limit_ns) return false;
     }
     return false;
   }
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
   }
   return false;
+}
+
+// Wait for the phase with the given parity to complete.  Gives up after
+// `limit_ns` of wall time (checked every 256 polls, every poll for a short
+// limit) or 2^30 polls, whichever comes first, and returns false then.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns >= kShortWaitNs && mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_polls(bar, parity, limit_ns);
 }
 
 // ------------------------------------------------------------------ dependent launch

@@ -68,7 +68,6 @@ struct IndexParams {
   int32_t stages;         // smem pipeline depth
   uint32_t tmem_cols;
   uint32_t smem_bytes;
-  int32_t speculate;      // build the q operand before the dependency wait (one-wave launches)
   uint64_t wait_ns;
 };
 // Fills in chunk_tiles / stages / tmem_cols / smem_bytes from the shape.
@@ -162,16 +161,12 @@ struct DecodeParams {
   int32_t heads;
   int32_t splits;
   int32_t split_len;   // selection entries per split (cluster form)
-  int32_t speculate;   // convert Q before the dependency wait (one-wave launches)
   uint64_t wait_ns;    // pipeline wait limit
   float kv_scale;
   float sm_scale;
 };
 // Split count / length of the gather-attend (a function of topk only).
 void plan_mla_decode_tc(DecodeParams& p);
-// Whether a launch of this shape fits one wave on num_sms SMs (then Q is
-// converted before the dependency wait).
-void plan_mla_decode_speculation(DecodeParams& p, int num_sms);
 size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 void mla_decode_tc_bind_workspace(DecodeParams& p, void* workspace);
 // Split kernel (tcgen05) followed by the merge kernel.  `pmap` describes the

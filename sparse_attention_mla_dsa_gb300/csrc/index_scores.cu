@@ -170,66 +170,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     return n < nreal ? *reinterpret_cast<const volatile float*>(p.head_w + static_cast<int64_t>(r0) * p.heads + n)
                      : 0.0f;
   };
-  // In a launch that fits one wave (set by the host), when one batch holds
-  // the whole operand (every decode launch group: npad * D / 8 <= 8 * 192),
-  // q and the head weights are loaded and converted speculatively before the
-  // dependency wait, overlapping the kernel before, and read again after it:
-  // a vector or weight that changed in between is converted again, so the
-  // operand always holds the values of after the wait.  Otherwise (larger
-  // operands, or launches whose later CTAs start after the kernel before has
-  // finished, where the second read would only cost) it is built after the
-  // wait.
-  // The raw speculative values are kept in the key-tile stages, which no TMA
-  // fills before the wait.
-  const bool spec = p.speculate != 0 && nvec <= kBatch * kThreads &&
-                    static_cast<uint32_t>(nvec) * 32u <= static_cast<uint32_t>(stages) * kStageBytes;
-  float4* raw = reinterpret_cast<float4*>(stage_base);  // [nvec][2] float4
-  float4 u[kBatch][2];
-  float w_spec = 0.0f;
-  if (spec) {
-    load_batch(threadIdx.x, u);
-    if (threadIdx.x < npad) w_spec = head_weight(threadIdx.x);
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int v = threadIdx.x + k * kThreads;
-      if (v < nvec) {
-        convert_vec(v, u[k][0], u[k][1]);
-        raw[2 * v] = u[k][0];
-        raw[2 * v + 1] = u[k][1];
-      }
-    }
-    if (threadIdx.x < npad) w_s[threadIdx.x] = w_spec;
-  } else {
-    for (int off = threadIdx.x * 32; off < nreal * D; off += kThreads * 32)
-      prefetch_l2(qsrc + off);  // 128-byte lines
-  }
+  // q and the head weights may come from the kernel before: prefetched into
+  // L2 here, loaded and converted after the wait.
+  for (int off = threadIdx.x * 32; off < nreal * D; off += kThreads * 32)
+    prefetch_l2(qsrc + off);  // 128-byte lines
   if (threadIdx.x < nrows) {
     prefetch_l2(p.seq_lens + r0 + threadIdx.x);
     prefetch_l2(p.idx_base + r0 + threadIdx.x);
   }
   grid_dep_wait();
-
-  if (spec) {  // q and head weights again (L2 hits), issued with the metadata loads
-    load_batch(threadIdx.x, u);
-    const float w2 = threadIdx.x < npad ? head_weight(threadIdx.x) : 0.0f;
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int v = threadIdx.x + k * kThreads;
-      if (v < nvec) {
-        const float4 a = raw[2 * v], b = raw[2 * v + 1];
-        const bool same = __float_as_uint(u[k][0].x) == __float_as_uint(a.x) &&
-                          __float_as_uint(u[k][0].y) == __float_as_uint(a.y) &&
-                          __float_as_uint(u[k][0].z) == __float_as_uint(a.z) &&
-                          __float_as_uint(u[k][0].w) == __float_as_uint(a.w) &&
-                          __float_as_uint(u[k][1].x) == __float_as_uint(b.x) &&
-                          __float_as_uint(u[k][1].y) == __float_as_uint(b.y) &&
-                          __float_as_uint(u[k][1].z) == __float_as_uint(b.z) &&
-                          __float_as_uint(u[k][1].w) == __float_as_uint(b.w);
-        if (!same) convert_vec(v, u[k][0], u[k][1]);
-      }
-    }
-    if (threadIdx.x < npad && __float_as_uint(w2) != __float_as_uint(w_spec)) w_s[threadIdx.x] = w2;
-  }
 
   // Row lengths and arena bases: one load per row, all rows in parallel.
   if (threadIdx.x < 32) {
@@ -275,9 +224,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   int issued = 0;
   if (threadIdx.x == 0) {
     policy = l2_policy_evict_first();
-    // The stages held the speculative q (generic-proxy writes) before the
-    // barrier above; order them before the TMA writes into the same bytes.
-    if (spec) fence_proxy_async_smem();
     // The first `stages` tiles need no empty-slot wait.
     for (; issued < min(stages, ntiles); ++issued) {
       uint8_t* dst = stage_base + issued * kStageBytes;
@@ -292,7 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ctl->tmem_base, p.tmem_cols);
     tmem_relinquish();
   }
-  if (!spec) {
+  {
+    float4 u[kBatch][2];
     for (int v0 = threadIdx.x; v0 < nvec; v0 += kBatch * kThreads) {
       load_batch(v0, u);
 #pragma unroll
@@ -458,9 +405,6 @@ void plan_index_scores(IndexParams& p, int num_sms) {
   if (stages < 1) stages = 1;
   p.stages = stages;
   p.smem_bytes = fixed + stages * stage_bytes;
-  // One wave: every CTA resident at once (two per SM).
-  const int64_t ctas = ((tiles_max + chunk - 1) / chunk) * groups;
-  p.speculate = ctas <= 2LL * num_sms ? 1 : 0;
 
   uint32_t cols = 32;
   while (cols < 2u * p.npad) cols <<= 1;

@@ -230,51 +230,6 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
   return v[0];
 }
 
-// Q operand rows of head h from this lane's 16 bf16 values of it (dims
-// 16l..16l+15): q*2^s = hi + lo with hi, lo E4M3 and s a power of two putting
-// the head's largest |q| in [128, 256); row h holds hi, row 64+h lo, in the
-// 128-byte-swizzled K-major layout of the S MMA.  Also the head's logit scale
-// (log2 units).  Warp-collective (the head's maximum is a warp reduction).
-__device__ __forceinline__ void q_operand_head(const uint4 qa, const uint4 qb, int h, int lane,
-                                               uint8_t* qop, float* qexp, float logit_scale) {
-  const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-  float x[16];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-  int e = 0;
-  if (amax > 0.0f) frexpf(amax, &e);  // amax < 2^e
-  const int sh = max(-100, min(100, 8 - e));
-  const float scale = ldexpf(1.0f, sh);
-  if (lane == 0) qexp[h] = logit_scale * ldexpf(1.0f, -sh);
-  uint32_t hw[4], lw[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint16_t hc[2], lc[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float a0 = x[4 * i + 2 * k] * scale, a1 = x[4 * i + 2 * k + 1] * scale;
-      hc[k] = e4m3x2(a0, a1);
-      const float2 hv = e4m3x2_decode(hc[k]);
-      lc[k] = e4m3x2(a0 - hv.x, a1 - hv.y);
-    }
-    hw[i] = static_cast<uint32_t>(hc[0]) | (static_cast<uint32_t>(hc[1]) << 16);
-    lw[i] = static_cast<uint32_t>(lc[0]) | (static_cast<uint32_t>(lc[1]) << 16);
-  }
-  // Dims 16l..16l+15 = 16-byte chunk l%8 of column block l/8.
-  uint8_t* blk = qop + (lane >> 3) * kSub;
-  const uint32_t c = static_cast<uint32_t>(((lane & 7) ^ (h & 7)) * 16);
-  *reinterpret_cast<uint4*>(blk + h * 128 + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-  *reinterpret_cast<uint4*>(blk + (h + kHeads) * 128 + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-}
-
 __device__ __forceinline__ void set_abort(Ctl* c) {
   *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
 }
@@ -337,43 +292,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (tid < kHeads) ctl->mrun[tid] = -INFINITY;
-  // ---- Q operand.  In a launch that fits one wave (set by the host) Q is
-  // loaded and converted speculatively before the dependency wait
-  // (overlapping the kernel before) and read again after it; a head whose
-  // values changed in between (Q written by the kernel before) is converted
-  // again, so the operand always holds the Q of after the wait.  In larger
-  // launches the later CTAs start after the kernel before has finished and
-  // the second read would only cost: Q is loaded and converted after the
-  // wait.  Warp w converts heads w, w+12, ...; lane l holds dims 16l..16l+15.
+  // Q may be the output of the kernel before (a projection), so it is only
+  // prefetched into L2 here (a prefetch cannot make a later load stale) and
+  // loaded after the dependency wait.  Warp w converts heads w, w+12, ...;
+  // lane l dims 16l..16l+15 (32 bytes: lanes 4i..4i+3 share a 128-byte line).
   constexpr int kQPer = (kHeads + kThreads / 32 - 1) / (kThreads / 32);
-  const float logit_scale = p.sm_scale * p.kv_scale * 1.4426950408889634f;
-  const uint16_t* qrow = p.q + (static_cast<int64_t>(r) * p.heads + head0) * 512 + lane * 16;
-  const bool spec = p.speculate != 0;
-  uint4 qa[kQPer], qb[kQPer];
 #pragma unroll
   for (int j = 0; j < kQPer; ++j) {
     const int h = warp + j * (kThreads / 32);
-    if (spec && h < nheads) {
-      const uint4* src = reinterpret_cast<const uint4*>(qrow + h * 512);
-      qa[j] = ld_dep_u4(src);
-      qb[j] = ld_dep_u4(src + 1);
-    } else {
-      qa[j] = make_uint4(0, 0, 0, 0);
-      qb[j] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  if (spec) {
-#pragma unroll
-    for (int j = 0; j < kQPer; ++j) {
-      const int h = warp + j * (kThreads / 32);
-      if (h < kHeads) q_operand_head(qa[j], qb[j], h, lane, qop, ctl->qexp, logit_scale);
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < kQPer; ++j) {
-      const int h = warp + j * (kThreads / 32);
-      if (h < nheads && (lane & 3) == 0) prefetch_l2(qrow + h * 512);
-    }
+    if (h < nheads && (lane & 3) == 0)
+      prefetch_l2(p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + lane * 16);
   }
   grid_dep_wait();  // the selection (and possibly Q, seq_lens) come from kernels before
 
@@ -382,7 +310,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (report && split == 0 && tid == 0) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
     len = 0;
   }
-  // The split's selection entries and Q again, in one round trip.
+  uint4 qa[kQPer], qb[kQPer];
+#pragma unroll
+  for (int j = 0; j < kQPer; ++j) {
+    const int h = warp + j * (kThreads / 32);
+    if (h < nheads) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + lane * 16);
+      qa[j] = ld_dep_u4(src);
+      qb[j] = ld_dep_u4(src + 1);
+    } else {
+      qa[j] = make_uint4(0, 0, 0, 0);
+      qb[j] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  // The split's selection entries, issued before the Q conversion so both
+  // round trips overlap.
   constexpr int kPer = (kMaxTiles * kTok + kThreads - 1) / kThreads;
   int idx[kPer];
 #pragma unroll
@@ -390,31 +333,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = tid + i * kThreads;
     idx[i] = e < nj ? p.sel[static_cast<int64_t>(r) * p.topk + j0 + e] : -1;  // plain load
   }
-  uint4 ra[kQPer], rb[kQPer];
+  // ---- Q operand: q*2^s = hi + lo (E4M3 each), s a power of two per head
+  // putting the head's largest |q| in [128, 256).  Row h holds hi, row 64+h lo.
 #pragma unroll
   for (int j = 0; j < kQPer; ++j) {
     const int h = warp + j * (kThreads / 32);
-    if (h < nheads) {
-      const uint4* src = reinterpret_cast<const uint4*>(qrow + h * 512);
-      ra[j] = ld_dep_u4(src);
-      rb[j] = ld_dep_u4(src + 1);
+    if (h >= kHeads) break;
+    const uint32_t w[8] = {qa[j].x, qa[j].y, qa[j].z, qa[j].w, qb[j].x, qb[j].y, qb[j].z, qb[j].w};
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
-  }
+    float amax = 0.0f;
 #pragma unroll
-  for (int j = 0; j < kQPer; ++j) {
-    const int h = warp + j * (kThreads / 32);
-    if (spec) {
-      if (h < nheads) {  // uniform over the warp
-        const bool changed = ra[j].x != qa[j].x || ra[j].y != qa[j].y || ra[j].z != qa[j].z ||
-                             ra[j].w != qa[j].w || rb[j].x != qb[j].x || rb[j].y != qb[j].y ||
-                             rb[j].z != qb[j].z || rb[j].w != qb[j].w;
-        if (__any_sync(0xFFFFFFFFu, changed))
-          q_operand_head(ra[j], rb[j], h, lane, qop, ctl->qexp, logit_scale);
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    int e = 0;
+    if (amax > 0.0f) frexpf(amax, &e);  // amax < 2^e
+    const int sh = max(-100, min(100, 8 - e));
+    const float scale = ldexpf(1.0f, sh);
+    if (lane == 0)
+      ctl->qexp[h] = p.sm_scale * p.kv_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint16_t hc[2], lc[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float a0 = x[4 * i + 2 * k] * scale, a1 = x[4 * i + 2 * k + 1] * scale;
+        hc[k] = e4m3x2(a0, a1);
+        const float2 hv = e4m3x2_decode(hc[k]);
+        lc[k] = e4m3x2(a0 - hv.x, a1 - hv.y);
       }
-    } else if (h < kHeads) {
-      if (h >= nheads) ra[j] = rb[j] = make_uint4(0, 0, 0, 0);
-      q_operand_head(ra[j], rb[j], h, lane, qop, ctl->qexp, logit_scale);
+      hw[i] = static_cast<uint32_t>(hc[0]) | (static_cast<uint32_t>(hc[1]) << 16);
+      lw[i] = static_cast<uint32_t>(lc[0]) | (static_cast<uint32_t>(lc[1]) << 16);
     }
+    // Dims 16l..16l+15 = 16-byte chunk l%8 of column block l/8.
+    uint8_t* blk = qop + (lane >> 3) * kSub;
+    const uint32_t c = static_cast<uint32_t>(((lane & 7) ^ (h & 7)) * 16);
+    *reinterpret_cast<uint4*>(blk + h * 128 + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(blk + (h + kHeads) * 128 + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
 
   // ---- slots of every entry of this split (a table lookup each)
@@ -773,11 +734,8 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
   const int nsplit = p.splits;
   const int64_t base = (static_cast<int64_t>(r) * groups + hg) * nsplit;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  // The next kernel (in a decode loop, the next layer's indexer) may start
-  // now: it waits for this kernel's completion before it reads anything,
-  // and its set-up overlaps the attend and this merge.
-  grid_dep_launch();
   grid_dep_wait();  // the partials come from the kernel before
+  grid_dep_launch();
   float mmax = -INFINITY;
   float lsum = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -871,12 +829,6 @@ void plan_mla_decode_tc(DecodeParams& p) {
   if (n < 1) n = 1;
   p.splits = n;
   p.split_len = (p.topk + n - 1) / n;
-}
-
-void plan_mla_decode_speculation(DecodeParams& p, int num_sms) {
-  // One CTA per SM (shared memory): one wave when the grid fits the SMs.
-  const int64_t ctas = static_cast<int64_t>(p.splits) * ((p.heads + kHeads - 1) / kHeads) * p.rows.rows;
-  p.speculate = ctas <= num_sms ? 1 : 0;
 }
 
 static int decode_splits(int32_t heads, int32_t topk) {
