@@ -64,13 +64,14 @@ struct IndexParams {
   int32_t dim;            // 64 or 128
   int32_t npad;           // sub_rows*heads rounded up to a multiple of 16
   int32_t max_len;
-  int32_t chunk_tiles;    // 128-token tiles per CTA
+  int32_t ctas;           // persistent CTAs (one wave)
+  int32_t direct;         // 1: one tile per CTA, grid (tile, group)
   int32_t stages;         // smem pipeline depth
   uint32_t tmem_cols;
   uint32_t smem_bytes;
   uint64_t wait_ns;
 };
-// Fills in chunk_tiles / stages / tmem_cols / smem_bytes from the shape.
+// Fills in direct / ctas / stages / tmem_cols / smem_bytes from the shape.
 void plan_index_scores(IndexParams& p, int num_sms);
 cudaError_t launch_index_scores(const IndexParams& p, const CUtensorMap& kmap,
                                 cudaStream_t stream);

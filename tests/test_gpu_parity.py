@@ -197,3 +197,79 @@ def test_host_argument_errors(dsa):
                              dw.max_len, dw.scores)
     assert e.value.status == 1
     assert api.dsa_get_error(reset=True)[0] == 0   # nothing was launched
+
+
+# ---------------------------------------------------------------------------- persistent indexer
+# A launch whose tiles exceed one wave even at its longest rows runs the
+# indexer as persistent CTAs, each scoring a contiguous run of the
+# concatenated tiles of every launch group (crossing group boundaries); a
+# smaller one runs one tile per CTA.  The small parity cases above are mostly
+# of the second kind; these are of the first.
+
+def test_persistent_indexer_ragged_many_groups(dsa, oracle):
+    """45 single-row groups with empty, one-token, tile-edge and long rows."""
+    api, path = dsa
+    lens = [0, 1, 127, 128, 129, 255, 3000, 9000, 4097, 0, 6000, 2, 8191, 300, 5000] * 3
+    wl = workloads.make_workload("persist", 51, seqs=len(lens), rows_per_seq=1, len_kind="list",
+                                 len_lo=0, len_hi=0, lens=lens, heads=16, index_heads=32,
+                                 index_dim=128, topk=256)
+    check_path(oracle, api, path, wl)
+
+
+def test_persistent_indexer_multi_row_sequences(dsa, oracle):
+    """Twelve sequences of K = 4 rows, each in two 64-column launch groups."""
+    api, path = dsa
+    wl = workloads.make_workload("persist_k", 52, seqs=12, rows_per_seq=4, len_kind="uniform",
+                                 len_lo=1500, len_hi=7000, heads=16, index_heads=32,
+                                 index_dim=128, topk=512)
+    check_path(oracle, api, path, wl)
+
+
+def test_persistent_and_direct_scores_bit_identical(dsa):
+    """A row's scores are the same bits in a batch (persistent CTAs) and alone
+    (one tile per CTA)."""
+    api, path = dsa
+    wl = workloads.make_workload("persist_bits", 53, seqs=40, rows_per_seq=1, len_kind="uniform",
+                                 len_lo=100, len_hi=9000, heads=16, index_heads=32,
+                                 index_dim=128, topk=256)
+    batch = path.DeviceWorkload(wl)
+    batch.index_scores()
+    torch.cuda.synchronize()
+    for r in (0, 7, 19, 39):
+        one = path.DeviceWorkload(workloads.select_rows(wl, [r]))
+        one.index_scores()
+        torch.cuda.synchronize()
+        L = int(wl.seq_lens[r])
+        assert torch.equal(batch.scores[r, :L], one.scores[0, :L]), f"row {r}"
+        del one
+    assert api.dsa_get_error(reset=True)[0] == 0
+
+
+def test_persistent_indexer_reports_bad_rows(dsa):
+    """A malformed row of a persistent launch is recorded and skipped; every
+    other row's scores are unchanged, bit for bit."""
+    api, path = dsa
+    wl = workloads.scaled("batched", seqs=32, len_div=8)      # 32 groups x 64 tiles
+    dw = path.DeviceWorkload(wl)
+    dw.index_scores()
+    torch.cuda.synchronize()
+    assert api.dsa_get_error(reset=True)[0] == 0
+    ref = dw.scores.clone()
+
+    def others_unchanged(bad):
+        for r in range(wl.rows):
+            if r != bad:
+                L = int(wl.seq_lens[r])
+                assert torch.equal(dw.scores[r, :L], ref[r, :L]), f"row {r} changed"
+
+    dw.seq_lens[5] = dw.max_len + 1
+    dw.index_scores()
+    code, row, _ = api.dsa_get_error(reset=True)
+    assert api.DEVERR[code] == "seq_len" and row == 5
+    others_unchanged(5)
+    dw.seq_lens[5] = int(wl.seq_lens[5])
+    dw.idx_base[9] = -3
+    dw.index_scores()
+    code, row, _ = api.dsa_get_error(reset=True)
+    assert api.DEVERR[code] == "arena" and row == 9
+    others_unchanged(9)
