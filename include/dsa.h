@@ -132,8 +132,9 @@ dsa_status dsa_latent_write(const dsa_rows *rows, const uint16_t *kv_a, const ui
  *   idx_base [rows] int64: the row's sequence start in the arena
  *   scores [rows][max_len] fp32 (output)
  * rows_per_seq: consecutive rows that share one sequence (a K-token verify);
- * they must have equal idx_base (checked on the device) and their keys are
- * read once for all of them.  rows must be a multiple of rows_per_seq.
+ * they must have equal idx_base (checked on the device) and share each key
+ * tile they read, up to 64 score columns (rows x index_heads) per read.
+ * rows must be a multiple of rows_per_seq.
  * idx_written (optional, may be NULL): [rows / rows_per_seq] int32, the rows
  * of each sequence's keys written so far (as kept by dsa_indexer_write); a
  * row whose seq_len exceeds its sequence's count is skipped (scores not
