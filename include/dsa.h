@@ -189,9 +189,11 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  * normalising sums and lse use the unrounded weights.  A row's selection is
  * cut into splits of at most 256 entries (2048 with more than 64 heads) whose
  * count depends only on topk and heads, so each row's result is bit-identical
- * whatever the other rows of the call are.  With more than one split the partial outputs pass
- * through the workspace (L2-resident, discarded after the merge), which must
- * hold dsa_workspace_bytes(rows, heads, topk) bytes, 256-byte aligned
+ * whatever the other rows of the call are.  With more than one split each
+ * split's normalised partial output O/l (a convex combination of latent
+ * values, kept in fp16: 2^-11 relative) and its (max, sum) pass through the
+ * workspace (L2-resident, discarded after the merge), which must hold
+ * dsa_workspace_bytes(rows, heads, topk) bytes, 256-byte aligned
  * (DSA_ERR_WORKSPACE otherwise).
  */
 dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,
@@ -236,9 +238,9 @@ dsa_status dsa_mla_decode_fp8_noalloc(const dsa_rows *rows, const uint16_t *q, c
  * call of this shape (0 on bad arguments). */
 size_t dsa_noalloc_scratch_bytes(int32_t rows, int32_t heads, int32_t topk);
 
-/* Device bytes of the caller-owned workspace that dsa_select_topk and
- * dsa_mla_decode_fp8 need for a call of this shape (the gather-attend's split
- * partials; 0 when no workspace is needed or on bad arguments). */
+/* Device bytes of the caller-owned workspace that dsa_mla_decode_fp8 needs
+ * for a call of this shape (the gather-attend's split partials; 0 when no
+ * workspace is needed or on bad arguments). */
 size_t dsa_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 
 /*

@@ -289,9 +289,10 @@ def dsa_workspace_bytes(rows: int, heads: int, topk: int) -> int:
 
 def decode_splits(heads: int, topk: int) -> int:
     """Splits per (row, 64-head group) of the gather-attend, read back from the
-    workspace size (one split's partials are 64 x (512 + 2) floats)."""
+    workspace size (one split's partials: 64 heads x (512 fp16 + an FP32 pair),
+    1032 bytes a head)."""
     groups = (int(heads) + 63) // 64
-    return dsa_workspace_bytes(1, heads, topk) // (groups * 64 * (512 + 2) * 4)
+    return dsa_workspace_bytes(1, heads, topk) // (groups * 64 * (512 * 2 + 8))
 
 
 def dsa_noalloc_scratch_bytes(rows: int, heads: int, topk: int) -> int:

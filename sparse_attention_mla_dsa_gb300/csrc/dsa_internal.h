@@ -155,7 +155,7 @@ struct DecodeParams {
   const int32_t* sel;
   uint16_t* out;
   float* lse;
-  float* part_o;    // workspace: [rows][head groups][splits][64][512] partial O
+  uint16_t* part_o; // workspace: [rows][head groups][splits][64][512] fp16 O / l of the split
   float* part_ml;   // workspace: [rows][head groups][splits][64] (max, sum)
   int* err;
   int32_t topk;

@@ -687,8 +687,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_lane != -INFINITY ? (m_lane + log2f(l_lane)) * 0.69314718055994531f : -INFINITY;
     }
     // O^T: lane = dim 128mb + 32*quarter + lane, column = head.  For a fixed
-    // head the 32 lanes write 32 consecutive dims.
-    const float sc_lane = (m_lane != -INFINITY && l_lane > 0.0f) ? p.kv_scale / l_lane : 0.0f;
+    // head the 32 lanes write 32 consecutive dims.  One split: the output,
+    // kv_scale * O / l, in bf16.  Several: the split's O / l in fp16 -- a
+    // convex combination of E4M3 latent values, so |O / l| <= 448 and fp16
+    // keeps it to 2^-11 relative, at half the bytes of FP32 (the stores of
+    // the partials bound this epilogue) -- with (max, sum) beside it.
+    const float sc_lane =
+        (m_lane != -INFINITY && l_lane > 0.0f) ? (nsplit > 1 ? 1.0f : p.kv_scale) / l_lane : 0.0f;
     float sc[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, sc_lane, i);
@@ -703,10 +708,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
       }
       if (nsplit > 1) {
-        float* dst = p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) *
-                                    (kHeads * 512) + d;
+        uint16_t* dst = p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) *
+                                       (kHeads * 512) + d;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dst[(hh + i) * 512] = v[i];
+        for (int i = 0; i < 32; ++i) dst[(hh + i) * 512] = __half_as_ushort(__float2half_rn(v[i] * sc[i]));
       } else {
         uint16_t* dst = p.out + (static_cast<int64_t>(r) * p.heads + head0) * 512 + d;
 #pragma unroll
@@ -723,6 +728,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// One split's share of a merged (row, head): weight w = l * 2^(m - mmax) on
+// the split's O / l (four fp16 values).
+__device__ __forceinline__ void accumulate_split(float2 ml, uint2 v, float mmax, float& lsum,
+                                                 float4& acc) {
+  const float w = ml.y * exp2f(ml.x - mmax);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  lsum += w;
+  acc.x += a.x * w;
+  acc.y += a.y * w;
+  acc.z += b.x * w;
+  acc.w += b.y * w;
 }
 
 // Merge of the n splits of one (row, head): 128 threads, 4 dims each, splits
@@ -742,31 +761,23 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
   if (nsplit <= 8) {
     // Every split's (max, sum) and partial row in flight at once: one round trip.
     float2 mlc[8];
-    float4 vc[8];
+    uint2 vc[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (u < nsplit) {
         mlc[u] = ld_dep_f2(ml + (base + u) * kHeads + hl);
-        vc[u] = ld_dep_f4(reinterpret_cast<const float4*>(p.part_o + ((base + u) * kHeads + hl) * 512) + tid);
+        vc[u] = ld_dep_u2(reinterpret_cast<const uint2*>(p.part_o + ((base + u) * kHeads + hl) * 512) + tid);
       } else {
         mlc[u] = make_float2(-INFINITY, 0.0f);
-        vc[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        vc[u] = make_uint2(0u, 0u);
       }
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) mmax = fmaxf(mmax, mlc[u].x);
     if (mmax != -INFINITY) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (u < nsplit) {
-          const float f = exp2f(mlc[u].x - mmax);
-          lsum += mlc[u].y * f;
-          acc.x += vc[u].x * f;
-          acc.y += vc[u].y * f;
-          acc.z += vc[u].z * f;
-          acc.w += vc[u].w * f;
-        }
-      }
+      for (int u = 0; u < 8; ++u)
+        if (u < nsplit) accumulate_split(mlc[u], vc[u], mmax, lsum, acc);
     }
   } else {
     // Maxima first (eight loads in flight per round), then the rows.
@@ -781,25 +792,17 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
     if (mmax != -INFINITY) {
       for (int c0 = 0; c0 < nsplit; c0 += 8) {
         float2 mlc[8];
-        float4 vc[8];
+        uint2 vc[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           if (c0 + u < nsplit) {
             mlc[u] = ld_dep_f2(ml + (base + c0 + u) * kHeads + hl);
-            vc[u] = ld_dep_f4(reinterpret_cast<const float4*>(p.part_o + ((base + c0 + u) * kHeads + hl) * 512) + tid);
+            vc[u] = ld_dep_u2(reinterpret_cast<const uint2*>(p.part_o + ((base + c0 + u) * kHeads + hl) * 512) + tid);
           }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (c0 + u < nsplit) {
-            const float f = exp2f(mlc[u].x - mmax);
-            lsum += mlc[u].y * f;
-            acc.x += vc[u].x * f;
-            acc.y += vc[u].y * f;
-            acc.z += vc[u].z * f;
-            acc.w += vc[u].w * f;
-          }
-        }
+        for (int u = 0; u < 8; ++u)
+          if (c0 + u < nsplit) accumulate_split(mlc[u], vc[u], mmax, lsum, acc);
       }
     }
   }
@@ -812,9 +815,9 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
   if (tid == 0 && p.lse != nullptr)
     p.lse[head] = mmax != -INFINITY ? (mmax + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
   // Every lane has used its partial values: drop the consumed 128-byte lines
-  // (8 lanes share one) from L2 instead of writing them back.
+  // (16 lanes share one) from L2 instead of writing them back.
   __syncwarp();
-  if ((tid & 7) == 0)
+  if ((tid & 15) == 0)
     for (int c = 0; c < nsplit; ++c)
       discard_l2_line(p.part_o + ((base + c) * kHeads + hl) * 512 + tid * 4);
 }
@@ -842,16 +845,16 @@ static int decode_splits(int32_t heads, int32_t topk) {
 size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk) {
   const int n = decode_splits(heads, topk);
   const size_t units = static_cast<size_t>(rows) * ((heads + kHeads - 1) / kHeads) * n * kHeads;
-  const size_t o_bytes = (units * 512 * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  const size_t o_bytes = (units * 512 * sizeof(uint16_t) + 255) & ~static_cast<size_t>(255);
   return o_bytes + units * 2 * sizeof(float);
 }
 
 void mla_decode_tc_bind_workspace(DecodeParams& p, void* workspace) {
   const size_t units =
       static_cast<size_t>(p.rows.rows) * ((p.heads + kHeads - 1) / kHeads) * p.splits * kHeads;
-  p.part_o = static_cast<float*>(workspace);
+  p.part_o = static_cast<uint16_t*>(workspace);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                       ((units * 512 * sizeof(float) + 255) & ~static_cast<size_t>(255)));
+                                       ((units * 512 * sizeof(uint16_t) + 255) & ~static_cast<size_t>(255)));
 }
 
 cudaError_t launch_mla_decode_tc(const DecodeParams& p, const CUtensorMap& pmap,

@@ -41,10 +41,12 @@ def test_host_helpers_without_gpu():
     assert lib.dsa_status_string(5).startswith(b"workspace")
     lib.dsa_workspace_bytes.restype = ctypes.c_size_t
     lib.dsa_workspace_bytes.argtypes = [ctypes.c_int32] * 3
-    units = 1 * 1 * 8 * 64                                   # rows x head groups x splits x 64
-    assert lib.dsa_workspace_bytes(1, 64, 2048) == units * 512 * 4 + units * 8
+    # rows x head groups x splits x 64 units of an fp16 partial row (512 x 2 B)
+    # and an FP32 (max, sum) pair
+    units = 1 * 1 * 8 * 64
+    assert lib.dsa_workspace_bytes(1, 64, 2048) == units * 512 * 2 + units * 8
     units = 2 * 2 * 1 * 64                                   # 128 heads: two head groups, one split
-    assert lib.dsa_workspace_bytes(2, 128, 2048) == units * 512 * 4 + units * 8
+    assert lib.dsa_workspace_bytes(2, 128, 2048) == units * 512 * 2 + units * 8
     assert lib.dsa_workspace_bytes(0, 64, 2048) == 0
 
 
