@@ -14,7 +14,11 @@
     e4m3(p) and lo = e4m3(p - hi), so a weight errs by at most 2^-8 of itself
     (2^-4 of 2^-4; RMS about 2^-8/3 for a residual spread over its rounding
     interval), and the output is rounded once to bf16 (at most 2^-9 of
-    itself, RMS 2^-9/sqrt(3)).  Together about 1.7e-3 relative RMS; per row
+    itself, RMS 2^-9/sqrt(3)).  With more than one split each split's O/l (a
+    weighted mean of the split's latent rows, so a few times |o| at most for
+    a flat row, |o| for a peaked one) is rounded once to fp16 (2^-11 of
+    itself) before the merge: under 1e-3 relative RMS more.  Together about
+    2e-3 relative RMS; per row
     the rel-L2 error is held to 4e-3, and every element to
     2^-8 |o| + 2^-6 rms(o_head) (the second term is ~9 standard deviations of
     the weight rounding noise on a flat row, where every element of o is a
