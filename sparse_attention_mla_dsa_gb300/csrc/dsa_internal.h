@@ -65,7 +65,8 @@ struct IndexParams {
   int32_t npad;           // sub_rows*heads rounded up to a multiple of 16
   int32_t max_len;
   int32_t ctas;           // persistent CTAs (one wave)
-  int32_t direct;         // 1: one tile per CTA, grid (tile, group)
+  int32_t direct;         // 1: direct_tiles tiles per CTA, grid (tile block, group)
+  int32_t direct_tiles;
   int32_t stages;         // smem pipeline depth
   uint32_t tmem_cols;
   uint32_t smem_bytes;

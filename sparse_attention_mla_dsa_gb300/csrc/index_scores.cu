@@ -51,6 +51,7 @@ constexpr int kEpiThreads = 128;  // warps 2-5
 constexpr int kMaxStages = 6;
 constexpr int kMaxSubRows = 32;
 constexpr int kSegRing = 4;       // segment records in flight
+constexpr int kDirectTiles = 2;   // tiles per CTA of a direct launch
 constexpr int kScanThreads = 64;  // warps 0-1 find the CTA's range
 constexpr int kScanRegs = 8;      // groups per scan thread kept between the two passes
 
@@ -212,9 +213,10 @@ __device__ __forceinline__ long long scan_prefix(long long v, long long* scratch
   return (warp == 1 ? s0 : 0) + x - v;
 }
 
-// kDirect: a launch small enough for one tile per CTA in a single wave --
-// CTA (x, y) scores tile x of group y, needs no scan, and warp 0 loads the
-// group's rows once, issues the tile's copy and posts its record itself.
+// kDirect: a launch small enough for a few tiles per CTA in a single wave --
+// CTA (x, y) scores tiles [x*dt, x*dt + dt) of group y (dt = direct_tiles,
+// one stage each), needs no scan, and warp 0 loads the group's rows once,
+// issues the tiles' copies and posts their record itself.
 template <int D, bool kDirect>
 __global__ void __launch_bounds__(kThreads, 1)
     index_scores_kernel(const __grid_constant__ CUtensorMap kmap, const IndexParams p) {
@@ -270,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&kmap);
     if (kDirect || groups == 1) {
       const long long tg = (p.max_len + kTileM - 1) / kTileM;
-      const long long b0 = kDirect ? blockIdx.x : tg * c / ctas;
-      const long long b1 = kDirect ? b0 + 1 : tg * (c + 1) / ctas;
+      const long long b0 = kDirect ? static_cast<long long>(blockIdx.x) * p.direct_tiles : tg * c / ctas;
+      const long long b1 = kDirect ? b0 + p.direct_tiles : tg * (c + 1) / ctas;
       const int64_t base_hint = *reinterpret_cast<const volatile int64_t*>(
           p.idx_base + group_rows(p, kDirect ? blockIdx.y : 0).seq_row0);
       for (long long t = b0; t < min(b1, b0 + stages); ++t) {
@@ -307,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
    if constexpr (kDirect) {
     if (warp == 0) {
       // The group's rows, one per lane; every lane's loads issued together.
-      const int g = blockIdx.y, t0 = blockIdx.x;
+      const int g = blockIdx.y, t0 = blockIdx.x * p.direct_tiles;
       const GroupRows gr = group_rows(p, g);
       const int64_t base = p.idx_base[gr.seq_row0];
       const int written = seq_written(p, gr.seq);
@@ -320,22 +322,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       int m = len;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      my_tiles = static_cast<long long>(t0) * kTileM < m ? 1 : 0;
+      const int tg = (m + kTileM - 1) / kTileM;
+      my_tiles = max(0, min(p.direct_tiles, tg - t0));
       if (my_tiles > 0) {
         Seg& sg = ctl->seg[0];
         sg.row_len[lane] = len;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->full[0], kStageBytes);
-          const int32_t y = static_cast<int32_t>(base + static_cast<int64_t>(t0) * kTileM);
           const uint64_t policy = l2_policy_evict_first();
+          for (int j = 0; j < my_tiles; ++j) {
+            mbar_arrive_expect_tx(&ctl->full[j], kStageBytes);
+            const int32_t y = static_cast<int32_t>(base + static_cast<int64_t>(t0 + j) * kTileM);
 #pragma unroll
-          for (int sb = 0; sb < kSub; ++sb)
-            tma_load_2d(stage_base + sb * (kTileM * 128), &kmap, &ctl->full[0], sb * 64, y, policy);
+            for (int sb = 0; sb < kSub; ++sb)
+              tma_load_2d(stage_base + j * kStageBytes + sb * (kTileM * 128), &kmap, &ctl->full[j],
+                          sb * 64, y, policy);
+          }
           sg.base = base;
           sg.r0 = gr.r0;
           sg.nrows = gr.nrows;
           sg.t_first = t0;
-          sg.ntiles = 1;
+          sg.ntiles = static_cast<int>(my_tiles);
           sg.max_len = m;
           ctl->g0 = g;
         }
@@ -409,8 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------------------- roles
   if (kDirect && warp == 0 && my_tiles > 0) {
-    // The CTA's one tile went out with its record: never leave with it in flight.
-    if (lane == 0) mbar_wait(&ctl->full[0], 0, kDrainWaitNs);
+    // The CTA's tiles went out with its record: never leave with one in flight.
+    if (lane == 0)
+      for (int j = 0; j < my_tiles; ++j) mbar_wait(&ctl->full[j], 0, kDrainWaitNs);
   } else if (!kDirect && warp == 0 && my_tiles > 0) {
     // ============================================================ segments + TMA
     uint64_t policy = 0;
@@ -765,7 +772,8 @@ void plan_index_scores(IndexParams& p, int num_sms) {
   const int64_t groups = static_cast<int64_t>(p.rows / p.rows_per_seq) * p.subs_per_seq;
   const int64_t wave = static_cast<int64_t>(per_sm) * num_sms;
   p.direct = (tiles_max * groups <= wave && groups <= 65535) ? 1 : 0;
-  if (p.direct) stages = 1;
+  p.direct_tiles = kDirectTiles;
+  if (p.direct) stages = kDirectTiles;
   p.stages = stages;
   p.smem_bytes = fixed + stages * stage_bytes;
   int64_t ctas = wave;
@@ -789,7 +797,8 @@ cudaError_t launch_index_scores(const IndexParams& p, const CUtensorMap& kmap,
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   const int64_t tiles_max = (static_cast<int64_t>(p.max_len) + kTileM - 1) / kTileM;
-  cfg.gridDim = p.direct ? dim3(static_cast<unsigned>(tiles_max), static_cast<unsigned>(groups), 1)
+  cfg.gridDim = p.direct ? dim3(static_cast<unsigned>((tiles_max + p.direct_tiles - 1) / p.direct_tiles),
+                                static_cast<unsigned>(groups), 1)
                          : dim3(static_cast<unsigned>(p.ctas), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = p.smem_bytes;
