@@ -230,7 +230,7 @@ def time_path(wl, dev, K, warmup, eager, world, api, path, shard):
     def one_step(dw, evs=None):
         s = torch.cuda.current_stream()
         calls = ([dw.latent_write] if wl.has_write else []) + [dw.index_scores, dw.select_topk,
-                                                               dw.mla_decode]
+                                                               lambda: dw.mla_decode(q_early=True)]
         if evs is not None:
             evs[0].record(s)
         for j, call in enumerate(calls):

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 #define DSA_LATENT_DIM 512
 
 typedef enum dsa_status {
@@ -201,6 +201,25 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uin
                               int32_t latent_dim, float kv_scale, float sm_scale, uint16_t *out,
                               float *lse_or_null, void *workspace, size_t workspace_bytes,
                               void *stream);
+
+/*
+ * S3 with flags.  dsa_mla_decode_fp8 is this call with flags 0.
+ * DSA_DECODE_Q_BEFORE_PREDECESSOR: the caller asserts that q was complete
+ * before the kernel issued just before this call on the stream started (the
+ * usual decode order: q comes from a projection before the indexer, and the
+ * kernel before the attend is dsa_select_topk, which writes only sel).  The
+ * attend may then load and convert q while that kernel still runs; sel, and
+ * everything else a predecessor may write, is still read after the
+ * dependency wait.  Without the flag q is read after the wait too.  The
+ * results are bit-identical either way.  Unknown flag bits:
+ * DSA_ERR_INVALID_ARG.
+ */
+#define DSA_DECODE_Q_BEFORE_PREDECESSOR 1u
+dsa_status dsa_mla_decode_fp8_ex(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,
+                                 int64_t nslots, const int32_t *sel, int32_t topk, int32_t heads,
+                                 int32_t latent_dim, float kv_scale, float sm_scale, uint16_t *out,
+                                 float *lse_or_null, void *workspace, size_t workspace_bytes,
+                                 uint32_t flags, void *stream);
 
 /*
  * S3 for callers that cannot allocate device memory at the point where they

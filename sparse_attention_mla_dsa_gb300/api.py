@@ -51,14 +51,15 @@ def load() -> ctypes.CDLL:
     if not os.path.exists(path):
         raise RuntimeError(f"libdsa_gb300.so is not built ({path}); run __graft_entry__.build()")
     lib = ctypes.CDLL(path)
-    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
-                            ctypes.c_size_t)
+    P, i32, i64, f32, sz, u32 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                 ctypes.c_size_t, ctypes.c_uint32)
     RP = ctypes.POINTER(Rows)
     sig = {
         "dsa_latent_write": [RP, P, P, P, i64, i32, f32, f32, P],
         "dsa_index_scores": [RP, P, P, P, P, i64, P, i32, i32, i32, i32, P, P, P],
         "dsa_select_topk": [RP, P, i32, i32, P, P],
         "dsa_mla_decode_fp8": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, sz, P],
+        "dsa_mla_decode_fp8_ex": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, sz, u32, P],
         "dsa_mla_decode_fp8_noalloc": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P],
         "dsa_get_error": [P, P, P, i32],
         "dsa_dense_mm_bf16": [P, P, P, i32, i32, i32, i32, P, sz, P],
@@ -176,22 +177,29 @@ def dsa_select_topk(rows: Rows, scores: torch.Tensor, max_len: int, topk: int, s
     _check("dsa_select_topk", st)
 
 
+DSA_DECODE_Q_BEFORE_PREDECESSOR = 1
+
+
 def dsa_mla_decode_fp8(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: torch.Tensor, topk: int,
                        kv_scale: float, sm_scale: float, out: torch.Tensor,
                        lse: torch.Tensor | None, workspace: torch.Tensor | None = None,
-                       stream=None) -> None:
-    """``out`` may be a CUDA tensor or a pinned host tensor (written directly)."""
+                       stream=None, q_early: bool = False) -> None:
+    """``out`` may be a CUDA tensor or a pinned host tensor (written directly).
+    ``q_early``: q was complete before the kernel issued just before this
+    call started (dsa_mla_decode_fp8_ex with DSA_DECODE_Q_BEFORE_PREDECESSOR)."""
     lib = load()
     heads = q.shape[-2]
-    st = lib.dsa_mla_decode_fp8(ctypes.byref(rows), _ptr(q, torch.uint16, "q"),
-                                _ptr(pool, torch.uint8, "pool"), pool.shape[0],
-                                _ptr(sel, torch.int32, "sel"), int(topk), heads, q.shape[-1],
-                                float(kv_scale), float(sm_scale),
-                                _ptr(out, torch.uint16, "out", host_ok=True),
-                                _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
-                                0 if workspace is None else workspace.numel() * workspace.element_size(),
-                                _stream(stream))
-    _check("dsa_mla_decode_fp8", st)
+    args = [ctypes.byref(rows), _ptr(q, torch.uint16, "q"), _ptr(pool, torch.uint8, "pool"),
+            pool.shape[0], _ptr(sel, torch.int32, "sel"), int(topk), heads, q.shape[-1],
+            float(kv_scale), float(sm_scale), _ptr(out, torch.uint16, "out", host_ok=True),
+            _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
+            0 if workspace is None else workspace.numel() * workspace.element_size()]
+    if q_early:
+        st = lib.dsa_mla_decode_fp8_ex(*args, DSA_DECODE_Q_BEFORE_PREDECESSOR, _stream(stream))
+        _check("dsa_mla_decode_fp8_ex", st)
+    else:
+        st = lib.dsa_mla_decode_fp8(*args, _stream(stream))
+        _check("dsa_mla_decode_fp8", st)
 
 
 def dsa_mla_decode_fp8_noalloc(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: torch.Tensor,

@@ -208,6 +208,17 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
                               int32_t latent_dim, float kv_scale, float sm_scale, uint16_t* out,
                               float* lse_or_null, void* workspace, size_t workspace_bytes,
                               void* stream) {
+  return dsa_mla_decode_fp8_ex(rows, q, pool, nslots, sel, topk, heads, latent_dim, kv_scale,
+                               sm_scale, out, lse_or_null, workspace, workspace_bytes, 0u, stream);
+}
+
+dsa_status dsa_mla_decode_fp8_ex(const dsa_rows* rows, const uint16_t* q, const uint8_t* pool,
+                                 int64_t nslots, const int32_t* sel, int32_t topk, int32_t heads,
+                                 int32_t latent_dim, float kv_scale, float sm_scale,
+                                 uint16_t* out, float* lse_or_null, void* workspace,
+                                 size_t workspace_bytes, uint32_t flags, void* stream) {
+  if ((flags & ~static_cast<uint32_t>(DSA_DECODE_Q_BEFORE_PREDECESSOR)) != 0u)
+    return DSA_ERR_INVALID_ARG;
   dsa_status st = check_rows(rows, true);
   if (st != DSA_OK) return st;
   if (q == nullptr || pool == nullptr || sel == nullptr || out == nullptr || nslots < 1)
@@ -244,6 +255,10 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows* rows, const uint16_t* q, const uin
   p.kv_scale = kv_scale;
   p.sm_scale = sm_scale;
   p.wait_ns = wait_limit_ns();
+  // Only CTAs of the first wave can be waiting on the kernel before: later
+  // ones start after it has finished, and for them the default order (q and
+  // the selection loaded together after the wait) is the faster one.
+  p.q_early = (flags & DSA_DECODE_Q_BEFORE_PREDECESSOR) != 0u ? dev->num_sms : 0;
   plan_mla_decode_tc(p);
   const size_t need = mla_decode_tc_workspace_bytes(rows->rows, heads, topk);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))

@@ -166,6 +166,7 @@ struct DecodeParams {
   uint64_t wait_ns;    // pipeline wait limit
   float kv_scale;
   float sm_scale;
+  int32_t q_early;     // CTAs (in launch order) that load q before the dependency wait
 };
 // Split count / length of the gather-attend (a function of topk only).
 void plan_mla_decode_tc(DecodeParams& p);

@@ -292,16 +292,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (tid < kHeads) ctl->mrun[tid] = -INFINITY;
-  // Q may be the output of the kernel before (a projection), so it is only
-  // prefetched into L2 here (a prefetch cannot make a later load stale) and
-  // loaded after the dependency wait.  Warp w converts heads w, w+12, ...;
-  // lane l dims 16l..16l+15 (32 bytes: lanes 4i..4i+3 share a 128-byte line).
+  // Q may be the output of the kernel before (a projection), so by default it
+  // is only prefetched into L2 here (a prefetch cannot make a later load
+  // stale) and loaded after the dependency wait.  With q_early the caller has
+  // declared Q complete before the kernel before this one started, and Q is
+  // loaded and converted now, while that kernel runs.  Warp w converts heads
+  // w, w+12, ...; lane l dims 16l..16l+15 (32 bytes: lanes 4i..4i+3 share a
+  // 128-byte line).
   constexpr int kQPer = (kHeads + kThreads / 32 - 1) / (kThreads / 32);
+  uint4 qa[kQPer], qb[kQPer];
+  auto load_q = [&]() {
 #pragma unroll
-  for (int j = 0; j < kQPer; ++j) {
-    const int h = warp + j * (kThreads / 32);
-    if (h < nheads && (lane & 3) == 0)
-      prefetch_l2(p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + lane * 16);
+    for (int j = 0; j < kQPer; ++j) {
+      const int h = warp + j * (kThreads / 32);
+      if (h < nheads) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + lane * 16);
+        qa[j] = ld_dep_u4(src);
+        qb[j] = ld_dep_u4(src + 1);
+      } else {
+        qa[j] = make_uint4(0, 0, 0, 0);
+        qb[j] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  // ---- Q operand: q*2^s = hi + lo (E4M3 each), s a power of two per head
+  // putting the head's largest |q| in [128, 256).  Row h holds hi, row 64+h lo.
+  auto convert_q = [&]() {
+#pragma unroll
+    for (int j = 0; j < kQPer; ++j) {
+      const int h = warp + j * (kThreads / 32);
+      if (h >= kHeads) break;
+      const uint32_t w[8] = {qa[j].x, qa[j].y, qa[j].z, qa[j].w, qb[j].x, qb[j].y, qb[j].z, qb[j].w};
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      int e = 0;
+      if (amax > 0.0f) frexpf(amax, &e);  // amax < 2^e
+      const int sh = max(-100, min(100, 8 - e));
+      const float scale = ldexpf(1.0f, sh);
+      if (lane == 0)
+        ctl->qexp[h] = p.sm_scale * p.kv_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint16_t hc[2], lc[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float a0 = x[4 * i + 2 * k] * scale, a1 = x[4 * i + 2 * k + 1] * scale;
+          hc[k] = e4m3x2(a0, a1);
+          const float2 hv = e4m3x2_decode(hc[k]);
+          lc[k] = e4m3x2(a0 - hv.x, a1 - hv.y);
+        }
+        hw[i] = static_cast<uint32_t>(hc[0]) | (static_cast<uint32_t>(hc[1]) << 16);
+        lw[i] = static_cast<uint32_t>(lc[0]) | (static_cast<uint32_t>(lc[1]) << 16);
+      }
+      // Dims 16l..16l+15 = 16-byte chunk l%8 of column block l/8.
+      uint8_t* blk = qop + (lane >> 3) * kSub;
+      const uint32_t c = static_cast<uint32_t>(((lane & 7) ^ (h & 7)) * 16);
+      *reinterpret_cast<uint4*>(blk + h * 128 + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(blk + (h + kHeads) * 128 + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+  };
+  const bool q_early =
+      static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(gridDim.x) * (blockIdx.y + static_cast<int64_t>(gridDim.y) * blockIdx.z) <
+      p.q_early;
+  if (q_early) {
+    load_q();
+    convert_q();
+  } else {
+#pragma unroll
+    for (int j = 0; j < kQPer; ++j) {
+      const int h = warp + j * (kThreads / 32);
+      if (h < nheads && (lane & 3) == 0)
+        prefetch_l2(p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + lane * 16);
+    }
   }
   grid_dep_wait();  // the selection (and possibly Q, seq_lens) come from kernels before
 
@@ -310,20 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (report && split == 0 && tid == 0) record_error(p.err, DSA_DEVERR_SEQ_LEN, r);
     len = 0;
   }
-  uint4 qa[kQPer], qb[kQPer];
-#pragma unroll
-  for (int j = 0; j < kQPer; ++j) {
-    const int h = warp + j * (kThreads / 32);
-    if (h < nheads) {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<int64_t>(r) * p.heads + head0 + h) * 512 + lane * 16);
-      qa[j] = ld_dep_u4(src);
-      qb[j] = ld_dep_u4(src + 1);
-    } else {
-      qa[j] = make_uint4(0, 0, 0, 0);
-      qb[j] = make_uint4(0, 0, 0, 0);
-    }
-  }
+  if (!q_early) load_q();
   // The split's selection entries, issued before the Q conversion so both
   // round trips overlap.
   constexpr int kPer = (kMaxTiles * kTok + kThreads - 1) / kThreads;
@@ -333,50 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = tid + i * kThreads;
     idx[i] = e < nj ? p.sel[static_cast<int64_t>(r) * p.topk + j0 + e] : -1;  // plain load
   }
-  // ---- Q operand: q*2^s = hi + lo (E4M3 each), s a power of two per head
-  // putting the head's largest |q| in [128, 256).  Row h holds hi, row 64+h lo.
-#pragma unroll
-  for (int j = 0; j < kQPer; ++j) {
-    const int h = warp + j * (kThreads / 32);
-    if (h >= kHeads) break;
-    const uint32_t w[8] = {qa[j].x, qa[j].y, qa[j].z, qa[j].w, qb[j].x, qb[j].y, qb[j].z, qb[j].w};
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    int e = 0;
-    if (amax > 0.0f) frexpf(amax, &e);  // amax < 2^e
-    const int sh = max(-100, min(100, 8 - e));
-    const float scale = ldexpf(1.0f, sh);
-    if (lane == 0)
-      ctl->qexp[h] = p.sm_scale * p.kv_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint16_t hc[2], lc[2];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float a0 = x[4 * i + 2 * k] * scale, a1 = x[4 * i + 2 * k + 1] * scale;
-        hc[k] = e4m3x2(a0, a1);
-        const float2 hv = e4m3x2_decode(hc[k]);
-        lc[k] = e4m3x2(a0 - hv.x, a1 - hv.y);
-      }
-      hw[i] = static_cast<uint32_t>(hc[0]) | (static_cast<uint32_t>(hc[1]) << 16);
-      lw[i] = static_cast<uint32_t>(lc[0]) | (static_cast<uint32_t>(lc[1]) << 16);
-    }
-    // Dims 16l..16l+15 = 16-byte chunk l%8 of column block l/8.
-    uint8_t* blk = qop + (lane >> 3) * kSub;
-    const uint32_t c = static_cast<uint32_t>(((lane & 7) ^ (h & 7)) * 16);
-    *reinterpret_cast<uint4*>(blk + h * 128 + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(blk + (h + kHeads) * 128 + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  }
+  if (!q_early) convert_q();
 
   // ---- slots of every entry of this split (a table lookup each)
   {

@@ -96,11 +96,14 @@ class DeviceWorkload:
     def select_topk(self, stream=None):
         api.dsa_select_topk(self.rows, self.scores, self.max_len, self.wl.topk, self.sel, stream)
 
-    def mla_decode(self, stream=None):
+    def mla_decode(self, stream=None, q_early: bool = False):
+        """S3.  ``q_early``: the call follows this workload's top-k on the same
+        stream (Q was uploaded before the step), so the attend may convert Q
+        before its dependency wait."""
         wl = self.wl
         out = self.out if self.out_target is None else self.out_target
         api.dsa_mla_decode_fp8(self.rows, self.Q, self.pool, self.sel, wl.topk, wl.kv_scale,
-                               wl.sm_scale, out, self.lse, self.workspace, stream)
+                               wl.sm_scale, out, self.lse, self.workspace, stream, q_early=q_early)
 
     def step(self, stream=None):
         """One pass of the whole hot path (S0 when the workload writes, S1-S3)."""
@@ -108,7 +111,7 @@ class DeviceWorkload:
             self.latent_write(stream)
         self.index_scores(stream)
         self.select_topk(stream)
-        self.mla_decode(stream)
+        self.mla_decode(stream, q_early=True)  # right after this workload's top-k
 
     # ---- host views of the results
     def out_f32(self) -> np.ndarray:

@@ -273,3 +273,28 @@ def test_persistent_indexer_reports_bad_rows(dsa):
     code, row, _ = api.dsa_get_error(reset=True)
     assert api.DEVERR[code] == "arena" and row == 9
     others_unchanged(9)
+
+
+def test_q_before_predecessor_flag_is_bit_identical(dsa):
+    """dsa_mla_decode_fp8_ex with DSA_DECODE_Q_BEFORE_PREDECESSOR (Q converted
+    before the dependency wait, as the chained step runs it) equals the
+    default order bit for bit; unknown flag bits are refused."""
+    import ctypes
+    api, path = dsa
+    for wl in (workloads.scaled("single", len_div=8), workloads.scaled("long", seqs=3, len_div=16)):
+        dw = path.DeviceWorkload(wl)
+        dw.step()                                   # the attend runs with q_early
+        torch.cuda.synchronize()
+        early_out, early_lse = dw.out.clone(), dw.lse.clone()
+        dw.mla_decode()                             # default: Q after the wait
+        torch.cuda.synchronize()
+        assert api.dsa_get_error(reset=True)[0] == 0
+        assert torch.equal(dw.out, early_out)
+        assert torch.equal(dw.lse.view(torch.int32), early_lse.view(torch.int32))
+    lib = api.load()
+    st = lib.dsa_mla_decode_fp8_ex(ctypes.byref(dw.rows), dw.Q.data_ptr(), dw.pool.data_ptr(),
+                                   dw.pool.shape[0], dw.sel.data_ptr(), wl.topk, wl.heads, 512,
+                                   wl.kv_scale, wl.sm_scale, dw.out.data_ptr(), None,
+                                   dw.workspace.data_ptr(),
+                                   dw.workspace.numel() * dw.workspace.element_size(), 2, None)
+    assert st == 1                                  # DSA_ERR_INVALID_ARG, nothing launched
