@@ -92,6 +92,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total)
 struct alignas(16) TopkShared {
   int hist[kBins * 32];          // [bin][lane] counters of the current pass
   int bin_tot[4][kBins];         // per-pass bin totals of this CTA (read remotely)
+  int scan_tmp[2 * kBins];       // per-bin exclusive prefix and count of the current pass
   alignas(8) int counts[2];      // this CTA's (key > T, key == T) counts
   int warp_tot[kWarps];
   int found_bin, found_above, found_count;
@@ -126,6 +127,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
   const int lo = min(len, static_cast<int>(crank) * per);
   const int n = min(len, lo + per) - lo;
   const float* row = p.scores + static_cast<int64_t>(r) * p.max_len + lo;
+  // The first pass's histogram (the keys' top 8 bits) is counted as the keys
+  // arrive; each later pass's counters are cleared by the threads that read
+  // them for the bin totals.
+#pragma unroll
+  for (int j = 0; j < kBins * 32 / kThreads; ++j) sh.hist[tid + j * kThreads] = 0;
+  __syncthreads();
   for (int base = 0; base < n; base += 8 * kThreads) {  // eight loads in flight per thread
     float v[8];
 #pragma unroll
@@ -136,7 +143,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int i = base + j * kThreads + tid;
-      if (i < n) keys[i] = order_key(v[j]);
+      if (i < n) {
+        const uint32_t key = order_key(v[j]);
+        keys[i] = key;
+        atomicAdd(&sh.hist[(key >> 24) * 32 + lane], 1);
+      }
     }
   }
 
@@ -146,13 +157,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
   bool all_taken = false;  // (uniform) every key equal to the threshold prefix is taken
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-#pragma unroll
-    for (int j = 0; j < kBins * 32 / kThreads; ++j) sh.hist[tid + j * kThreads] = 0;
-    __syncthreads();
+    if (pass > 0) {
 #pragma unroll 8
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = keys[i];
-      if ((key & prefix_mask) == prefix) atomicAdd(&sh.hist[((key >> shift) & 255u) * 32 + lane], 1);
+      for (int i = tid; i < n; i += kThreads) {
+        const uint32_t key = keys[i];
+        if ((key & prefix_mask) == prefix) atomicAdd(&sh.hist[((key >> shift) & 255u) * 32 + lane], 1);
+      }
     }
     __syncthreads();
     // Bin totals: 2 threads per bin, 16 lane counters each.  The 16 threads
@@ -162,7 +172,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
       const int b = tid >> 1, q = tid & 1;
       int t = 0;
 #pragma unroll
-      for (int l = 0; l < 16; ++l) t += sh.hist[b * 32 + q * 16 + ((l + b) & 15)];
+      for (int l = 0; l < 16; ++l) {
+        int* h = &sh.hist[b * 32 + q * 16 + ((l + b) & 15)];
+        t += *h;
+        *h = 0;  // ready for the next pass
+      }
       t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
       if (q == 0) sh.bin_tot[pass][b] = t;
     }
@@ -192,15 +206,15 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
       sh.warp_tot[warp] = 0;  // placeholder, overwritten below
       __syncwarp();
       if (lane == 31) sh.warp_tot[warp] = x;
-      sh.hist[(warp * 32 + lane)] = x - c;   // exclusive within the warp (hist is free now)
-      sh.hist[kBins + warp * 32 + lane] = c;
+      sh.scan_tmp[warp * 32 + lane] = x - c;   // exclusive within the warp
+      sh.scan_tmp[kBins + warp * 32 + lane] = c;
     }
     __syncthreads();
     if (warp < kBins / 32) {
       int before = 0;
       for (int w = 0; w < warp; ++w) before += sh.warp_tot[w];
-      const int above = before + sh.hist[warp * 32 + lane];
-      const int c = sh.hist[kBins + warp * 32 + lane];
+      const int above = before + sh.scan_tmp[warp * 32 + lane];
+      const int c = sh.scan_tmp[kBins + warp * 32 + lane];
       if (above < remaining && above + c >= remaining) {
         sh.found_bin = kBins - 1 - (warp * 32 + lane);
         sh.found_above = above;
