@@ -11,8 +11,9 @@
 //
 // A row's selection is cut into n splits of at most 256 entries (2048 with
 // more than 64 heads); n depends on topk and heads only, never on the number
-// of rows, so a row's arithmetic is the same in any launch.  One CTA (12 warps) runs one split of one (row, 64-head group)
-// as a pipeline over 128-entry tiles:
+// of rows, so a row's arithmetic is the same in any launch.  One CTA (20
+// warps) runs one split of one (row, 64-head group) as a pipeline over
+// 128-entry tiles:
 //   - the latent stays FP8: TMA tile::gather4 copies the selected 512-byte
 //     rows (4 rows x one 128-byte column block per copy, rows that are not
 //     there zero-filled) straight into a 128-byte-swizzled tile, two tiles in
@@ -26,8 +27,12 @@
 //     last bit); the two terms are the N = 128 rows of one operand, so
 //     S^T = Khat [Qhi|Qlo]^T is one M = 128 (tokens) x N = 128 x K = 512 MMA
 //     chain whose two column halves add up to the exact logits (warp 3);
-//   - S is double-buffered in TMEM, so the MMAs of tile t+1 run while eight
-//     softmax warps (one token x 32 heads per thread) work on tile t;
+//   - S is double-buffered in TMEM, so the MMAs of tile t+1 run while sixteen
+//     softmax warps (one token x 16 heads per thread) work on tile t.  The
+//     softmax is bound by the latency of its dependent steps, not by the
+//     exponential and conversion units: sixteen warps of 16 heads (four per
+//     scheduler) run a tile in about two thirds of the time eight warps of
+//     32 heads take, at 96 registers per thread;
 //   - softmax: the running maximum m of a head only moves when a logit would
 //     push p = 2^(z-m) past 2^8.75 (below the E4M3 maximum 448); it is then
 //     set 8 below the new tile maximum (the O columns and sums of that head
@@ -51,12 +56,13 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 384;          // warps 0-2 gather, warp 3 MMA, warps 4-11 softmax
-constexpr int kProducerWarps = 3;      // (12 warps keep 168 registers per thread)
+constexpr int kThreads = 640;          // warps 0-2 gather, warp 3 MMA, warps 4-19 softmax
+constexpr int kProducerWarps = 3;      // (20 warps keep 96 registers per thread)
 constexpr int kMmaWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kSoftmaxThreads = 512;
 constexpr int kHeads = 64;             // heads per CTA
+constexpr int kHpt = 16;               // heads per softmax thread (one token each)
 constexpr int kTok = 128;              // entries per tile (MMA M of S^T)
 constexpr int kTilesPerSplit = 2;      // split length target (tiles), up to 64 heads
 constexpr int kTilesPerSplitWide = 16; // the same with more than 64 heads (two head-group CTAs)
@@ -145,42 +151,31 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void discard_l2_line(const void* p) {
   asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
-// 32 consecutive TMEM columns of this thread's lane (waited in the same asm).
-__device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 16 consecutive TMEM columns of this thread's lane (waited in the same asm).
+__device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-// The same columns written back from registers (the caller waits with
-// tmem_store_wait before the values are used by an MMA).
-__device__ __forceinline__ void tmem_store32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tmem_store16(uint32_t taddr, const float (&v)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
       "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
       "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
       "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
       "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
       "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      "r"(__float_as_uint(v[15]))
       : "memory");
 }
 __device__ __forceinline__ void tmem_store_wait() {
@@ -206,9 +201,7 @@ __device__ __forceinline__ bool softmax_sync_or(bool pred) {
 
 // One butterfly step of a warp transpose-reduction: on entry v[0..2S) are
 // values of 2S heads in this lane; on exit v[0..S) hold, for the S heads
-// selected by lane bit S, the reduction over this lane and lane ^ S.  After
-// the steps S = 16, 8, 4, 2, 1, v[0] of lane l is the reduction of head l over
-// the 32 lanes, in an order fixed by the lane numbering.
+// selected by lane bit S, the reduction over this lane and lane ^ S.
 template <int S, bool kMax>
 __device__ __forceinline__ void butterfly_step(float* v, int lane) {
   const bool up = (lane & S) != 0;
@@ -220,14 +213,17 @@ __device__ __forceinline__ void butterfly_step(float* v, int lane) {
     v[j] = kMax ? fmaxf(keep, recv) : keep + recv;
   }
 }
+// The steps S = 8, 4, 2, 1 on 16 heads, then lanes l and l ^ 16 combined:
+// v[0] of lane l ends as the reduction of head l % 16 over the 32 lanes, in an
+// order fixed by the lane numbering (lanes l and l ^ 16 hold the same value).
 template <bool kMax>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
-  butterfly_step<16, kMax>(v, lane);
+__device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lane) {
   butterfly_step<8, kMax>(v, lane);
   butterfly_step<4, kMax>(v, lane);
   butterfly_step<2, kMax>(v, lane);
   butterfly_step<1, kMax>(v, lane);
-  return v[0];
+  const float o = __shfl_xor_sync(0xFFFFFFFFu, v[0], 16);
+  return kMax ? fmaxf(v[0], o) : v[0] + o;
 }
 
 __device__ __forceinline__ void set_abort(Ctl* c) {
@@ -297,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stale) and loaded after the dependency wait.  With q_early the caller has
   // declared Q complete before the kernel before this one started, and Q is
   // loaded and converted now, while that kernel runs.  Warp w converts heads
-  // w, w+12, ...; lane l dims 16l..16l+15 (32 bytes: lanes 4i..4i+3 share a
+  // w, w+20, ...; lane l dims 16l..16l+15 (32 bytes: lanes 4i..4i+3 share a
   // 128-byte line).
   constexpr int kQPer = (kHeads + kThreads / 32 - 1) / (kThreads / 32);
   uint4 qa[kQPer], qb[kQPer];
@@ -438,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- the first two tiles (both ring stages are free) are gathered by every
   // warp but the MMA warp: the softmax warps have nothing to do before the
   // first S is ready, and each warp issues its copies one after another.
-  // Copy g of the pair is issued by warp g % 11, lane g / 11 (tile 0's copies
+  // Copy g of the pair is issued by warp g % 19, lane g / 19 (tile 0's copies
   // come first in every warp).
   const int first = min(ntiles, 2);
   if (warp != kMmaWarp) {
@@ -557,32 +553,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ softmax
     // Every softmax warp passes the same named barriers in the same order
     // whatever happens (a timed-out wait only makes the warp skip work), so a
-    // timeout can never leave a barrier short of threads.
+    // timeout can never leave a barrier short of threads.  Softmax warp w
+    // (0..15) reads TMEM lanes 32*(w%4).. (its tokens) and heads 16*(w/4)..;
+    // lane l reduces for head hh + l%16.
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. = tokens
-    const int hh = ((warp - kSoftmaxWarp0) >> 2) * 32;  // heads hh .. hh+31
+    const int hh = ((warp - kSoftmaxWarp0) >> 2) * kHpt;  // heads hh .. hh+15
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int tok = quarter * 32 + lane;
-    float ls[32];                                 // this token lane's share of each head's sum
+    const int hl = hh + (lane & (kHpt - 1));
+    float ls[kHpt];                               // this token lane's share of each head's sum
 #pragma unroll
-    for (int i = 0; i < 32; ++i) ls[i] = 0.0f;
-    float m_lane = -INFINITY;  // running maximum of head hh + lane (log2 units)
+    for (int i = 0; i < kHpt; ++i) ls[i] = 0.0f;
+    float m_lane = -INFINITY;  // running maximum of head hl (log2 units)
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int b = t & 1;
-      float z[32];
+      float z[kHpt];
       if (ok) ok = warp_wait(ctl, &ctl->sfull[b], (t >> 1) & 1, lane, p.err, r, p.wait_ns);
       if (ok) {
-        float zl[32];
+        float zl[kHpt];
         tc_fence_after();
-        tmem_load32(tmem + lane_base + b * 2 * kHeads + hh, z);
-        tmem_load32(tmem + lane_base + b * 2 * kHeads + kHeads + hh, zl);
+        tmem_load16(tmem + lane_base + b * 2 * kHeads + hh, z);
+        tmem_load16(tmem + lane_base + b * 2 * kHeads + kHeads + hh, zl);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->sfree[b]);
         const int e = t * kTok + tok;
         const bool valid = e < nj && ctl->slot[e] >= 0;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
+        for (int i = 0; i < kHpt; i += 4) {
           const float4 qe = *reinterpret_cast<const float4*>(&ctl->qexp[hh + i]);
           z[i] = valid ? (z[i] + zl[i]) * qe.x : -INFINITY;
           z[i + 1] = valid ? (z[i + 1] + zl[i + 1]) * qe.y : -INFINITY;
@@ -591,11 +590,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = -INFINITY;
+        for (int i = 0; i < kHpt; ++i) z[i] = -INFINITY;
       }
       bool exceed = false;
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
+      for (int i = 0; i < kHpt; i += 4) {
         const float4 mr = *reinterpret_cast<const float4*>(&ctl->mrun[hh + i]);
         exceed |= z[i] > mr.x + kPMaxLog2;
         exceed |= z[i + 1] > mr.y + kPMaxLog2;
@@ -606,23 +605,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (softmax_sync_or(exceed)) {
         // Tile maximum of every head, then the new running maxima.
         {
-          float w[32];
+          float w[kHpt];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = z[i];
-          ctl->red[quarter][hh + lane] = warp_transpose_reduce<true>(w, lane);
+          for (int i = 0; i < kHpt; ++i) w[i] = z[i];
+          const float tq = warp_transpose_reduce16<true>(w, lane);
+          if (lane < kHpt) ctl->red[quarter][hl] = tq;
         }
         softmax_sync();
-        const float tm = fmaxf(fmaxf(ctl->red[0][hh + lane], ctl->red[1][hh + lane]),
-                               fmaxf(ctl->red[2][hh + lane], ctl->red[3][hh + lane]));
+        const float tm = fmaxf(fmaxf(ctl->red[0][hl], ctl->red[1][hl]),
+                               fmaxf(ctl->red[2][hl], ctl->red[3][hl]));
         float alpha = 1.0f;
         if (tm > m_lane + kPMaxLog2) {
           const float mn = tm - kPResetLog2;
           alpha = exp2f(m_lane - mn);  // 0 while nothing was accumulated
           m_lane = mn;
         }
-        float a[32];
+        float a[kHpt];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < kHpt; ++i) {
           a[i] = __shfl_sync(0xFFFFFFFFu, alpha, i);
           ls[i] *= a[i];
         }
@@ -635,24 +635,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll 1
             for (int mb = 0; mb < 4; ++mb) {
-              float v[32];
+              float v[kHpt];
               const uint32_t taddr = tmem + lane_base + kOCol + mb * kHeads + hh;
-              tmem_load32(taddr, v);
+              tmem_load16(taddr, v);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= a[i];
-              tmem_store32(taddr, v);
+              for (int i = 0; i < kHpt; ++i) v[i] *= a[i];
+              tmem_store16(taddr, v);
             }
             tmem_store_wait();
           }
         }
         softmax_sync();                        // every warp has read red[] and the old mrun
-        if (quarter == 0) ctl->mrun[hh + lane] = m_lane;
+        if (quarter == 0 && lane < kHpt) ctl->mrun[hl] = m_lane;
         softmax_sync();                        // the new mrun is visible
       }
       // p = 2^(z - m) as two E4M3 terms (hi, lo); the sums add the unrounded p.
-      uint32_t hiw[8], low[8];
+      uint32_t hiw[kHpt / 4], low[kHpt / 4];
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
+      for (int i = 0; i < kHpt; i += 4) {
         const float4 mr = *reinterpret_cast<const float4*>(&ctl->mrun[hh + i]);
         const float mm[4] = {mr.x, mr.y, mr.z, mr.w};
         uint16_t hc[2], lc[2];
@@ -673,13 +673,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The P buffer is free once the previous tile's O MMAs are complete.
       if (ok && t > 0 && !waited_o) ok = warp_wait(ctl, &ctl->odone, (t - 1) & 1, lane, p.err, r, p.wait_ns);
       if (ok) {
-        // P^T row `tok`: hi bytes of heads hh.. = chunks hh/16, +1; lo = 4 + hh/16, +1.
+        // P^T row `tok`: hi bytes of heads hh.. = chunk hh/16; lo = chunk 4 + hh/16.
         uint8_t* row = pop + tok * 128;
         const int c0 = hh >> 4, sw = tok & 7;
         *reinterpret_cast<uint4*>(row + ((c0 ^ sw) * 16)) = make_uint4(hiw[0], hiw[1], hiw[2], hiw[3]);
-        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ sw) * 16)) = make_uint4(hiw[4], hiw[5], hiw[6], hiw[7]);
         *reinterpret_cast<uint4*>(row + (((c0 + 4) ^ sw) * 16)) = make_uint4(low[0], low[1], low[2], low[3]);
-        *reinterpret_cast<uint4*>(row + (((c0 + 5) ^ sw) * 16)) = make_uint4(low[4], low[5], low[6], low[7]);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -690,12 +688,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- epilogue: the last O MMAs, per-head sums in fixed order, output
     if (ok && ntiles > 0) ok = warp_wait(ctl, &ctl->odone, (ntiles - 1) & 1, lane, p.err, r, p.wait_ns);
     tc_fence_after();
-    const float l_quarter = warp_transpose_reduce<false>(ls, lane);
-    ctl->red[quarter][hh + lane] = l_quarter;
+    const float l_quarter = warp_transpose_reduce16<false>(ls, lane);
+    if (lane < kHpt) ctl->red[quarter][hl] = l_quarter;
     softmax_sync();
-    const int hl = hh + lane;
     const float l_lane = ((ctl->red[0][hl] + ctl->red[1][hl]) + ctl->red[2][hl]) + ctl->red[3][hl];
-    if (quarter == 0) {
+    if (quarter == 0 && lane < kHpt) {
       if (nsplit > 1)
         reinterpret_cast<float2*>(p.part_ml)[((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit +
                                               split) * kHeads + hl] = make_float2(m_lane, l_lane);
@@ -711,28 +708,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the partials bound this epilogue) -- with (max, sum) beside it.
     const float sc_lane =
         (m_lane != -INFINITY && l_lane > 0.0f) ? (nsplit > 1 ? 1.0f : p.kv_scale) / l_lane : 0.0f;
-    float sc[32];
+    float sc[kHpt];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, sc_lane, i);
+    for (int i = 0; i < kHpt; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, sc_lane, i);
 #pragma unroll 1
     for (int mb = 0; mb < 4; ++mb) {
-      float v[32];
+      float v[kHpt];
       const int d = mb * 128 + quarter * 32 + lane;
       if (ok && ntiles > 0) {  // (ok is uniform over the warp: tcgen05.ld is warp-collective)
-        tmem_load32(tmem + lane_base + kOCol + mb * kHeads + hh, v);
+        tmem_load16(tmem + lane_base + kOCol + mb * kHeads + hh, v);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        for (int i = 0; i < kHpt; ++i) v[i] = 0.0f;
       }
       if (nsplit > 1) {
         uint16_t* dst = p.part_o + ((static_cast<int64_t>(r) * gridDim.y + hg) * nsplit + split) *
                                        (kHeads * 512) + d;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dst[(hh + i) * 512] = __half_as_ushort(__float2half_rn(v[i] * sc[i]));
+        for (int i = 0; i < kHpt; ++i) dst[(hh + i) * 512] = __half_as_ushort(__float2half_rn(v[i] * sc[i]));
       } else {
         uint16_t* dst = p.out + (static_cast<int64_t>(r) * p.heads + head0) * 512 + d;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < kHpt; ++i)
           if (hh + i < nheads)
             dst[(hh + i) * 512] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i] * sc[i]));
       }
