@@ -229,7 +229,8 @@ def time_path(wl, dev, K, warmup, eager, world, api, path, shard):
 
     def one_step(dw, evs=None):
         s = torch.cuda.current_stream()
-        calls = ([dw.latent_write] if wl.has_write else []) + [dw.index_scores, dw.select_topk,
+        calls = ([dw.latent_write] if wl.has_write else []) + [lambda: dw.index_scores(inputs_early=True),
+                                                               dw.select_topk,
                                                                lambda: dw.mla_decode(q_early=True)]
         if evs is not None:
             evs[0].record(s)

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 3
+#define DSA_ABI_VERSION 4
 #define DSA_LATENT_DIM 512
 
 typedef enum dsa_status {
@@ -148,6 +148,27 @@ dsa_status dsa_index_scores(const dsa_rows *rows, const float *q_idx, const floa
                             const int64_t *idx_base, int32_t index_heads, int32_t index_dim,
                             int32_t rows_per_seq, int32_t max_len, float *scores,
                             const int32_t *idx_written, void *stream);
+
+/*
+ * S1 with flags.  dsa_index_scores is this call with flags 0.
+ * DSA_INDEX_INPUTS_BEFORE_PREDECESSOR: the caller asserts that every input of
+ * the call (q_idx, head_w, idx_k, idx_gate, idx_base, idx_written and the
+ * rows' seq_lens) was complete before the kernel issued just before this call
+ * on the stream started -- for instance a decode step whose queries and keys
+ * were produced before its latent write, or steps replayed back to back over
+ * resident inputs.  The indexer may then load its inputs, run its MMAs and
+ * compute its scores while that kernel still runs; its stores to `scores`
+ * (which a kernel before may still read) and its completion still wait for
+ * that kernel.  Do not set it when the kernel before writes an input (an
+ * indexer write or a projection producing q_idx).  The results are
+ * bit-identical either way.  Unknown flag bits: DSA_ERR_INVALID_ARG.
+ */
+#define DSA_INDEX_INPUTS_BEFORE_PREDECESSOR 1u
+dsa_status dsa_index_scores_ex(const dsa_rows *rows, const float *q_idx, const float *head_w,
+                               const uint16_t *idx_k, const uint16_t *idx_gate, int64_t idx_tokens,
+                               const int64_t *idx_base, int32_t index_heads, int32_t index_dim,
+                               int32_t rows_per_seq, int32_t max_len, float *scores,
+                               const int32_t *idx_written, uint32_t flags, void *stream);
 
 /*
  * S2 -- per-row top-k ("glm5next_dsa/layer.rs", notes on batch_select_enabled

@@ -57,6 +57,7 @@ def load() -> ctypes.CDLL:
     sig = {
         "dsa_latent_write": [RP, P, P, P, i64, i32, f32, f32, P],
         "dsa_index_scores": [RP, P, P, P, P, i64, P, i32, i32, i32, i32, P, P, P],
+        "dsa_index_scores_ex": [RP, P, P, P, P, i64, P, i32, i32, i32, i32, P, P, u32, P],
         "dsa_select_topk": [RP, P, i32, i32, P, P],
         "dsa_mla_decode_fp8": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, sz, P],
         "dsa_mla_decode_fp8_ex": [RP, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, sz, u32, P],
@@ -152,21 +153,32 @@ def dsa_latent_write(rows: Rows, kv_a: torch.Tensor, norm_w: torch.Tensor, pool:
     _check("dsa_latent_write", st)
 
 
+DSA_INDEX_INPUTS_BEFORE_PREDECESSOR = 1
+
+
 def dsa_index_scores(rows: Rows, q_idx: torch.Tensor, head_w: torch.Tensor, idx_k: torch.Tensor,
                      idx_gate: torch.Tensor, idx_base: torch.Tensor, rows_per_seq: int,
                      max_len: int, scores: torch.Tensor, idx_written: torch.Tensor | None = None,
-                     stream=None) -> None:
+                     stream=None, inputs_early: bool = False) -> None:
     """``idx_written``: optional int32 [R / rows_per_seq] rows written per
-    sequence; a row past its sequence's count is skipped and recorded."""
+    sequence; a row past its sequence's count is skipped and recorded.
+    ``inputs_early``: every input was complete before the kernel issued just
+    before this call started (dsa_index_scores_ex with
+    DSA_INDEX_INPUTS_BEFORE_PREDECESSOR)."""
     lib = load()
     heads, dim = q_idx.shape[-2], q_idx.shape[-1]
-    st = lib.dsa_index_scores(ctypes.byref(rows), _ptr(q_idx, torch.float32, "q_idx"),
-                              _ptr(head_w, torch.float32, "head_w"), _ptr(idx_k, torch.uint16, "idx_k"),
-                              _ptr(idx_gate, torch.uint16, "idx_gate"), idx_k.shape[0],
-                              _ptr(idx_base, torch.int64, "idx_base"), heads, dim, int(rows_per_seq),
-                              int(max_len), _ptr(scores, torch.float32, "scores"),
-                              _ptr(idx_written, torch.int32, "idx_written"), _stream(stream))
-    _check("dsa_index_scores", st)
+    args = [ctypes.byref(rows), _ptr(q_idx, torch.float32, "q_idx"),
+            _ptr(head_w, torch.float32, "head_w"), _ptr(idx_k, torch.uint16, "idx_k"),
+            _ptr(idx_gate, torch.uint16, "idx_gate"), idx_k.shape[0],
+            _ptr(idx_base, torch.int64, "idx_base"), heads, dim, int(rows_per_seq),
+            int(max_len), _ptr(scores, torch.float32, "scores"),
+            _ptr(idx_written, torch.int32, "idx_written")]
+    if inputs_early:
+        st = lib.dsa_index_scores_ex(*args, DSA_INDEX_INPUTS_BEFORE_PREDECESSOR, _stream(stream))
+        _check("dsa_index_scores_ex", st)
+    else:
+        st = lib.dsa_index_scores(*args, _stream(stream))
+        _check("dsa_index_scores", st)
 
 
 def dsa_select_topk(rows: Rows, scores: torch.Tensor, max_len: int, topk: int, sel: torch.Tensor,

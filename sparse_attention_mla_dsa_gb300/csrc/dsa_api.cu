@@ -120,6 +120,17 @@ dsa_status dsa_index_scores(const dsa_rows* rows, const float* q_idx, const floa
                             const int64_t* idx_base, int32_t index_heads, int32_t index_dim,
                             int32_t rows_per_seq, int32_t max_len, float* scores,
                             const int32_t* idx_written, void* stream) {
+  return dsa_index_scores_ex(rows, q_idx, head_w, idx_k, idx_gate, idx_tokens, idx_base,
+                             index_heads, index_dim, rows_per_seq, max_len, scores, idx_written,
+                             0u, stream);
+}
+
+dsa_status dsa_index_scores_ex(const dsa_rows* rows, const float* q_idx, const float* head_w,
+                               const uint16_t* idx_k, const uint16_t* idx_gate, int64_t idx_tokens,
+                               const int64_t* idx_base, int32_t index_heads, int32_t index_dim,
+                               int32_t rows_per_seq, int32_t max_len, float* scores,
+                               const int32_t* idx_written, uint32_t flags, void* stream) {
+  if ((flags & ~DSA_INDEX_INPUTS_BEFORE_PREDECESSOR) != 0) return DSA_ERR_INVALID_ARG;
   dsa_status st = check_rows(rows, false);
   if (st != DSA_OK) return st;
   if (q_idx == nullptr || head_w == nullptr || idx_k == nullptr || idx_gate == nullptr ||
@@ -165,6 +176,7 @@ dsa_status dsa_index_scores(const dsa_rows* rows, const float* q_idx, const floa
   p.npad = ((sub * index_heads + 15) / 16) * 16;
   p.max_len = max_len;
   p.wait_ns = wait_limit_ns();
+  p.inputs_early = (flags & DSA_INDEX_INPUTS_BEFORE_PREDECESSOR) != 0 ? 1 : 0;
   plan_index_scores(p, dev->num_sms);
 
   // Key arena [idx_tokens, index_dim] bf16, boxes of 128 tokens x 64 dims

@@ -71,6 +71,8 @@ struct IndexParams {
   uint32_t tmem_cols;
   uint32_t smem_bytes;
   uint64_t wait_ns;
+  int32_t inputs_early;   // inputs complete before the kernel before started: only the
+                          // score stores (and the exit) wait for it
 };
 // Fills in direct / ctas / stages / tmem_cols / smem_bytes from the shape.
 void plan_index_scores(IndexParams& p, int num_sms);

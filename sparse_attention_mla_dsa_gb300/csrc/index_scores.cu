@@ -244,14 +244,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- before the wait
   // Every input may be the output of the kernel before (the key arena and
   // gates of an indexer write, q and the head weights of a projection, row
-  // metadata written on the device), so nothing is loaded before
-  // grid_dep_wait().  What overlaps the kernel before: barrier set-up, the
+  // metadata written on the device), so by default nothing is loaded before
+  // grid_dep_wait().  When the caller declares the inputs complete before the
+  // kernel before started (inputs_early), the wait moves to the epilogue's
+  // first score store and to the exit: the loads, MMAs and score arithmetic
+  // then overlap that kernel, and the scores buffer -- which a kernel before
+  // may still read -- is written after it completes.  What overlaps the
+  // kernel before in either case: barrier set-up, the
   // tensor map, and -- for a direct launch, or one of a single group, whose
   // split is known up to the row length -- L2 prefetches of the CTA's first
   // key tiles and of q (a
   // prefetch only warms L2, where the device's writes land, so it cannot make
   // a later load return a stale value; the arena base read for the address
   // may be stale, which only wastes the prefetch).
+  const bool inputs_early = p.inputs_early != 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&ctl->full[s], 1);
@@ -270,7 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_map(&kmap);
-    if (kDirect || groups == 1) {
+    // (With inputs_early the loads themselves go out right after the barrier
+    // below, so the prefetch and the load of the base it needs are skipped.)
+    if ((kDirect || groups == 1) && !inputs_early) {
       const long long tg = (p.max_len + kTileM - 1) / kTileM;
       const long long b0 = kDirect ? static_cast<long long>(blockIdx.x) * p.direct_tiles : tg * c / ctas;
       const long long b1 = kDirect ? b0 + p.direct_tiles : tg * (c + 1) / ctas;
@@ -284,7 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (kDirect || groups == 1) {
+  // A direct launch allocates TMEM now (it reads no input); a persistent one
+  // once the scan has shown that the CTA has tiles.
+  if (kDirect && warp == 1) {
+    tmem_alloc(&ctl->tmem_base, p.tmem_cols);
+    tmem_relinquish();
+  }
+  if ((kDirect || groups == 1) && !inputs_early) {
     const GroupRows gr = group_rows(p, kDirect ? blockIdx.y : 0);
     const float* qsrc = p.q_idx + static_cast<int64_t>(gr.r0) * p.heads * D;
     for (int off = threadIdx.x * 32; off < gr.nrows * p.heads * D; off += kThreads * 32)
@@ -294,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The barriers are initialised before any warp can arrive on or wait for
   // one: the roles below start without a CTA-wide barrier between them.
   __syncthreads();
-  grid_dep_wait();
+  if (!inputs_early) grid_dep_wait();
 
   // ---------------------------------------------------------------- this CTA's range
   // Warps 0-1 find the range -- pass 1: T = sum of T_g (CTA 0 records the
@@ -402,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     scan_sync();  // g0 / t0 / tg0 / base0 / my_tiles
    }
     if (warp == 1) {
-      if (my_tiles > 0) {
+      if (!kDirect && my_tiles > 0) {
         tmem_alloc(&ctl->tmem_base, p.tmem_cols);
         tmem_relinquish();
       }
@@ -662,6 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       build_q(gr.r0, gr.nrows);
     }
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    bool waited = !inputs_early;
     long long done = 0;
     int i = 0;        // tiles consumed by this CTA so far (TMEM buffer and phase)
     bool ok = true;
@@ -689,7 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // Each tile's gate is loaded one tile ahead, so the load's DRAM latency
       // hides behind the TMA and the MMAs (plain loads: the gates may come
-      // from the kernel before, which the wait at the top has ordered).
+      // from the kernel before, which the wait at the top has ordered unless
+      // the caller declared them complete before it).
       auto load_gate = [&](int j) {
         const int t = (t_first + j) * kTileM + lane_tok;
         return (j < n && t < max_len_group) ? p.gate[base + t] : static_cast<uint16_t>(0);
@@ -722,8 +738,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (col < nreal) sum = fmaf(w_s[col], fmaxf(v[e], 0.0f), sum);
             }
           }
-          if (t < sg.row_len[jr])
+          if (t < sg.row_len[jr]) {
+            if (!waited) {  // (inputs_early) the first store waits for the kernel before
+              grid_dep_wait();
+              waited = true;
+            }
             p.scores[static_cast<int64_t>(r0 + jr) * p.max_len + t] = gt * sum;
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -740,11 +761,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  // (inputs_early) No CTA completes before the kernel before has: whatever
+  // waits for this kernel also waits for that one.
+  if (inputs_early) grid_dep_wait();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1 && my_tiles > 0) {
+  if (warp == 1 && (kDirect || my_tiles > 0)) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, p.tmem_cols);
+    tmem_dealloc(kDirect ? ctl->tmem_base : tmem_base, p.tmem_cols);
   }
 }
 

@@ -89,9 +89,14 @@ class DeviceWorkload:
         api.dsa_latent_write(self.rows, self.kv_a, self.norm_w, self.pool, wl.eps, wl.kv_scale,
                              stream)
 
-    def index_scores(self, stream=None):
+    def index_scores(self, stream=None, inputs_early: bool = False):
+        """S1.  ``inputs_early``: the indexer's inputs (resident here, or
+        uploaded before the step) were complete before the kernel issued just
+        before this call started, so the indexer may load and score them
+        before its dependency wait (its stores still wait)."""
         api.dsa_index_scores(self.rows, self.q_idx, self.head_w, self.idx_k, self.idx_gate,
-                             self.idx_base, self.wl.group_rows, self.max_len, self.scores, stream)
+                             self.idx_base, self.wl.group_rows, self.max_len, self.scores,
+                             stream=stream, inputs_early=inputs_early)
 
     def select_topk(self, stream=None):
         api.dsa_select_topk(self.rows, self.scores, self.max_len, self.wl.topk, self.sel, stream)
@@ -109,7 +114,7 @@ class DeviceWorkload:
         """One pass of the whole hot path (S0 when the workload writes, S1-S3)."""
         if self.kv_a is not None:
             self.latent_write(stream)
-        self.index_scores(stream)
+        self.index_scores(stream, inputs_early=True)  # no kernel of the step writes its inputs
         self.select_topk(stream)
         self.mla_decode(stream, q_early=True)  # right after this workload's top-k
 

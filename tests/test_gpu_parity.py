@@ -298,3 +298,62 @@ def test_q_before_predecessor_flag_is_bit_identical(dsa):
                                    dw.workspace.data_ptr(),
                                    dw.workspace.numel() * dw.workspace.element_size(), 2, None)
     assert st == 1                                  # DSA_ERR_INVALID_ARG, nothing launched
+
+
+def _scores_bits(dw, fill_nan):
+    if fill_nan:
+        dw.scores.fill_(float("nan"))
+        torch.cuda.synchronize()
+    return dw.scores.view(torch.int32)
+
+
+def test_index_inputs_before_predecessor_flag(dsa):
+    """dsa_index_scores_ex with DSA_INDEX_INPUTS_BEFORE_PREDECESSOR (inputs
+    loaded and scored before the dependency wait, stores after it) writes the
+    same bits as the default order, in a direct and in a persistent launch;
+    right after a top-k that reads the same scores buffer its stores wait for
+    that top-k; unknown flag bits are refused."""
+    import ctypes
+    api, path = dsa
+    for wl in (workloads.scaled("single", len_div=8), workloads.scaled("verify", seqs=2, len_div=32),
+               workloads.scaled("batched", seqs=32, len_div=8)):      # the last is persistent
+        dw = path.DeviceWorkload(wl)
+        _scores_bits(dw, True)
+        dw.index_scores()
+        torch.cuda.synchronize()
+        ref = dw.scores.view(torch.int32).clone()
+        _scores_bits(dw, True)
+        dw.index_scores(inputs_early=True)
+        torch.cuda.synchronize()
+        assert api.dsa_get_error(reset=True)[0] == 0
+        assert torch.equal(dw.scores.view(torch.int32), ref), wl.name
+    # The predecessor reads the buffer the flagged call overwrites: a top-k over
+    # the scores of q, then the scores of -q into the same buffer.
+    wl = workloads.scaled("single", len_div=4)
+    dw = path.DeviceWorkload(wl)
+    q_neg = (-dw.q_idx).contiguous()
+    dw.index_scores()
+    dw.select_topk()
+    torch.cuda.synchronize()
+    sel_ref = dw.sel.clone()
+    ref_neg = path.DeviceWorkload(wl)
+    ref_neg.q_idx.copy_(q_neg)
+    ref_neg.index_scores()
+    torch.cuda.synchronize()
+    for _ in range(5):
+        dw.sel.fill_(-7)
+        dw.index_scores()
+        dw.select_topk()
+        api.dsa_index_scores(dw.rows, q_neg, dw.head_w, dw.idx_k, dw.idx_gate, dw.idx_base,
+                             wl.group_rows, dw.max_len, dw.scores, inputs_early=True)
+        torch.cuda.synchronize()
+        assert api.dsa_get_error(reset=True)[0] == 0
+        assert torch.equal(dw.sel, sel_ref)
+        L = int(wl.seq_lens[0])
+        assert torch.equal(dw.scores[:, :L].view(torch.int32), ref_neg.scores[:, :L].view(torch.int32))
+    lib = api.load()
+    st = lib.dsa_index_scores_ex(ctypes.byref(dw.rows), dw.q_idx.data_ptr(), dw.head_w.data_ptr(),
+                                 dw.idx_k.data_ptr(), dw.idx_gate.data_ptr(), dw.idx_k.shape[0],
+                                 dw.idx_base.data_ptr(), wl.index_heads, wl.index_dim,
+                                 wl.group_rows, dw.max_len, dw.scores.data_ptr(), None, 2, None)
+    assert st == 1                                  # DSA_ERR_INVALID_ARG, nothing launched
