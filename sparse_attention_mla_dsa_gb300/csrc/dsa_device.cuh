@@ -93,6 +93,8 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
 // Limits below this are short: every poll is bounded (32 ns suspend) and
 // followed by a look at the clock, so the limit holds to within a poll.
 constexpr uint64_t kShortWaitNs = 1000ull * 1000ull;
+// Longest time a poll may leave the thread suspended.
+constexpr uint32_t kSuspendHintNs = 1000;
 
 // The polling loop of mbar_wait, out of line so that the kernels' wait sites
 // stay small (a wait that gets here is waiting anyway).
@@ -106,7 +108,7 @@ static __device__ __noinline__ bool mbar_wait_polls(uint64_t* bar, uint32_t pari
     return false;
   }
   for (uint32_t i = 1; i < (1u << 30); ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, kSuspendHintNs)) return true;
     if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
   }
   return false;

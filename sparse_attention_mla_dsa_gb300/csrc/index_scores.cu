@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&kmap);
     // (With inputs_early the loads themselves go out right after the barrier
     // below, so the prefetch and the load of the base it needs are skipped.)
-    if ((kDirect || groups == 1) && !inputs_early) {
+    if (kDirect || groups == 1) {
       const long long tg = (p.max_len + kTileM - 1) / kTileM;
       const long long b0 = kDirect ? static_cast<long long>(blockIdx.x) * p.direct_tiles : tg * c / ctas;
       const long long b1 = kDirect ? b0 + p.direct_tiles : tg * (c + 1) / ctas;

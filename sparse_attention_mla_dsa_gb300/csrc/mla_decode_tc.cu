@@ -767,8 +767,12 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
   const int nsplit = p.splits;
   const int64_t base = (static_cast<int64_t>(r) * groups + hg) * nsplit;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  grid_dep_wait();  // the partials come from the kernel before
+  // The successor (the next step's indexer) may start now: a kernel that
+  // reads what this one writes waits for it in any case, and an indexer whose
+  // caller declared its inputs ready scores its keys while the attend and
+  // this merge finish.
   grid_dep_launch();
+  grid_dep_wait();  // the partials come from the kernel before
   float mmax = -INFINITY;
   float lsum = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
