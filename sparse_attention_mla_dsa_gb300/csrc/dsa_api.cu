@@ -210,7 +210,7 @@ dsa_status dsa_select_topk(const dsa_rows* rows, const float* scores, int32_t ma
   p.rows = rows->rows;
   p.max_len = max_len;
   p.topk = topk;
-  p.cluster = topk_cluster_size(max_len);
+  p.cluster = topk_cluster_size(max_len, rows->rows, dev->num_sms);
   if (topk_smem_bytes(max_len, p.cluster) > 227u * 1024u) return DSA_ERR_UNSUPPORTED;
   return launched(launch_select_topk(p, static_cast<cudaStream_t>(stream)));
 }

@@ -89,7 +89,8 @@ struct TopkParams {
   int32_t topk;
   int32_t cluster;   // CTAs per row (one thread-block cluster)
 };
-int topk_cluster_size(int32_t max_len);
+// CTAs per row (one cluster) for `rows` rows of max_len keys.
+int topk_cluster_size(int32_t max_len, int32_t rows, int num_sms);
 size_t topk_smem_bytes(int32_t max_len, int cluster);
 cudaError_t launch_select_topk(const TopkParams& p, cudaStream_t stream);
 

@@ -18,6 +18,13 @@
 // prefix of the per-CTA counts over the cluster gives each CTA its output
 // offset and its share of the tied tokens, and block-wide prefix sums order
 // the writes inside it.
+//
+// The cluster size follows the row length (about 4k keys per CTA).  When the
+// launch would then need more than one wave of CTAs (two per SM) and fewer
+// CTAs per row still keep their slices in shared memory with two CTAs per SM,
+// the cluster is cut to what one wave holds, down to one CTA per row (many
+// short rows: a prefill).  The selection is exact, so the cluster size never
+// changes a result.
 #include "dsa_device.cuh"
 #include "dsa_internal.h"
 
@@ -29,6 +36,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;             // 8-bit digits
 constexpr int kItems = 8;              // consecutive tokens per thread in the output pass
 constexpr int kKeysPerCta = 4096;      // target keys per CTA when choosing the cluster size
+constexpr size_t kTwoPerSmBytes = 112 * 1024;  // shared memory that leaves room for two CTAs per SM
 
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -329,9 +337,16 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
 
 }  // namespace
 
-int topk_cluster_size(int32_t max_len) {
+int topk_cluster_size(int32_t max_len, int32_t rows, int num_sms) {
   int c = (max_len + kKeysPerCta - 1) / kKeysPerCta;
-  return c < 1 ? 1 : (c > 8 ? 8 : c);
+  c = c < 1 ? 1 : (c > 8 ? 8 : c);
+  const long long wave = 2LL * (num_sms > 0 ? num_sms : 1);  // two CTAs per SM
+  if (static_cast<long long>(rows) * c > wave) {
+    const long long fit = wave / (rows > 0 ? rows : 1);
+    const int cut = static_cast<int>(fit < 1 ? 1 : fit);
+    if (cut < c && topk_smem_bytes(max_len, cut) <= kTwoPerSmBytes) c = cut;
+  }
+  return c;
 }
 
 size_t topk_smem_bytes(int32_t max_len, int cluster) {

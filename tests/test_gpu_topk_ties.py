@@ -3,6 +3,11 @@ signed zeros and negatives, over row lengths that exercise one CTA and
 clusters of five and eight CTAs per row, against the oracle's full-sort selection
 ("glm5next_dsa/layer.rs", notes on batch_select_enabled / select_rows_batched:
 score DESC, then index ASC).  Bit-exact: the selection is integer work.
+
+Launches with more rows than one wave of clusters holds take smaller clusters
+where the slices still fit in shared memory (seven, one CTA per row); with long
+rows they keep eight CTAs over two waves.  Those launches are checked the same
+way.
 """
 import numpy as np
 import pytest
@@ -35,6 +40,12 @@ def _patterns(rng, n):
     (20000, [2049, 5000, 20000]),                      # clusters of five CTAs
     (70000, [2049, 5000, 40000, 70000]),               # clusters of eight CTAs
     (270000, [33000, 140000, 270000]),                 # eight CTAs, 34k keys each
+    # 40 rows of 64k: clusters cut from eight to seven CTAs (one wave)
+    (65536, [2049, 65536, 40000] + [2100 + 97 * i for i in range(37)]),
+    # 64 rows of 128k: eight CTAs per row over two waves (four would not fit)
+    (131072, [2049, 131072, 70000, 99999] + [2100 + 37 * i for i in range(60)]),
+    # 400 rows of 9k: one CTA per row
+    (9000, [9000, 2049, 2048, 1] + [2050 + 17 * i for i in range(396)]),
 ])
 def test_topk_ties_match_oracle(api, oracle, max_len, lens):
     rng = np.random.default_rng(11)
