@@ -115,6 +115,25 @@ __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
+// 32 consecutive 32-bit TMEM columns of this thread's lane, one wait for all.
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // ---------------------------------------------------------------- launch groups
 struct GroupRows {
   int seq, seq_row0, r0, nrows;
@@ -696,7 +715,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r0 = sg.r0, nrows = sg.nrows, n = sg.ntiles, t_first = sg.t_first;
       const int max_len_group = sg.max_len;
       const int64_t base = sg.base;
-      const int nreal = nrows * heads;
       // Later segments: the previous segment's MMAs are complete (this warp
       // consumed its last accumulator), so the operand can be rewritten.
       if (k > 0) build_q(r0, nrows);
@@ -727,15 +745,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t acc = lane_addr + a * npad;
         for (int jr = 0; jr < nrows; ++jr) {
+          // Columns in ascending order, 32 per TMEM read (16 at an odd end).
+          // Columns past the real ones hold 0 (zero q rows) with weight 0, so
+          // they add +-0 and leave the sum as it is (it is never -0).
           float sum = 0.0f;
-          const int c_begin = jr * cols_per_row;
-          for (int c0 = c_begin; c0 < c_begin + cols_per_row; c0 += 16) {
+          const int c_begin = jr * cols_per_row, c_end = c_begin + cols_per_row;
+          int c0 = c_begin;
+          for (; c0 + 32 <= c_end; c0 += 32) {
+            float v[32];
+            tmem_load32(acc + c0, v);
+            const float4* w4 = reinterpret_cast<const float4*>(w_s + c0);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 w = w4[e];
+              sum = fmaf(w.x, fmaxf(v[4 * e], 0.0f), sum);
+              sum = fmaf(w.y, fmaxf(v[4 * e + 1], 0.0f), sum);
+              sum = fmaf(w.z, fmaxf(v[4 * e + 2], 0.0f), sum);
+              sum = fmaf(w.w, fmaxf(v[4 * e + 3], 0.0f), sum);
+            }
+          }
+          if (c0 < c_end) {
             float v[16];
             tmem_load16(acc + c0, v);
+            const float4* w4 = reinterpret_cast<const float4*>(w_s + c0);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int col = c0 + e;
-              if (col < nreal) sum = fmaf(w_s[col], fmaxf(v[e], 0.0f), sum);
+            for (int e = 0; e < 4; ++e) {
+              const float4 w = w4[e];
+              sum = fmaf(w.x, fmaxf(v[4 * e], 0.0f), sum);
+              sum = fmaf(w.y, fmaxf(v[4 * e + 1], 0.0f), sum);
+              sum = fmaf(w.z, fmaxf(v[4 * e + 2], 0.0f), sum);
+              sum = fmaf(w.w, fmaxf(v[4 * e + 3], 0.0f), sum);
             }
           }
           if (t < sg.row_len[jr]) {

@@ -685,9 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    // ---- epilogue: the last O MMAs, per-head sums in fixed order, output
-    if (ok && ntiles > 0) ok = warp_wait(ctl, &ctl->odone, (ntiles - 1) & 1, lane, p.err, r, p.wait_ns);
-    tc_fence_after();
+    // ---- epilogue: per-head sums in fixed order (while the last O MMAs
+    // run), then the output once they are complete
     const float l_quarter = warp_transpose_reduce16<false>(ls, lane);
     if (lane < kHpt) ctl->red[quarter][hl] = l_quarter;
     softmax_sync();
@@ -711,6 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float sc[kHpt];
 #pragma unroll
     for (int i = 0; i < kHpt; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, sc_lane, i);
+    if (ok && ntiles > 0) ok = warp_wait(ctl, &ctl->odone, (ntiles - 1) & 1, lane, p.err, r, p.wait_ns);
+    tc_fence_after();
 #pragma unroll 1
     for (int mb = 0; mb < 4; ++mb) {
       float v[kHpt];
