@@ -20,11 +20,12 @@
 // the writes inside it.
 //
 // The cluster size follows the row length (about 4k keys per CTA).  When the
-// launch would then need more than one wave of CTAs (two per SM) and fewer
-// CTAs per row still keep their slices in shared memory with two CTAs per SM,
-// the cluster is cut to what one wave holds, down to one CTA per row (many
-// short rows: a prefill).  The selection is exact, so the cluster size never
-// changes a result.
+// launch would then need more CTAs than there are SMs and fewer CTAs per row
+// still keep their slices in shared memory with two CTAs per SM, the cluster
+// is cut to one CTA per SM (32 rows of 64k: four CTAs each), else to what one
+// wave of two CTAs per SM holds, down to one CTA per row (many short rows: a
+// prefill).  The selection is exact, so the cluster size never changes a
+// result.
 #include "dsa_device.cuh"
 #include "dsa_internal.h"
 
@@ -340,11 +341,17 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
 int topk_cluster_size(int32_t max_len, int32_t rows, int num_sms) {
   int c = (max_len + kKeysPerCta - 1) / kKeysPerCta;
   c = c < 1 ? 1 : (c > 8 ? 8 : c);
-  const long long wave = 2LL * (num_sms > 0 ? num_sms : 1);  // two CTAs per SM
-  if (static_cast<long long>(rows) * c > wave) {
-    const long long fit = wave / (rows > 0 ? rows : 1);
+  // One CTA per SM first (clusters then pack into the GPCs without a
+  // straggler wave), else two.
+  const long long sms = num_sms > 0 ? num_sms : 1;
+  for (long long slots = sms; slots <= 2 * sms; slots += sms) {
+    if (static_cast<long long>(rows) * c <= slots) break;
+    const long long fit = slots / (rows > 0 ? rows : 1);
     const int cut = static_cast<int>(fit < 1 ? 1 : fit);
-    if (cut < c && topk_smem_bytes(max_len, cut) <= kTwoPerSmBytes) c = cut;
+    if (cut < c && topk_smem_bytes(max_len, cut) <= kTwoPerSmBytes) {
+      c = cut;
+      break;
+    }
   }
   return c;
 }
