@@ -103,7 +103,7 @@ struct alignas(16) TopkShared {
   int bin_tot[4][kBins];         // per-pass bin totals of this CTA (read remotely)
   int scan_tmp[2 * kBins];       // per-bin exclusive prefix and count of the current pass
   alignas(8) int counts[2];      // this CTA's (key > T, key == T) counts
-  int warp_tot[kWarps];
+  alignas(16) int warp_tot[kWarps];
   int found_bin, found_above, found_count;
 };
 static_assert(sizeof(TopkShared) % 16 == 0, "keys must start 16-byte aligned");
@@ -220,8 +220,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
     }
     __syncthreads();
     if (warp < kBins / 32) {
-      int before = 0;
-      for (int w = 0; w < warp; ++w) before += sh.warp_tot[w];
+      // Totals of the scanning warps before this one (two vector loads).
+      const int4 t0 = *reinterpret_cast<const int4*>(&sh.warp_tot[0]);
+      const int4 t1 = *reinterpret_cast<const int4*>(&sh.warp_tot[4]);
+      const int before = (warp > 0 ? t0.x : 0) + (warp > 1 ? t0.y : 0) + (warp > 2 ? t0.z : 0) +
+                         (warp > 3 ? t0.w : 0) + (warp > 4 ? t1.x : 0) + (warp > 5 ? t1.y : 0) +
+                         (warp > 6 ? t1.z : 0);
       const int above = before + sh.scan_tmp[warp * 32 + lane];
       const int c = sh.scan_tmp[kBins + warp * 32 + lane];
       if (above < remaining && above + c >= remaining) {
