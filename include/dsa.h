@@ -208,9 +208,10 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  * tensor cores; the softmax weights enter the weighted sum as two E4M3 terms
  * (about bf16 precision; weights 2^18 below a head's largest drop out), the
  * normalising sums and lse use the unrounded weights.  A row's selection is
- * cut into splits of at most 256 entries (2048 with more than 64 heads) whose
- * count depends only on topk and heads, so each row's result is bit-identical
- * whatever the other rows of the call are.  With more than one split each
+ * cut into splits of at most 256 entries (2048 with more than 64 heads; 512
+ * with DSA_DECODE_LONG_SPLITS, below) whose count depends only on topk, heads
+ * and that flag, so each row's result is bit-identical whatever the other
+ * rows of the call are.  With more than one split each
  * split's normalised partial output O/l (a convex combination of latent
  * values, kept in fp16: 2^-11 relative) and its (max, sum) pass through the
  * workspace (L2-resident, discarded after the merge), which must hold
@@ -225,6 +226,14 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uin
 
 /*
  * S3 with flags.  dsa_mla_decode_fp8 is this call with flags 0.
+ * DSA_DECODE_LONG_SPLITS: with at most 64 heads, splits of at most 512
+ * entries instead of 256 (half the CTAs, each twice as long: for launches
+ * with many rows, whose CTAs otherwise fill the GPU in more waves; a single
+ * row runs faster without it).  The split count then depends on topk, heads
+ * and this flag, still never on the other rows: calls whose results must
+ * agree bit for bit (a K-row verify and the same rows run one at a time) use
+ * the same value of the flag.  The workspace from dsa_workspace_bytes covers
+ * both plans.
  * DSA_DECODE_Q_BEFORE_PREDECESSOR: the caller asserts that q was complete
  * before the kernel issued just before this call on the stream started (the
  * usual decode order: q comes from a projection before the indexer, and the
@@ -236,6 +245,7 @@ dsa_status dsa_mla_decode_fp8(const dsa_rows *rows, const uint16_t *q, const uin
  * DSA_ERR_INVALID_ARG.
  */
 #define DSA_DECODE_Q_BEFORE_PREDECESSOR 1u
+#define DSA_DECODE_LONG_SPLITS 2u
 dsa_status dsa_mla_decode_fp8_ex(const dsa_rows *rows, const uint16_t *q, const uint8_t *pool,
                                  int64_t nslots, const int32_t *sel, int32_t topk, int32_t heads,
                                  int32_t latent_dim, float kv_scale, float sm_scale, uint16_t *out,

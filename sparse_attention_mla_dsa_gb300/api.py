@@ -190,15 +190,18 @@ def dsa_select_topk(rows: Rows, scores: torch.Tensor, max_len: int, topk: int, s
 
 
 DSA_DECODE_Q_BEFORE_PREDECESSOR = 1
+DSA_DECODE_LONG_SPLITS = 2
 
 
 def dsa_mla_decode_fp8(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: torch.Tensor, topk: int,
                        kv_scale: float, sm_scale: float, out: torch.Tensor,
                        lse: torch.Tensor | None, workspace: torch.Tensor | None = None,
-                       stream=None, q_early: bool = False) -> None:
+                       stream=None, q_early: bool = False, long_splits: bool = False) -> None:
     """``out`` may be a CUDA tensor or a pinned host tensor (written directly).
     ``q_early``: q was complete before the kernel issued just before this
-    call started (dsa_mla_decode_fp8_ex with DSA_DECODE_Q_BEFORE_PREDECESSOR)."""
+    call started (dsa_mla_decode_fp8_ex with DSA_DECODE_Q_BEFORE_PREDECESSOR).
+    ``long_splits``: 512-entry splits at up to 64 heads (DSA_DECODE_LONG_SPLITS);
+    calls whose rows must agree bit for bit pass the same value."""
     lib = load()
     heads = q.shape[-2]
     args = [ctypes.byref(rows), _ptr(q, torch.uint16, "q"), _ptr(pool, torch.uint8, "pool"),
@@ -206,8 +209,10 @@ def dsa_mla_decode_fp8(rows: Rows, q: torch.Tensor, pool: torch.Tensor, sel: tor
             float(kv_scale), float(sm_scale), _ptr(out, torch.uint16, "out", host_ok=True),
             _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
             0 if workspace is None else workspace.numel() * workspace.element_size()]
-    if q_early:
-        st = lib.dsa_mla_decode_fp8_ex(*args, DSA_DECODE_Q_BEFORE_PREDECESSOR, _stream(stream))
+    flags = ((DSA_DECODE_Q_BEFORE_PREDECESSOR if q_early else 0)
+             | (DSA_DECODE_LONG_SPLITS if long_splits else 0))
+    if flags:
+        st = lib.dsa_mla_decode_fp8_ex(*args, flags, _stream(stream))
         _check("dsa_mla_decode_fp8_ex", st)
     else:
         st = lib.dsa_mla_decode_fp8(*args, _stream(stream))

@@ -229,7 +229,7 @@ dsa_status dsa_mla_decode_fp8_ex(const dsa_rows* rows, const uint16_t* q, const 
                                  int32_t latent_dim, float kv_scale, float sm_scale,
                                  uint16_t* out, float* lse_or_null, void* workspace,
                                  size_t workspace_bytes, uint32_t flags, void* stream) {
-  if ((flags & ~static_cast<uint32_t>(DSA_DECODE_Q_BEFORE_PREDECESSOR)) != 0u)
+  if ((flags & ~static_cast<uint32_t>(DSA_DECODE_Q_BEFORE_PREDECESSOR | DSA_DECODE_LONG_SPLITS)) != 0u)
     return DSA_ERR_INVALID_ARG;
   dsa_status st = check_rows(rows, true);
   if (st != DSA_OK) return st;
@@ -271,6 +271,7 @@ dsa_status dsa_mla_decode_fp8_ex(const dsa_rows* rows, const uint16_t* q, const 
   // ones start after it has finished, and for them the default order (q and
   // the selection loaded together after the wait) is the faster one.
   p.q_early = (flags & DSA_DECODE_Q_BEFORE_PREDECESSOR) != 0u ? dev->num_sms : 0;
+  p.long_splits = (flags & DSA_DECODE_LONG_SPLITS) != 0u ? 1 : 0;
   plan_mla_decode_tc(p);
   const size_t need = mla_decode_tc_workspace_bytes(rows->rows, heads, topk);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))

@@ -170,8 +170,10 @@ struct DecodeParams {
   float kv_scale;
   float sm_scale;
   int32_t q_early;     // CTAs (in launch order) that load q before the dependency wait
+  int32_t long_splits; // caller's choice: 512-entry splits at up to 64 heads (set before planning)
 };
-// Split count / length of the gather-attend (a function of topk only).
+// Split count / length of the gather-attend (a function of topk, heads and
+// long_splits only).
 void plan_mla_decode_tc(DecodeParams& p);
 size_t mla_decode_tc_workspace_bytes(int32_t rows, int32_t heads, int32_t topk);
 void mla_decode_tc_bind_workspace(DecodeParams& p, void* workspace);

@@ -9,9 +9,10 @@
 // head:  z_j = sm_scale * kv_scale * (Q . e4m3(latent_j)),  p = softmax(z),
 //        out = kv_scale * sum_j p_j e4m3(latent_j),  lse = log sum_j exp(z_j).
 //
-// A row's selection is cut into n splits of at most 256 entries (2048 with
-// more than 64 heads); n depends on topk and heads only, never on the number
-// of rows, so a row's arithmetic is the same in any launch.  One CTA (20
+// A row's selection is cut into n splits of at most 256 entries (512 when
+// the caller asks for long splits, 2048 with more than 64 heads); n depends
+// on topk, heads and that choice only, never on the number of rows, so a
+// row's arithmetic is the same in any launch.  One CTA (20
 // warps) runs one split of one (row, 64-head group) as a pipeline over
 // 128-entry tiles:
 //   - the latent stays FP8: TMA tile::gather4 copies the selected 512-byte
@@ -65,6 +66,7 @@ constexpr int kHeads = 64;             // heads per CTA
 constexpr int kHpt = 16;               // heads per softmax thread (one token each)
 constexpr int kTok = 128;              // entries per tile (MMA M of S^T)
 constexpr int kTilesPerSplit = 2;      // split length target (tiles), up to 64 heads
+constexpr int kTilesPerSplitLong = 4;  // the same with the caller's long-splits flag
 constexpr int kTilesPerSplitWide = 16; // the same with more than 64 heads (two head-group CTAs)
 constexpr int kMaxTiles = 16;          // tiles per split the CTA can hold slots for
 constexpr int kMergeThreads = 128;     // merge kernel: one CTA per (row, head), 4 dims per thread
@@ -846,7 +848,8 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
 void plan_mla_decode_tc(DecodeParams& p) {
   // A function of topk and heads only, so a row's arithmetic does not depend
   // on the other rows of the launch.
-  const int target = (p.heads > kHeads ? kTilesPerSplitWide : kTilesPerSplit) * kTok;
+  const int target = (p.heads > kHeads ? kTilesPerSplitWide
+                                       : (p.long_splits ? kTilesPerSplitLong : kTilesPerSplit)) * kTok;
   int n = (p.topk + target - 1) / target;
   if (n < 1) n = 1;
   p.splits = n;

@@ -104,11 +104,13 @@ class DeviceWorkload:
     def mla_decode(self, stream=None, q_early: bool = False):
         """S3.  ``q_early``: the call follows this workload's top-k on the same
         stream (Q was uploaded before the step), so the attend may convert Q
-        before its dependency wait."""
+        before its dependency wait.  The split plan is the workload's
+        (``long_splits``)."""
         wl = self.wl
         out = self.out if self.out_target is None else self.out_target
         api.dsa_mla_decode_fp8(self.rows, self.Q, self.pool, self.sel, wl.topk, wl.kv_scale,
-                               wl.sm_scale, out, self.lse, self.workspace, stream, q_early=q_early)
+                               wl.sm_scale, out, self.lse, self.workspace, stream, q_early=q_early,
+                               long_splits=wl.long_splits)
 
     def step(self, stream=None):
         """One pass of the whole hot path (S0 when the workload writes, S1-S3)."""

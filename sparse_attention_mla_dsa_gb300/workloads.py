@@ -23,6 +23,12 @@ prefill    1 seq x 1024 rows (a 9,000-token prompt's last 1,024 positions, lens
            7977..9000), 64 heads, index 32x128, topk 2048
 =========  =====================================================================
 
+batched, verify and prefill run the gather-attend with its long-split plan
+(512-entry splits: half the CTAs of the 256-entry plan, for launches with many
+rows); single, tiny and long (128 heads: one 2048-entry split per 64-head
+group either way) keep the default.  ``select_rows`` keeps the parent's plan,
+so rows run one at a time are bit-identical to the same rows run together.
+
 Value distributions: latent ~ N(0,1) stored as fp8(x / kv_scale) with
 kv_scale 0.02; keys ~ N(0,1) bf16; q_idx ~ N(0,1) fp32; w ~ N(0,1) * Hi^-0.5;
 gate = sigmoid(N(0,1)) bf16; Q ~ 0.05 * N(0,1) bf16; kv_a ~ N(0,1) bf16;
@@ -76,6 +82,7 @@ class Workload:
     Q: np.ndarray              # [R, H, 512] uint16 bf16 bits
     kv_a: np.ndarray | None    # [R, 512] uint16 bf16 bits (rows written by the latent write)
     norm_w: np.ndarray | None  # [512] uint16 bf16 bits
+    long_splits: bool = False  # the gather-attend's 512-entry split plan (many-row launches)
 
     @property
     def max_len(self) -> int:
@@ -122,7 +129,7 @@ def make_workload(name: str, seed: int, *, seqs: int, rows_per_seq: int, len_kin
                   free_fraction: float = 0.0, shuffle_blocks: bool = True,
                   with_write: bool = False, kv_scale: float = 0.02,
                   sm_scale: float = 256 ** -0.5, eps: float = 1e-6,
-                  shared_table: bool = False, lens=None) -> Workload:
+                  shared_table: bool = False, lens=None, long_splits: bool = False) -> Workload:
     """Draw one workload.  ``len_kind``: 'fixed' (len_lo), 'uniform' (integers
     in [len_lo, len_hi]) or 'loguniform' (exp of uniform in [ln lo, ln hi],
     floored).  A sequence's rows have lens base, base+1, ... (K-token verify).
@@ -221,7 +228,7 @@ def make_workload(name: str, seed: int, *, seqs: int, rows_per_seq: int, len_kin
                     kv_scale=kv_scale, sm_scale=sm_scale, eps=eps, seq_lens=seq_lens,
                     positions=positions, slots=slots, block_table=block_table, pool=pool,
                     idx_k=idx_k, idx_gate=idx_gate, idx_base=idx_base, q_idx=q_idx,
-                    head_w=head_w, Q=Q, kv_a=kv_a, norm_w=norm_w)
+                    head_w=head_w, Q=Q, kv_a=kv_a, norm_w=norm_w, long_splits=long_splits)
 
 
 # The five named workloads, each with a scale-down factor for parity cases the
@@ -233,9 +240,11 @@ NAMED = {
                    len_hi=32768, heads=64, index_heads=32, index_dim=128, topk=2048,
                    pool_blocks=1024),
     "batched": dict(seed=2, seqs=32, rows_per_seq=1, len_kind="uniform", len_lo=8192,
-                    len_hi=65536, heads=64, index_heads=32, index_dim=128, topk=2048),
+                    len_hi=65536, heads=64, index_heads=32, index_dim=128, topk=2048,
+                    long_splits=True),
     "verify": dict(seed=3, seqs=8, rows_per_seq=4, len_kind="uniform", len_lo=65536,
-                   len_hi=131072, heads=64, index_heads=32, index_dim=128, topk=2048),
+                   len_hi=131072, heads=64, index_heads=32, index_dim=128, topk=2048,
+                   long_splits=True),
     "long": dict(seed=4, seqs=64, rows_per_seq=1, len_kind="loguniform", len_lo=4096,
                  len_hi=131072, heads=128, index_heads=64, index_dim=128, topk=2048,
                  free_fraction=0.5, with_write=True),
@@ -244,7 +253,8 @@ NAMED = {
     # causal horizon): the last 1,024 tokens of a 9,000-token prompt as query
     # rows of one sequence, row j seeing tokens [0, 7977 + j).
     "prefill": dict(seed=7, seqs=1, rows_per_seq=1024, len_kind="fixed", len_lo=7977,
-                    len_hi=7977, heads=64, index_heads=32, index_dim=128, topk=2048),
+                    len_hi=7977, heads=64, index_heads=32, index_dim=128, topk=2048,
+                    long_splits=True),
 }
 
 

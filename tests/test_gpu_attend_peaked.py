@@ -8,8 +8,9 @@ deviation ~7, one dominant token per head, logits that climb tile after tile
 (the running maximum moves in every tile, forcing the in-TMEM rescale of O),
 flat and peaked heads side by side in one CTA, and a selection whose later
 splits all weigh far below the first split (the merge).  Each runs at 16, 64
-(eight 256-entry splits per row) and 128 heads (one 2048-entry split per
-64-head group), through the whole path (index, top-k, attend) on the GPU, and
+(eight 256-entry splits per row; four 512-entry splits with the long-split
+plan) and 128 heads (one 2048-entry split per 64-head group), through the
+whole path (index, top-k, attend) on the GPU, and
 the attend is compared with the oracle on the GPU's own selection under the
 numerics-derived bounds of ``tests/parity.py``.
 
@@ -17,6 +18,8 @@ The bounds are themselves checked: the same GPU output compared with an
 oracle whose softmax scale is off by 10 % must fail them, on a peaked row and
 on a flat one.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -37,11 +40,13 @@ def dsa():
     return api, path
 
 
-CASES = ([(k, h, 2048) for k in workloads.ATTEND_KINDS for h in (64, 128)]
-         + [("sharp", 64, 2000),        # 48 padding entries in the last tile
-            ("dominant", 16, 2048),
-            ("rising", 16, 2048),
-            ("sharp", 64, 8192)])       # a real top-k of 2048 out of 8192
+CASES = ([(k, h, 2048, False) for k in workloads.ATTEND_KINDS for h in (64, 128)]
+         + [(k, 64, 2048, True) for k in workloads.ATTEND_KINDS]   # 512-entry splits
+         + [("sharp", 64, 2000, False),        # 48 padding entries in the last tile
+            ("sharp", 64, 2000, True),
+            ("dominant", 16, 2048, False),
+            ("rising", 16, 2048, False),
+            ("sharp", 64, 8192, False)])       # a real top-k of 2048 out of 8192
 
 
 def _run(api, path, wl):
@@ -53,10 +58,11 @@ def _run(api, path, wl):
     return dw
 
 
-@pytest.mark.parametrize("kind,heads,length", CASES)
-def test_attend_peaked_rows(dsa, oracle, kind, heads, length):
+@pytest.mark.parametrize("kind,heads,length,long_splits", CASES)
+def test_attend_peaked_rows(dsa, oracle, kind, heads, length, long_splits):
     api, path = dsa
-    wl = workloads.attend_case(kind, heads=heads, length=length)
+    wl = dataclasses.replace(workloads.attend_case(kind, heads=heads, length=length),
+                             long_splits=long_splits)
     dw = _run(api, path, wl)
     L = int(wl.seq_lens[0])
     scores = dw.scores.cpu().numpy()[0, :L]

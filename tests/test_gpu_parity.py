@@ -296,7 +296,7 @@ def test_q_before_predecessor_flag_is_bit_identical(dsa):
                                    dw.pool.shape[0], dw.sel.data_ptr(), wl.topk, wl.heads, 512,
                                    wl.kv_scale, wl.sm_scale, dw.out.data_ptr(), None,
                                    dw.workspace.data_ptr(),
-                                   dw.workspace.numel() * dw.workspace.element_size(), 2, None)
+                                   dw.workspace.numel() * dw.workspace.element_size(), 4, None)
     assert st == 1                                  # DSA_ERR_INVALID_ARG, nothing launched
 
 
