@@ -1,9 +1,11 @@
 """The host-facing decoder: pinned host inputs in, attention output out.
 
-DsaDecoder replays one captured CUDA graph per cache replica (host-to-device
-copies, the four calls, device-to-host copy).  Each replay must move the
-pinned buffers' current contents: two steps with different staged queries
-must each equal, bit for bit, an eager run of the same inputs.
+DsaDecoder replays one captured CUDA graph per cache replica (the host-to-device
+copy of the staged inputs, the four calls; the output lands in pinned host
+memory).  Each replay must move the pinned buffers' current contents: steps
+with different staged queries must each equal, bit for bit, an eager run of
+the same inputs, with one replica and with two; steps launched back to back
+over three replicas end with the same output as an eager run.
 """
 import dataclasses
 
@@ -26,12 +28,13 @@ def dsa():
     return api, path
 
 
-def test_graph_decoder_moves_current_inputs(dsa):
+@pytest.mark.parametrize("replicas", [1, 2])
+def test_graph_decoder_moves_current_inputs(dsa, replicas):
     api, path = dsa
     wl = workloads.scaled("batched", seqs=3, len_div=16)
-    dec = path.DsaDecoder(wl, "cuda", replicas=1, graphs=True)
+    dec = path.DsaDecoder(wl, "cuda", replicas=replicas, graphs=True)
     rng = np.random.default_rng(5)
-    for step in range(3):                 # eager capture run, then two replays
+    for step in range(2 * replicas + 1):  # eager capture runs, then replays
         q = workloads._bf16_bits(np.float32(0.05) * rng.standard_normal(wl.Q.shape,
                                                                         dtype=np.float32))
         cur = dataclasses.replace(wl, Q=q)
@@ -43,6 +46,23 @@ def test_graph_decoder_moves_current_inputs(dsa):
         ref.step()
         torch.cuda.synchronize()
         assert torch.equal(got, ref.out.cpu()), f"step {step}"
+    assert api.dsa_get_error(reset=True)[0] == 0
+
+
+def test_graph_decoder_back_to_back_steps(dsa):
+    # Seven steps over three replicas with no synchronise between them: the
+    # output equals an eager run.
+    api, path = dsa
+    wl = workloads.scaled("single", len_div=8)
+    dec = path.DsaDecoder(wl, "cuda", replicas=3, graphs=True)
+    dec.stage(wl)
+    for _ in range(7):
+        out = dec.decode()
+    torch.cuda.synchronize()
+    ref = path.DeviceWorkload(wl)
+    ref.step()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref.out.cpu())
     assert api.dsa_get_error(reset=True)[0] == 0
 
 
