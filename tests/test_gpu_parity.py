@@ -134,10 +134,12 @@ def test_many_head_groups_with_write(dsa, oracle):
     check_path(oracle, api, path, wl)
 
 
-def test_k_row_verify_bit_identical_to_serial(dsa, oracle):
-    """decode_k: a K-row verify launch equals K single-row launches bit for bit."""
+@pytest.mark.parametrize("long_splits", [True, False])
+def test_k_row_verify_bit_identical_to_serial(dsa, oracle, long_splits):
+    """decode_k: a K-row verify launch equals K single-row launches bit for bit,
+    under either split plan of the gather-attend (both sides use the same)."""
     api, path = dsa
-    wl = workloads.scaled("verify", seqs=2, len_div=32)
+    wl = workloads.scaled("verify", seqs=2, len_div=32, long_splits=long_splits)
     batch = path.DeviceWorkload(wl)
     batch.step()
     torch.cuda.synchronize()
