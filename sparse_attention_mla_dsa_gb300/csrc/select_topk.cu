@@ -20,12 +20,12 @@
 // the writes inside it.
 //
 // The cluster size follows the row length (about 4k keys per CTA).  When the
-// launch would then need more CTAs than there are SMs and fewer CTAs per row
-// still keep their slices in shared memory with two CTAs per SM, the cluster
-// is cut to one CTA per SM (32 rows of 64k: four CTAs each), else to what one
-// wave of two CTAs per SM holds, down to one CTA per row (many short rows: a
-// prefill).  The selection is exact, so the cluster size never changes a
-// result.
+// launch would then need more CTAs than there are SMs, the cluster is cut to
+// one CTA per SM if the longer slices still fit in shared memory (32 rows of
+// 64k or 128k: four CTAs each), else to what one wave of two CTAs per SM
+// holds if the slices fit two per SM, down to one CTA per row (many short
+// rows: a prefill).  The selection is exact, so the cluster size never
+// changes a result.
 #include "dsa_device.cuh"
 #include "dsa_internal.h"
 
@@ -38,6 +38,7 @@ constexpr int kBins = 256;             // 8-bit digits
 constexpr int kItems = 8;              // consecutive tokens per thread in the output pass
 constexpr int kKeysPerCta = 4096;      // target keys per CTA when choosing the cluster size
 constexpr size_t kTwoPerSmBytes = 112 * 1024;  // shared memory that leaves room for two CTAs per SM
+constexpr size_t kOnePerSmBytes = 227 * 1024;  // the most one CTA may have
 
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -346,13 +347,14 @@ int topk_cluster_size(int32_t max_len, int32_t rows, int num_sms) {
   int c = (max_len + kKeysPerCta - 1) / kKeysPerCta;
   c = c < 1 ? 1 : (c > 8 ? 8 : c);
   // One CTA per SM first (clusters then pack into the GPCs without a
-  // straggler wave), else two.
+  // straggler wave; a slice may then take up to a whole SM's shared memory),
+  // else two.
   const long long sms = num_sms > 0 ? num_sms : 1;
   for (long long slots = sms; slots <= 2 * sms; slots += sms) {
     if (static_cast<long long>(rows) * c <= slots) break;
     const long long fit = slots / (rows > 0 ? rows : 1);
     const int cut = static_cast<int>(fit < 1 ? 1 : fit);
-    if (cut < c && topk_smem_bytes(max_len, cut) <= kTwoPerSmBytes) {
+    if (cut < c && topk_smem_bytes(max_len, cut) <= (slots == sms ? kOnePerSmBytes : kTwoPerSmBytes)) {
       c = cut;
       break;
     }

@@ -5,7 +5,7 @@ clusters of five and eight CTAs per row, against the oracle's full-sort selectio
 score DESC, then index ASC).  Bit-exact: the selection is integer work.
 
 Launches with more rows than one wave of clusters holds take smaller clusters
-where the slices still fit in shared memory (four, seven, one CTA per row); with long
+where the slices still fit in shared memory (four, three, one CTA per row); with long
 rows they keep eight CTAs over two waves.  Those launches are checked the same
 way.
 """
@@ -42,7 +42,7 @@ def _patterns(rng, n):
     (270000, [33000, 140000, 270000]),                 # eight CTAs, 34k keys each
     # 32 rows of 64k: clusters cut from eight to four CTAs (one per SM)
     (65536, [65536, 2049, 40000] + [2200 + 1999 * i for i in range(29)]),
-    # 40 rows of 64k: clusters cut from eight to seven CTAs (one wave)
+    # 40 rows of 64k: clusters cut from eight to three CTAs (one per SM)
     (65536, [2049, 65536, 40000] + [2100 + 97 * i for i in range(37)]),
     # 64 rows of 128k: eight CTAs per row over two waves (four would not fit)
     (131072, [2049, 131072, 70000, 99999] + [2100 + 37 * i for i in range(60)]),
