@@ -296,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_map(&kmap);
     // (With inputs_early the loads themselves go out right after the barrier
-    // below, so the prefetch and the load of the base it needs are skipped.)
+    // below; thread 0's prefetch still starts the first tiles' DRAM reads a
+    // little sooner, which measured faster than skipping it.)
     if (kDirect || groups == 1) {
       const long long tg = (p.max_len + kTileM - 1) / kTileM;
       const long long b0 = kDirect ? static_cast<long long>(blockIdx.x) * p.direct_tiles : tg * c / ctas;

@@ -846,8 +846,8 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
 }  // namespace
 
 void plan_mla_decode_tc(DecodeParams& p) {
-  // A function of topk and heads only, so a row's arithmetic does not depend
-  // on the other rows of the launch.
+  // A function of topk, heads and the caller's long-splits choice only, so a
+  // row's arithmetic does not depend on the other rows of the launch.
   const int target = (p.heads > kHeads ? kTilesPerSplitWide
                                        : (p.long_splits ? kTilesPerSplitLong : kTilesPerSplit)) * kTok;
   int n = (p.topk + target - 1) / target;
