@@ -272,6 +272,7 @@ dsa_status dsa_mla_decode_fp8_ex(const dsa_rows* rows, const uint16_t* q, const 
   // the selection loaded together after the wait) is the faster one.
   p.q_early = (flags & DSA_DECODE_Q_BEFORE_PREDECESSOR) != 0u ? dev->num_sms : 0;
   p.long_splits = (flags & DSA_DECODE_LONG_SPLITS) != 0u ? 1 : 0;
+  p.num_sms = dev->num_sms;
   plan_mla_decode_tc(p);
   const size_t need = mla_decode_tc_workspace_bytes(rows->rows, heads, topk);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))

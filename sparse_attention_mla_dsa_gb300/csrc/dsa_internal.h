@@ -171,6 +171,7 @@ struct DecodeParams {
   float sm_scale;
   int32_t q_early;     // CTAs (in launch order) that load q before the dependency wait
   int32_t long_splits; // caller's choice: 512-entry splits at up to 64 heads (set before planning)
+  int32_t num_sms;     // SMs of the device (the merge kernel's launch shape only)
 };
 // Split count / length of the gather-attend (a function of topk, heads and
 // long_splits only).

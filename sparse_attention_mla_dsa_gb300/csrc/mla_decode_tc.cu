@@ -69,7 +69,8 @@ constexpr int kTilesPerSplit = 2;      // split length target (tiles), up to 64 
 constexpr int kTilesPerSplitLong = 4;  // the same with the caller's long-splits flag
 constexpr int kTilesPerSplitWide = 16; // the same with more than 64 heads (two head-group CTAs)
 constexpr int kMaxTiles = 16;          // tiles per split the CTA can hold slots for
-constexpr int kMergeThreads = 128;     // merge kernel: one CTA per (row, head), 4 dims per thread
+constexpr int kMergeHeads = 4;         // merge kernel: heads per CTA for many rows (64 threads a head)
+constexpr int kMergeThreads = 64 * kMergeHeads;
 constexpr float kPMaxLog2 = 8.75f;     // p = 2^(z - m) stays below 2^8.75 < 448
 constexpr float kPResetLog2 = 8.0f;    // a reset maps the tile maximum to p = 2^8
 constexpr uint32_t kSub = kTok * 128;              // one 128-dim column block: 128 rows x 128 B
@@ -748,23 +749,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // One split's share of a merged (row, head): weight w = l * 2^(m - mmax) on
-// the split's O / l (four fp16 values).
-__device__ __forceinline__ void accumulate_split(float2 ml, uint2 v, float mmax, float& lsum,
-                                                 float4& acc) {
+// the split's O / l (eight fp16 values).
+__device__ __forceinline__ void accumulate_split(float2 ml, uint4 v, float mmax, float& lsum,
+                                                 float (&acc)[8]) {
   const float w = ml.y * exp2f(ml.x - mmax);
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  const uint32_t h[4] = {v.x, v.y, v.z, v.w};
   lsum += w;
-  acc.x += a.x * w;
-  acc.y += a.y * w;
-  acc.z += b.x * w;
-  acc.w += b.y * w;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h[k]));
+    acc[2 * k] += a.x * w;
+    acc[2 * k + 1] += a.y * w;
+  }
 }
 
-// Merge of the n splits of one (row, head): 128 threads, 4 dims each, splits
-// in fixed order; the consumed partial lines are discarded from L2.
+// Merge of the n splits of (row, head): blockDim.x / 64 heads per CTA (one
+// for a few rows, four for many), 64 threads a head and 8 dims a thread,
+// splits in fixed order; the consumed partial lines are discarded from L2.
+// The arithmetic of an element does not depend on the mapping.
 __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const DecodeParams p) {
-  const int h = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+  const int tid = threadIdx.x, d8 = tid % 64;
+  const int h = blockIdx.x * (blockDim.x / 64) + tid / 64, r = blockIdx.y;
   const int groups = (p.heads + kHeads - 1) / kHeads;
   const int hg = h / kHeads, hl = h % kHeads;
   const int nsplit = p.splits;
@@ -776,21 +781,25 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
   // this merge finish.
   grid_dep_launch();
   grid_dep_wait();  // the partials come from the kernel before
+  if (h >= p.heads) return;  // (heads is a multiple of 16: never)
   float mmax = -INFINITY;
   float lsum = 0.0f;
-  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+  auto row_of = [&](int u) {
+    return reinterpret_cast<const uint4*>(p.part_o + ((base + u) * kHeads + hl) * 512) + d8;
+  };
   if (nsplit <= 8) {
     // Every split's (max, sum) and partial row in flight at once: one round trip.
     float2 mlc[8];
-    uint2 vc[8];
+    uint4 vc[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (u < nsplit) {
         mlc[u] = ld_dep_f2(ml + (base + u) * kHeads + hl);
-        vc[u] = ld_dep_u2(reinterpret_cast<const uint2*>(p.part_o + ((base + u) * kHeads + hl) * 512) + tid);
+        vc[u] = ld_dep_u4(row_of(u));
       } else {
         mlc[u] = make_float2(-INFINITY, 0.0f);
-        vc[u] = make_uint2(0u, 0u);
+        vc[u] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
 #pragma unroll
@@ -813,12 +822,12 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
     if (mmax != -INFINITY) {
       for (int c0 = 0; c0 < nsplit; c0 += 8) {
         float2 mlc[8];
-        uint2 vc[8];
+        uint4 vc[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           if (c0 + u < nsplit) {
             mlc[u] = ld_dep_f2(ml + (base + c0 + u) * kHeads + hl);
-            vc[u] = ld_dep_u2(reinterpret_cast<const uint2*>(p.part_o + ((base + c0 + u) * kHeads + hl) * 512) + tid);
+            vc[u] = ld_dep_u4(row_of(c0 + u));
           }
         }
 #pragma unroll
@@ -828,19 +837,25 @@ __global__ void __launch_bounds__(kMergeThreads) mla_decode_merge_kernel(const D
     }
   }
   const float scale = (mmax != -INFINITY && lsum > 0.0f) ? p.kv_scale / lsum : 0.0f;
-  uint2 packed;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.x) : "f"(acc.y * scale), "f"(acc.x * scale));
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed.y) : "f"(acc.w * scale), "f"(acc.z * scale));
+  uint32_t packed[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+        : "=r"(packed[k])
+        : "f"(acc[2 * k + 1] * scale), "f"(acc[2 * k] * scale));
   const int64_t head = static_cast<int64_t>(r) * p.heads + h;
-  reinterpret_cast<uint2*>(p.out + head * 512)[tid] = packed;
-  if (tid == 0 && p.lse != nullptr)
+  // Two 8-byte stores (out is only required to be 8-byte aligned).
+  uint2* o2 = reinterpret_cast<uint2*>(p.out + head * 512 + d8 * 8);
+  o2[0] = make_uint2(packed[0], packed[1]);
+  o2[1] = make_uint2(packed[2], packed[3]);
+  if (d8 == 0 && p.lse != nullptr)
     p.lse[head] = mmax != -INFINITY ? (mmax + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
   // Every lane has used its partial values: drop the consumed 128-byte lines
-  // (16 lanes share one) from L2 instead of writing them back.
+  // (eight lanes of one warp share one) from L2 instead of writing them back.
   __syncwarp();
-  if ((tid & 15) == 0)
+  if ((d8 & 7) == 0)
     for (int c = 0; c < nsplit; ++c)
-      discard_l2_line(p.part_o + ((base + c) * kHeads + hl) * 512 + tid * 4);
+      discard_l2_line(p.part_o + ((base + c) * kHeads + hl) * 512 + d8 * 8);
 }
 
 }  // namespace
@@ -897,8 +912,11 @@ cudaError_t launch_mla_decode_tc(const DecodeParams& p, const CUtensorMap& pmap,
   e = cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, pmap, p);
   if (e != cudaSuccess || p.splits == 1) return e;
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(p.heads, p.rows.rows, 1);
-  mcfg.blockDim = dim3(kMergeThreads, 1, 1);
+  // One head per CTA while that gives fewer than four CTAs per SM (a single
+  // row: the most SMs), four per CTA beyond.
+  const int hpc = static_cast<int64_t>(p.rows.rows) * p.heads >= 4LL * p.num_sms ? kMergeHeads : 1;
+  mcfg.gridDim = dim3((p.heads + hpc - 1) / hpc, p.rows.rows, 1);
+  mcfg.blockDim = dim3(64 * hpc, 1, 1);
   mcfg.stream = stream;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;
