@@ -248,6 +248,50 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
   const uint32_t thresh = prefix;
   const int take_equal = remaining;  // >= 1, counted over the whole row
 
+  // ---- one chunk a slice (every CTA of the cluster: the slice length is
+  // uniform) with every key at the threshold prefix taken: the output's own
+  // scan of the take bits gives this CTA's count too, so the count pass and
+  // its scan are skipped.  The exchange and the barriers are those of the
+  // general path below.
+  if (C > 1 && all_taken && per <= kThreads * kItems) {
+    const int t0 = tid * kItems;
+    uint32_t kv[kItems];
+    if (t0 + kItems <= n) {
+      const uint4 u0 = *reinterpret_cast<const uint4*>(keys + t0);
+      const uint4 u1 = *reinterpret_cast<const uint4*>(keys + t0 + 4);
+      kv[0] = u0.x; kv[1] = u0.y; kv[2] = u0.z; kv[3] = u0.w;
+      kv[4] = u1.x; kv[5] = u1.y; kv[6] = u1.z; kv[7] = u1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < kItems; ++i) kv[i] = t0 + i < n ? keys[t0 + i] : 0u;
+    }
+    uint32_t take = 0;
+#pragma unroll
+    for (int i = 0; i < kItems; ++i)
+      if (t0 + i < n) take |= static_cast<uint32_t>((kv[i] & prefix_mask) >= thresh) << i;
+    int total;
+    int pos = block_excl_scan(__popc(take), sh.warp_tot, total);
+    if (tid == 0) {
+      sh.counts[0] = total;
+      sh.counts[1] = 0;
+    }
+    cluster_sync();
+    int2 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (c < static_cast<int>(crank)) v[c] = ld_remote_s32x2(remote_addr(&sh.counts[0], c));
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (c < static_cast<int>(crank)) pos += v[c].x;
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < kItems; ++i)
+      if ((take >> i) & 1u) out[pos++] = lo + t0 + i;
+    for (int i = want + crank * kThreads + tid; i < p.topk; i += C * kThreads) out[i] = -1;
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    return;
+  }
+
   // ---- this CTA's counts, then its offsets from the CTAs before it.  When
   // every key at the threshold prefix is taken a key is selected iff its
   // masked bits are >= the prefix (one count, one scan per chunk); otherwise
