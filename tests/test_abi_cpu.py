@@ -109,3 +109,21 @@ def test_dense_mm_split_plan_host_arithmetic():
         per = (kblocks + s - 1) // s
         assert s >= 1 and (s - 1) * per < kblocks          # no empty range
         assert s == 1 or per >= 4                           # at least four blocks each
+
+
+def test_attend_flags_match_the_header_and_unknown_bits_are_refused():
+    # The binding's flag values are the header's; a call with a bit the
+    # library does not know is refused before any CUDA call.
+    from sparse_attention_mla_dsa_gb300 import api, build
+    hdr = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    for name in ("DSA_DECODE_Q_BEFORE_PREDECESSOR", "DSA_DECODE_LONG_SPLITS"):
+        value = int(re.search(r"#define %s (\d+)u" % name, hdr).group(1))
+        assert getattr(api, name) == value
+    lib = ctypes.CDLL(build.build())
+    f = lib.dsa_mla_decode_fp8_ex
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    f.argtypes = [P, P, P, i64, P, i32, i32, i32, f32, f32, P, P, P, ctypes.c_size_t,
+                  ctypes.c_uint32, P]
+    f.restype = ctypes.c_int
+    x = 1 << 20
+    assert f(x, x, x, 64, x, 2048, 64, 512, 0.02, 0.0625, x, None, x, 1 << 20, 4, None) == 1
