@@ -37,6 +37,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;             // 8-bit digits
 constexpr int kItems = 8;              // consecutive tokens per thread in the output pass
 constexpr int kKeysPerCta = 4096;      // target keys per CTA when choosing the cluster size
+constexpr int kFastChunks = 4;         // output chunks a slice may have for the count-free path
 constexpr size_t kTwoPerSmBytes = 112 * 1024;  // shared memory that leaves room for two CTAs per SM
 constexpr size_t kOnePerSmBytes = 227 * 1024;  // the most one CTA may have
 
@@ -248,31 +249,43 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
   const uint32_t thresh = prefix;
   const int take_equal = remaining;  // >= 1, counted over the whole row
 
-  // ---- one chunk a slice (every CTA of the cluster: the slice length is
-  // uniform) with every key at the threshold prefix taken: the output's own
-  // scan of the take bits gives this CTA's count too, so the count pass and
-  // its scan are skipped.  The exchange and the barriers are those of the
-  // general path below.
-  if (C > 1 && all_taken && per <= kThreads * kItems) {
-    const int t0 = tid * kItems;
-    uint32_t kv[kItems];
-    if (t0 + kItems <= n) {
-      const uint4 u0 = *reinterpret_cast<const uint4*>(keys + t0);
-      const uint4 u1 = *reinterpret_cast<const uint4*>(keys + t0 + 4);
-      kv[0] = u0.x; kv[1] = u0.y; kv[2] = u0.z; kv[3] = u0.w;
-      kv[4] = u1.x; kv[5] = u1.y; kv[6] = u1.z; kv[7] = u1.w;
-    } else {
+  // ---- up to kFastChunks output chunks a slice (every CTA of the cluster:
+  // the slice length is uniform) with every key at the threshold prefix
+  // taken: the output's own scans of the take bits give this CTA's count
+  // too, so the count pass and its scan are skipped; the take bits wait in
+  // registers for the exchange.  The exchange and the barriers are those of
+  // the general path below.
+  if (C > 1 && all_taken && per <= kFastChunks * kThreads * kItems) {
+    uint32_t take[kFastChunks];
+    int pos[kFastChunks];
+    int count = 0;
 #pragma unroll
-      for (int i = 0; i < kItems; ++i) kv[i] = t0 + i < n ? keys[t0 + i] : 0u;
+    for (int k = 0; k < kFastChunks; ++k) {
+      take[k] = 0;
+      pos[k] = 0;
+      const int c0 = k * kThreads * kItems;
+      if (c0 < n) {  // (uniform over the CTA)
+        const int t0 = c0 + tid * kItems;
+        uint32_t kv[kItems];
+        if (t0 + kItems <= n) {
+          const uint4 u0 = *reinterpret_cast<const uint4*>(keys + t0);
+          const uint4 u1 = *reinterpret_cast<const uint4*>(keys + t0 + 4);
+          kv[0] = u0.x; kv[1] = u0.y; kv[2] = u0.z; kv[3] = u0.w;
+          kv[4] = u1.x; kv[5] = u1.y; kv[6] = u1.z; kv[7] = u1.w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < kItems; ++i) kv[i] = t0 + i < n ? keys[t0 + i] : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < kItems; ++i)
+          if (t0 + i < n) take[k] |= static_cast<uint32_t>((kv[i] & prefix_mask) >= thresh) << i;
+        int chunk_total;
+        pos[k] = count + block_excl_scan(__popc(take[k]), sh.warp_tot, chunk_total);
+        count += chunk_total;
+      }
     }
-    uint32_t take = 0;
-#pragma unroll
-    for (int i = 0; i < kItems; ++i)
-      if (t0 + i < n) take |= static_cast<uint32_t>((kv[i] & prefix_mask) >= thresh) << i;
-    int total;
-    int pos = block_excl_scan(__popc(take), sh.warp_tot, total);
     if (tid == 0) {
-      sh.counts[0] = total;
+      sh.counts[0] = count;
       sh.counts[1] = 0;
     }
     cluster_sync();
@@ -280,13 +293,19 @@ __global__ void __launch_bounds__(kThreads, 2) select_topk_kernel(const TopkPara
 #pragma unroll
     for (int c = 0; c < 8; ++c)
       if (c < static_cast<int>(crank)) v[c] = ld_remote_s32x2(remote_addr(&sh.counts[0], c));
+    int base = 0;
 #pragma unroll
     for (int c = 0; c < 8; ++c)
-      if (c < static_cast<int>(crank)) pos += v[c].x;
+      if (c < static_cast<int>(crank)) base += v[c].x;
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < kItems; ++i)
-      if ((take >> i) & 1u) out[pos++] = lo + t0 + i;
+    for (int k = 0; k < kFastChunks; ++k) {
+      int q = base + pos[k];
+      const int t0 = k * kThreads * kItems + tid * kItems;
+#pragma unroll
+      for (int i = 0; i < kItems; ++i)
+        if ((take[k] >> i) & 1u) out[q++] = lo + t0 + i;
+    }
     for (int i = want + crank * kThreads + tid; i < p.topk; i += C * kThreads) out[i] = -1;
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     return;
