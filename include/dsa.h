@@ -203,9 +203,11 @@ dsa_status dsa_select_topk(const dsa_rows *rows, const float *scores, int32_t ma
  * space (cudaHostAlloc memory under unified addressing): the kernels store the
  * result there directly, with no separate device-to-host copy.
  * latent_dim must be 512; heads a multiple of 16; nslots below 2^31
- * (DSA_ERR_UNSUPPORTED otherwise).  Numerics: the logits are the exact
- * products of the bf16 q and the E4M3 latent accumulated in FP32 on the
- * tensor cores; the softmax weights enter the weighted sum as two E4M3 terms
+ * (DSA_ERR_UNSUPPORTED otherwise).  Numerics: q enters the tensor cores as
+ * two E4M3 terms per element (hi and the residual, scaled by a power of two
+ * per head), which hold a bf16 q exactly except elements more than 2^10
+ * below the head's largest |q|, whose last bits fall into E4M3 subnormals;
+ * their products with the E4M3 latent accumulate in FP32; the softmax weights enter the weighted sum as two E4M3 terms
  * (about bf16 precision; weights 2^18 below a head's largest drop out), the
  * normalising sums and lse use the unrounded weights.  A row's selection is
  * cut into splits of at most 256 entries (2048 with more than 64 heads; 512
